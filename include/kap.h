@@ -1,0 +1,198 @@
+/*
+ * kap.h - C ABI of the selected-KV sparse decode hot path (GB300, sm_103a).
+ *
+ * The operations follow the runtime access plan A = (U, M, pos, rho_access, rho_verify) of
+ * "KAP: Bridging the Knowledge Selection-Runtime Consumption Gap in LLM Systems" (the arXiv paper and
+ * its agifrontier.github.io tutorial, section on the runtime access plan):
+ *   U           - units: KV pages (16 tokens) or token spans,
+ *   M           - page map: block table from logical page to physical page, plus lengths,
+ *   pos         - logical positions, kept on both the proposal and the verification path,
+ *   rho_access  - sparse-access policy: the A<a>R<r>K<k> split of the KRI page (knlp.io, "The A<a>R<r>K<k> tag"),
+ *   rho_verify  - verification policy: the short causal query window of the full-context verifier.
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument named *_dev, and every pointer inside the structs below, is DEVICE memory owned by
+ *     the caller. The library never allocates, frees or synchronises on these calls; all launches go to `stream`
+ *     (NULL = the legacy default stream), so every call can be captured in a CUDA graph.
+ *   - KV pool layout: K and V are separate arrays [num_pages][num_kv_heads][16][head_dim] of the pool dtype.
+ *     One (page, head) chunk is 16*head_dim*elem bytes and contiguous.
+ *   - Query head hq reads KV head hq / (num_q_heads / num_kv_heads) (grouped-query attention).
+ *   - Attention logits are (q . k) / sqrt(head_dim); lse is the natural-log log-sum-exp of those logits (fp32).
+ *   - K in the pool is post-RoPE; queries passed to attention are post-RoPE at their logical positions.
+ *   - Errors are returned as kap_status; nothing is thrown across the ABI. Host-side argument checks always run.
+ *     Kernels that meet an inconsistent device-side value (a page id outside the pool, a selection larger than its
+ *     capacity) skip that access and record a code readable with kap_device_error().
+ */
+#ifndef KAP_H
+#define KAP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st *kap_stream; /* same type as cudaStream_t */
+
+typedef enum {
+  KAP_OK = 0,
+  KAP_FALLBACK_FULL = 1,   /* plan infeasible for selected access: use full-context attention (KAP paper, fallback) */
+  KAP_EINVAL = -1,         /* a NULL pointer, a negative size, or an out-of-range scalar */
+  KAP_ESHAPE = -2,         /* shapes that are inconsistent with one another */
+  KAP_ECAPACITY = -3,      /* a caller buffer (capacity, workspace) is too small */
+  KAP_ECUDA = -4,          /* a CUDA runtime call failed; see kap_last_cuda_error() */
+  KAP_EUNSUPPORTED = -5    /* a shape this build has no kernel for (head_dim, group size, dtype) */
+} kap_status;
+
+typedef enum { KAP_BF16 = 0, KAP_F32 = 1 } kap_dtype;
+
+/* Paged KV pool. All pointers are device memory owned by the caller. */
+typedef struct {
+  int32_t num_pages;    /* physical pages in the pool */
+  int32_t page_size;    /* tokens per page; must be 16 */
+  int32_t num_kv_heads; /* Hkv */
+  int32_t num_q_heads;  /* Hq, a multiple of Hkv; G = Hq / Hkv in 1..8 */
+  int32_t head_dim;     /* d: 64 or 128 */
+  int32_t dtype;        /* kap_dtype of K, V, queries and attention outputs */
+  void *k_pages;        /* [num_pages][Hkv][16][d] post-RoPE keys */
+  void *v_pages;        /* [num_pages][Hkv][16][d] values */
+  float *k_summary;     /* [num_pages][Hkv][d] fp32 block-mean keys (K-summary cache); may be NULL if unused */
+} kap_kv_pool;
+
+/* Page map M and lengths. Logical page j of request r covers positions 16j .. 16j+15. */
+typedef struct {
+  int32_t num_seqs;           /* R */
+  int32_t max_pages;          /* row stride of block_table */
+  const int32_t *block_table; /* [R][max_pages] physical page of each logical page */
+  const int32_t *ctx_len;     /* [R] prompt tokens: positions < ctx_len are the selectable prompt */
+  const int32_t *seq_len;     /* [R] tokens present (prompt + generated); a decode query sits at seq_len-1 */
+} kap_page_map;
+
+/* rho_access: the A<a>R<r>K<k> split. Prompt pages [0,a) and the last r prompt pages are pinned; k more pages
+ * are chosen from the middle by score (ties to the lower page id). */
+typedef struct {
+  int32_t anchor, recent, topk;  /* a, r, k used for every request when per_seq_ark is NULL */
+  int32_t per_kv_head;           /* 1: one selection per KV head; 0: one selection shared by all heads */
+  int32_t cap;                   /* capacity of one selection row (entries) */
+  const int32_t *per_seq_ark;    /* optional device [R][3] = (a, r, k) per request; overrides the scalars */
+} kap_access_policy;
+
+/* Compact selected-KV view, written by kap_compile_view and read by kap_attn_propose.
+ * Row (r, v) with v < rows_per_seq lists the visible pages of request r for KV head v (or for all heads when
+ * rows_per_seq == 1): first the n_selected selected prompt pages in ascending logical order ("compacted in
+ * access order"), then the tail pages holding positions >= ctx_len, up to the horizon given at compile time. */
+typedef struct {
+  int32_t rows_per_seq;   /* Hkv (per-head views) or 1 (one view shared by all heads) */
+  int32_t cap;            /* entries per row */
+  int32_t *block_table;   /* [R][rows_per_seq][cap] physical page of each entry */
+  int32_t *logical_page;  /* [R][rows_per_seq][cap] logical page of each entry (keeps logical positions) */
+  int32_t *n_entries;     /* [R][rows_per_seq] entries in use */
+  int32_t *n_selected;    /* [R][rows_per_seq] leading entries that are selected prompt pages */
+} kap_view;
+
+/* rho_verify: the verification window. Request r owns query rows q_offsets[r] .. q_offsets[r+1]-1; row i of
+ * request r sits at logical position q_start_pos[r] + i and sees every position <= its own (full context,
+ * causal among the candidates). */
+typedef struct {
+  int32_t max_q;              /* upper bound on q_offsets[r+1]-q_offsets[r]; G*max_q <= 64 */
+  int32_t total_q;            /* q_offsets[R] */
+  const int32_t *q_offsets;   /* [R+1] */
+  const int32_t *q_start_pos; /* [R] */
+} kap_verify_policy;
+
+/* ---------------------------------------------------------------------------------------------------------
+ * K-summary cache. EarlySelectKV page (routing over a K-summary cache) and the KRI page's KRI-Q row
+ * (block-mean K). For every request r and prompt page j < ceil(ctx_len[r]/16), with n = min(16, ctx_len-16j)
+ * valid tokens: k_summary[page][h][i] = (sum over t < n of K[page][h][t][i], fp32, t ascending) / n.
+ * Requires pool->k_summary. Pages shared between requests must agree on n. */
+kap_status kap_build_summaries(const kap_kv_pool *pool, const kap_page_map *map, kap_stream stream);
+
+/* Page scoring and A/R/K top-K. KRI page (KRI-Q row; A<a>R<r>K<k> tag and its 128-block example) and
+ * EarlySelectKV page (score and top-k over the K-summary cache, proxy query allowed).
+ *   q_dev     [R][Hq][d] pool dtype: the routing query (the real query or a proxy).
+ *   qbar[h]   = sum over g < G of q[h*G+g] (fp32, g ascending).
+ *   score     = dot(qbar[h], k_summary[page][h]) in the fixed 32-lane order: lane l accumulates fmaf over
+ *               i = l, l+32, ...; then lanes are combined by xor-butterfly 16, 8, 4, 2, 1 (a + b).
+ *               Shared selection (per_kv_head = 0): score = sum over h ascending of the per-head scores.
+ *   sel_ids   [R][rows][cap] out: selected prompt pages ascending; rows = Hkv or 1.
+ *   n_sel     [R][rows] out: count = min(N, a + r + k) with N = ceil(ctx_len/16).
+ *   workspace >= kap_score_workspace_size(...) bytes of device memory (scores). */
+kap_status kap_score_topk(const kap_kv_pool *pool, const kap_page_map *map, const void *q_dev,
+                          const kap_access_policy *policy, int32_t *sel_ids, int32_t *n_sel,
+                          void *workspace, size_t workspace_bytes, kap_stream stream);
+size_t kap_score_workspace_size(int32_t num_seqs, int32_t rows_per_seq, int32_t max_pages);
+
+/* Span selection. KAP paper, compiler stage 3 (selected spans resolved to KV pages): a prompt page is kept when
+ * any token of a selected span falls in it; pinned anchor/recent pages (policy a, r) are added. One row per
+ * request (shared by all heads).
+ *   spans_dev        [S][2] int32 (first token, length); span_offsets_dev [R+1] splits them by request.
+ *   sel_ids          [R][1][policy->cap] out, ascending; n_sel [R][1] out. */
+kap_status kap_select_spans(const kap_page_map *map, const int32_t *spans_dev, const int32_t *span_offsets_dev,
+                            const kap_access_policy *policy, int32_t *sel_ids, int32_t *n_sel, kap_stream stream);
+
+/* View compilation. KAP paper, compiler stage 3 and "selected-KV view" (selected pages compacted in access
+ * order, logical positions preserved through block tables). For each row: entries 0..n_sel-1 are the selected
+ * pages (block_table[i] = map->block_table[r][sel[i]], logical_page[i] = sel[i]); then tail pages: every page
+ * j >= floor(ctx_len/16) with 16j < seq_len + horizon_tokens that is not already selected.
+ *   sel_rows_per_seq/sel_cap give the layout of sel_ids; view->rows_per_seq must equal sel_rows_per_seq.
+ *   fallback_dev     optional [R] out: 1 when request r's retained prompt fraction n_sel/N exceeds s_max,
+ *                    else 0 (KAP paper, fallback: "retains too much KV").
+ * Returns KAP_ECAPACITY when view->cap < sel_cap + ceil(horizon/16) + 1. */
+kap_status kap_compile_view(const kap_page_map *map, const int32_t *sel_ids, const int32_t *n_sel,
+                            int32_t sel_rows_per_seq, int32_t sel_cap, int32_t horizon_tokens,
+                            const kap_view *view, int32_t *fallback_dev, float s_max, kap_stream stream);
+
+/* Slot mapping. KAP paper, selected-KV view ("slot mappings place newly scheduled tokens into their
+ * physical KV slots"). Request r owns tokens tok_offsets[r] .. tok_offsets[r+1]-1; token j sits at
+ * pos = start_pos[r] + (j - tok_offsets[r]) and slot = block_table[r][pos/16]*16 + pos%16 (-1 when the page is
+ * outside the table or negative). Writes slot_out[j] and pos_out[j]. */
+kap_status kap_slot_mapping(const kap_page_map *map, const int32_t *tok_offsets_dev, const int32_t *start_pos_dev,
+                            int32_t num_tokens, int64_t *slot_out, int32_t *pos_out, kap_stream stream);
+
+/* KV append with RoPE. KAP paper, executor (proposal KV written through the slot mapping; the verifier advances
+ * the full-context KV state). For token t (0 <= t < T) with p = pos[t*tok_stride], s = slots[t*tok_stride]:
+ * when s >= 0, K[s] = RoPE(k_new[t], p), V[s] = v_new[t] (fp32 math, round-to-nearest into the pool dtype);
+ * when q_inout is not NULL, q_inout[t] = RoPE(q_inout[t], p) in place.
+ * RoPE: pairs (i, i + d/2), angle = (float)p * inv_freq[i] (fp32), x' = x*cos - y*sin, y' = x*sin + y*cos.
+ *   k_new, v_new [T][Hkv][d], q_inout [T][Hq][d] in the pool dtype; inv_freq_dev [d/2] fp32. */
+kap_status kap_append_kv(const kap_kv_pool *pool, const void *k_new, const void *v_new, void *q_inout,
+                         const int32_t *pos_dev, const int64_t *slots_dev, int32_t num_tokens, int32_t tok_stride,
+                         const float *inv_freq_dev, kap_stream stream);
+
+/* Selected-KV proposal attention, q = 1 per request. KAP paper, executor (proposal: a decode-like step with
+ * q_prop = 1 over the compact view; only prompt-side KV is restricted) and EarlySelectKV (sparse attention with
+ * the real query on precomputed page indices).
+ * Query of request r, head hq sits at position P = seq_len[r]-1. A token at position p of view entry i is
+ * visible when p <= P and (i < n_selected or p >= ctx_len).
+ *   q_dev [R][Hq][d], out [R][Hq][d] (pool dtype), lse [R][Hq] fp32.
+ *   workspace >= kap_propose_workspace_size(...) bytes, zero-filled once before first use (the kernels leave
+ *   their counters at zero again on completion). */
+kap_status kap_attn_propose(const kap_kv_pool *pool, const kap_page_map *map, const kap_view *view,
+                            const void *q_dev, void *out, float *lse, void *workspace, size_t workspace_bytes,
+                            kap_stream stream);
+size_t kap_propose_workspace_size(int32_t num_seqs, int32_t num_kv_heads, int32_t num_q_heads, int32_t head_dim);
+
+/* Full-context verification attention, q = n_q per request, causal among the candidates. KAP paper, verifier
+ * (short contiguous query window over the full KV cache, full block table and original positions).
+ *   q_dev [total_q][Hq][d], out [total_q][Hq][d] (pool dtype), lse [total_q][Hq] fp32.
+ *   workspace >= kap_verify_workspace_size(...) bytes, zero-filled once before first use. */
+kap_status kap_attn_verify(const kap_kv_pool *pool, const kap_page_map *map, const kap_verify_policy *vp,
+                           const void *q_dev, void *out, float *lse, void *workspace, size_t workspace_bytes,
+                           kap_stream stream);
+size_t kap_verify_workspace_size(int32_t num_seqs, int32_t num_kv_heads, int32_t num_q_heads, int32_t head_dim,
+                                 int32_t max_q);
+
+/* Diagnostics. */
+const char *kap_status_str(kap_status s);
+const char *kap_last_cuda_error(void);   /* text of the last CUDA error seen by this thread, "" if none */
+/* Reads (with a device synchronisation) and clears the device-side error word of the current device.
+ * 0 = no error; otherwise a bit set: 1 page id out of the pool, 2 selection over capacity, 4 bad page length,
+ * 8 a bounded wait in a kernel ran out. */
+kap_status kap_device_error(int32_t *code_out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KAP_H */

@@ -1,0 +1,471 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix (no GPU).
+
+Each test ties an oracle function to something other than itself: the KRI page's worked A<a>R<r>K<k> example,
+closed forms of softmax attention, torch's fp64 scaled_dot_product_attention on a dense gather, brute force on
+tiny inputs, exact integer arithmetic, and the algebra of the KAP cost model.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+PAGE = 16
+
+
+# ----------------------------------------------------------------------------------------------- A/R/K top-K
+def _read_ark_fixture():
+    tags = {}
+    for line in open(os.path.join(GOLDEN, "ark_128_block_example.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        f = line.split()
+        if f[0] == "num_blocks":
+            n = int(f[1])
+        elif f[0] == "budget":
+            budget = int(f[1])
+        elif f[0] == "tag":
+            kv = dict(zip(f[2::2], f[3::2]))
+            pinned = [] if kv["pinned"] == "-" else [int(x) for x in kv["pinned"].split(",")]
+            tags[f[1]] = dict(a=int(kv["anchor"]), r=int(kv["recent"]), k=int(kv["k"]), pinned=pinned,
+                              mid=(int(kv["middle_first"]), int(kv["middle_last"])))
+    return n, budget, tags
+
+
+@pytest.mark.parametrize("tag", ["A1R2K13", "A0R0K16", "A4R4K8"])
+def test_ark_worked_example(orc, tag):
+    n, budget, tags = _read_ark_fixture()
+    t = tags[tag]
+    assert t["a"] + t["r"] + t["k"] == budget
+    rng = np.random.default_rng(5)
+    scores = rng.standard_normal(n).astype(np.float32)
+    sel = orc.topk_ark(scores, n, t["a"], t["r"], t["k"])
+    assert len(sel) == budget
+    assert list(sel) == sorted(sel)
+    for p in t["pinned"]:
+        assert p in sel
+    lo, hi = t["mid"]
+    chosen = [j for j in sel if j not in t["pinned"]]
+    assert all(lo <= j <= hi for j in chosen)
+    best = sorted(range(lo, hi + 1), key=lambda j: -float(scores[j]))[: t["k"]]
+    assert sorted(best) == chosen
+
+
+def test_ark_ties_go_to_lower_page(orc):
+    scores = np.zeros(40, dtype=np.float32)
+    scores[[7, 9, 30, 31]] = 2.0
+    sel = orc.topk_ark(scores, 40, 1, 1, 3)
+    assert list(sel) == [0, 7, 9, 30, 39]
+    # all equal: the lowest middle ids win
+    sel = orc.topk_ark(np.ones(20, np.float32), 20, 2, 3, 4)
+    assert list(sel) == [0, 1, 2, 3, 4, 5, 17, 18, 19]
+
+
+def test_ark_signed_zero_and_nan(orc):
+    s = np.array([0, -0.0, 0.0, np.nan, -1.0, 0.0], dtype=np.float32)
+    # -0 and +0 tie (the lower id wins); NaN ranks below -1
+    assert list(orc.topk_ark(s, 6, 0, 0, 2)) == [0, 1]
+    assert list(orc.topk_ark(s, 6, 0, 0, 5)) == [0, 1, 2, 4, 5]
+
+
+def test_ark_small_and_degenerate(orc):
+    s = np.arange(10, dtype=np.float32)
+    assert list(orc.topk_ark(s, 3, 1, 2, 5)) == [0, 1, 2]          # N <= a + r: everything pinned
+    assert list(orc.topk_ark(s, 10, 2, 2, 0)) == [0, 1, 8, 9]      # k = 0: the anchor+recency hybrid
+    assert list(orc.topk_ark(s, 10, 0, 3, 0)) == [7, 8, 9]         # recency only
+    assert list(orc.topk_ark(s, 10, 0, 0, 100)) == list(range(10))  # k beyond the middle keeps everything
+    assert list(orc.topk_ark(s, 1, 0, 0, 1)) == [0]
+
+
+def test_ark_random_brute_force(orc):
+    rng = np.random.default_rng(11)
+    for _ in range(200):
+        n = int(rng.integers(1, 90))
+        a, r, k = (int(x) for x in rng.integers(0, 6, 3))
+        s = rng.integers(-3, 4, n).astype(np.float32)  # many ties
+        sel = orc.topk_ark(s, n, a, r, k)
+        pinned = set(range(min(a, n))) | set(range(max(0, n - r), n))
+        mid = [j for j in range(n) if j not in pinned]
+        mid.sort(key=lambda j: (-float(s[j]), j))
+        assert list(sel) == sorted(pinned | set(mid[:k]))
+
+
+# --------------------------------------------------------------------------------------------- summaries
+def test_summary_is_block_mean(orc):
+    rng = np.random.default_rng(0)
+    P, hkv, d = 12, 2, 64
+    K = rng.integers(-8, 9, (P, hkv, PAGE, d)).astype(np.float32)   # integer values: sums are exact
+    bt = np.array([[3, 7, 1, 0], [5, 2, 9, -1]], np.int32)
+    ctx = np.array([64, 37], np.int32)                                  # second request: partial last page
+    K[9, :, 37 - 32:, :] = np.nan                                         # invalid slots of that page
+    S = orc.build_summaries(K, bt, ctx)
+    for r in range(2):
+        for j in range((ctx[r] + 15) // 16):
+            n = min(16, ctx[r] - 16 * j)
+            want = K[bt[r, j], :, :n, :].astype(np.float64).mean(axis=1)
+            got = S[bt[r, j]].astype(np.float64)
+            if n == 16:
+                assert np.array_equal(got, want)  # division by 16 is exact
+            else:
+                np.testing.assert_allclose(got, want, rtol=2 ** -23, atol=0)
+            assert np.isfinite(got).all()
+
+
+# ----------------------------------------------------------------------------------------------- scores
+def test_dot_fixed_order_exact_on_integers(orc):
+    rng = np.random.default_rng(1)
+    for d in (64, 128):
+        a = rng.integers(-50, 51, d).astype(np.float32)
+        b = rng.integers(-50, 51, d).astype(np.float32)
+        assert float(orc.dot_fixed_order(a, b)) == float(np.dot(a.astype(np.int64), b.astype(np.int64)))
+
+
+def test_dot_fixed_order_is_the_stated_order(orc):
+    # 2^24 + 1 rounds back to 2^24 inside partial 0 (i = 0 and i = 32), and partial 16 holds -2^24: the stated order
+    # gives 0 where an exact or sequential sum gives 1. A different lane assignment or combine order fails here.
+    a = np.zeros(64, np.float32)
+    b = np.ones(64, np.float32)
+    a[0], a[32], a[16] = 2.0 ** 24, 1.0, -(2.0 ** 24)
+    assert float(orc.dot_fixed_order(a, b)) == 0.0
+    a2 = a.copy()
+    a2[32], a2[48] = 0.0, 1.0   # the 1 now sits in partial 16 next to -2^24: -2^24 + 1 is exact, result 1
+    assert float(orc.dot_fixed_order(a2, b)) == 1.0
+
+
+def test_scores_exact_on_integers(orc):
+    rng = np.random.default_rng(2)
+    R, hq, hkv, d, P = 2, 8, 2, 64, 10
+    q = rng.integers(-4, 5, (R, hq, d)).astype(np.float32)
+    S = rng.integers(-4, 5, (P, hkv, d)).astype(np.float32)
+    bt = np.array([[4, 1, 7], [0, 9, 2]], np.int32)
+    ctx = np.array([48, 40], np.int32)
+    G = hq // hkv
+    per, per64 = orc.scores(q, S, bt, ctx, per_head=True)
+    pooled, _ = orc.scores(q, S, bt, ctx, per_head=False)
+    for r in range(R):
+        for j in range(3):
+            tot = 0
+            for h in range(hkv):
+                qbar = q[r, h * G:(h + 1) * G].astype(np.int64).sum(axis=0)
+                v = int(np.dot(qbar, S[bt[r, j], h].astype(np.int64)))
+                assert per[r, h, j] == v and per64[r, h, j] == v
+                tot += v
+            assert pooled[r, 0, j] == tot
+
+
+def test_scores_fp32_close_to_fp64(orc):
+    rng = np.random.default_rng(3)
+    R, hq, hkv, d, P = 1, 32, 8, 128, 40
+    q = rng.standard_normal((R, hq, d)).astype(np.float32)
+    S = rng.standard_normal((P, hkv, d)).astype(np.float32)
+    bt = rng.permutation(P)[:32].astype(np.int32)[None]
+    ctx = np.array([512], np.int32)
+    s32, s64 = orc.scores(q, S, bt, ctx, per_head=True)
+    assert np.abs(s32[:, :, :32] - s64[:, :, :32]).max() < 1e-4 * np.abs(s64[:, :, :32]).max()
+
+
+# ------------------------------------------------------------------------------------------------ spans
+def test_select_spans_brute_force(orc):
+    rng = np.random.default_rng(4)
+    for _ in range(100):
+        N = int(rng.integers(1, 60))
+        ns = int(rng.integers(0, 5))
+        spans = [(int(rng.integers(0, N * 16 + 20)), int(rng.integers(0, 40))) for _ in range(ns)]
+        a, r = (int(x) for x in rng.integers(0, 3, 2))
+        want = set(range(min(a, N))) | set(range(max(0, N - r), N))
+        for first, ln in spans:
+            for t in range(first, first + ln):
+                if t < N * 16:
+                    want.add(t // 16)
+        got = orc.select_spans(N, np.array(spans, np.int32).reshape(-1, 2), a, r)
+        assert list(got) == sorted(want)
+
+
+# ------------------------------------------------------------------------------------- view and slots
+def test_compile_view_invariants(orc):
+    rng = np.random.default_rng(6)
+    for _ in range(100):
+        ctx = int(rng.integers(1, 400))
+        horizon = int(rng.integers(0, 20))
+        seq = ctx + int(rng.integers(0, 10))
+        npages = (seq + horizon + 15) // 16 + 1
+        bt = rng.permutation(1000)[:npages].astype(np.int32)
+        N = (ctx + 15) // 16
+        sel = sorted(set(int(x) for x in rng.integers(0, N, int(rng.integers(1, N + 1)))))
+        cbt, clog, nsel = orc.compile_view_row(bt, ctx, seq, horizon, np.array(sel, np.int32))
+        assert nsel == len(sel)
+        assert list(clog[:nsel]) == sel
+        assert np.all(np.diff(clog) > 0)                       # access order == logical order, no duplicates
+        assert np.array_equal(cbt, bt[clog])                    # logical positions preserved
+        tail = [j for j in range(ctx // 16, npages) if j * 16 < seq + horizon]
+        assert sorted(set(clog)) == sorted(set(sel) | set(tail))
+        # KRI connector skip list: the selected prompt blocks and their sorted complement partition range(N)
+        skip = sorted(b for b in range(N) if b not in set(sel))
+        assert sorted(set(sel) | set(skip)) == list(range(N)) and not (set(sel) & set(skip))
+
+
+def test_slot_mapping_inverts_through_the_table(orc):
+    rng = np.random.default_rng(7)
+    bt = rng.permutation(300)[:20].astype(np.int32)
+    inverse = {int(p): j for j, p in enumerate(bt)}
+    for pos in range(0, 20 * 16):
+        s = orc.slot(bt, pos)
+        page, off = divmod(s, 16)
+        assert inverse[page] * 16 + off == pos
+    assert orc.slot(bt, 20 * 16) == -1
+    bt2 = bt.copy()
+    bt2[3] = -1
+    assert orc.slot(bt2, 3 * 16 + 5) == -1
+
+
+# ------------------------------------------------------------------------------------------------- RoPE
+def test_inv_freq_closed_form(orc):
+    for d in (64, 128):
+        f = orc.inv_freq(d, 1.0e4).astype(np.float64)
+        assert f[0] == 1.0
+        assert abs(f[d // 4] - 0.01) <= 0.01 * 2 ** -23        # theta^(-1/2) = 0.01
+        ratio = f[1:] / f[:-1]
+        np.testing.assert_allclose(ratio, 1.0e4 ** (-2.0 / d), rtol=3e-7)
+
+
+def test_rope_properties(orc):
+    rng = np.random.default_rng(8)
+    d = 64
+    f = orc.inv_freq(d)
+    x = rng.standard_normal((5, 3, d)).astype(np.float32)
+    y0 = orc.rope(x, np.zeros(5, np.int32), f)
+    np.testing.assert_array_equal(y0, x.astype(np.float64))      # position 0 is the identity
+    pos = np.array([1, 17, 1000, 65535, 131071], np.int32)
+    y = orc.rope(x, pos, f)
+    h = d // 2
+    np.testing.assert_allclose(y[..., :h] ** 2 + y[..., h:] ** 2,
+                               x[..., :h].astype(np.float64) ** 2 + x[..., h:].astype(np.float64) ** 2,
+                               rtol=1e-12, atol=1e-12)            # each pair keeps its norm
+    # complex-number form: (x_i + i x_{i+d/2}) * exp(i * angle), angle formed in fp32
+    ang = (pos.astype(np.float32)[:, None] * f[None, :]).astype(np.float64)
+    z = (x[..., :h].astype(np.float64) + 1j * x[..., h:].astype(np.float64)) * np.exp(1j * ang)[:, None, :]
+    np.testing.assert_allclose(y[..., :h], z.real, atol=1e-12)
+    np.testing.assert_allclose(y[..., h:], z.imag, atol=1e-12)
+
+
+def test_rope_relative_position(orc):
+    rng = np.random.default_rng(9)
+    d = 128
+    f = orc.inv_freq(d)
+    q = rng.standard_normal((1, 1, d)).astype(np.float32)
+    k = rng.standard_normal((1, 1, d)).astype(np.float32)
+    def dot(m, n):
+        return float(np.sum(orc.rope(q, np.array([m], np.int32), f) * orc.rope(k, np.array([n], np.int32), f)))
+    base = dot(10, 3)
+    for c in (1, 5, 100, 2000):
+        assert abs(dot(10 + c, 3 + c) - base) < 1e-3 * (1 + abs(base))
+
+
+# -------------------------------------------------------------------------------------------- attention
+def _dense(K, bt_row, n_tok, h):
+    """Gathers positions 0..n_tok-1 of KV head h through one block-table row into a dense [n_tok][d] array."""
+    return np.stack([K[bt_row[p // 16], h, p % 16] for p in range(n_tok)]).astype(np.float64)
+
+
+def _sdpa(q, k, v, mask):
+    """torch fp64 scaled_dot_product_attention plus its log-sum-exp (the library routine the oracle must match)."""
+    qt = torch.from_numpy(q)[None, None, None]   # [1,1,1,d]
+    kt = torch.from_numpy(k)[None, None]
+    vt = torch.from_numpy(v)[None, None]
+    m = torch.from_numpy(mask)[None, None, None]
+    o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=m)[0, 0, 0].numpy()
+    logits = (k @ q) / math.sqrt(q.shape[0])
+    lse = float(torch.logsumexp(torch.from_numpy(logits[mask]), 0))
+    return o, lse
+
+
+def _toy(seed, R=2, hq=8, hkv=2, d=64, ctx=(70, 100), extra=4, poison=True):
+    rng = np.random.default_rng(seed)
+    npg = [(c + extra + 15) // 16 for c in ctx]
+    P = sum(npg) + 3
+    perm = rng.permutation(P)
+    bt = np.full((R, max(npg)), -1, np.int32)
+    o = 0
+    for r in range(R):
+        bt[r, :npg[r]] = perm[o:o + npg[r]]
+        o += npg[r]
+    K = rng.standard_normal((P, hkv, 16, d)).astype(np.float32)
+    V = rng.standard_normal((P, hkv, 16, d)).astype(np.float32)
+    return rng, bt, K, V
+
+
+def test_propose_matches_sdpa_on_masked_subset(orc):
+    R, hq, hkv, d = 2, 8, 2, 64
+    ctx = np.array([70, 100], np.int32)
+    seq = ctx + 3
+    rng, bt, K, V = _toy(10, R, hq, hkv, d, tuple(ctx))
+    # poison every slot at or past seq_len: the oracle must never read them
+    for r in range(R):
+        for p in range(seq[r], bt.shape[1] * 16):
+            if bt[r, p // 16] >= 0:
+                K[bt[r, p // 16], :, p % 16] = np.nan
+                V[bt[r, p // 16], :, p % 16] = np.nan
+    q = rng.standard_normal((R, hq, d)).astype(np.float32)
+    cap = 7
+    sel = np.zeros((R, hkv, cap), np.int32)
+    nsel = np.zeros((R, hkv), np.int32)
+    for r in range(R):
+        N = (ctx[r] + 15) // 16
+        for h in range(hkv):
+            s = sorted(rng.choice(N, size=min(3 + h, N), replace=False))
+            sel[r, h, :len(s)] = s
+            nsel[r, h] = len(s)
+    out, lse = orc.attn_propose(q, K, V, bt, ctx, seq, sel, nsel)
+    G = hq // hkv
+    for r in range(R):
+        for h in range(hkv):
+            n_tok = int(seq[r])
+            k = _dense(K, bt[r], n_tok, h)
+            v = _dense(V, bt[r], n_tok, h)
+            chosen = set(sel[r, h, :nsel[r, h]].tolist())
+            mask = np.array([(p >= ctx[r]) or (p // 16 in chosen) for p in range(n_tok)])
+            for g in range(G):
+                o, l = _sdpa(q[r, h * G + g].astype(np.float64), k, v, mask)
+                np.testing.assert_allclose(out[r, h * G + g], o, atol=1e-12)
+                assert abs(lse[r, h * G + g] - l) < 1e-12
+    assert np.isfinite(out).all()
+
+
+def test_propose_all_pages_equals_full_attention(orc):
+    R, hq, hkv, d = 2, 8, 2, 64
+    ctx = np.array([70, 100], np.int32)
+    seq = ctx + 2
+    rng, bt, K, V = _toy(12, R, hq, hkv, d, tuple(ctx))
+    q = rng.standard_normal((R, hq, d)).astype(np.float32)
+    cap = 8
+    sel = np.zeros((R, 1, cap), np.int32)
+    nsel = np.zeros((R, 1), np.int32)
+    for r in range(R):
+        N = (ctx[r] + 15) // 16
+        sel[r, 0, :N] = np.arange(N)
+        nsel[r, 0] = N
+    out, lse = orc.attn_propose(q, K, V, bt, ctx, seq, sel, nsel)
+    G = hq // hkv
+    for r in range(R):
+        for h in range(hkv):
+            k = _dense(K, bt[r], int(seq[r]), h)
+            v = _dense(V, bt[r], int(seq[r]), h)
+            for g in range(G):
+                o, l = _sdpa(q[r, h * G + g].astype(np.float64), k, v, np.ones(int(seq[r]), bool))
+                np.testing.assert_allclose(out[r, h * G + g], o, atol=1e-12)
+                assert abs(lse[r, h * G + g] - l) < 1e-12
+
+
+def test_attention_closed_forms(orc):
+    d, hkv, hq = 64, 1, 2
+    rng = np.random.default_rng(13)
+    K = rng.standard_normal((4, hkv, 16, d)).astype(np.float32)
+    V = rng.standard_normal((4, hkv, 16, d)).astype(np.float32)
+    q = rng.standard_normal((1, hq, d)).astype(np.float32)
+    bt = np.array([[2, 0, 3]], np.int32)
+    # one visible token: out = v, lse = its logit
+    out, lse = orc.attn_verify(q, K, V, bt, np.array([0, 1], np.int32), np.array([0], np.int32))
+    kk = K[2, 0, 0].astype(np.float64)
+    for g in range(hq):
+        np.testing.assert_allclose(out[0, g], V[2, 0, 0], atol=1e-12)
+        assert abs(lse[0, g] - float(q[0, g].astype(np.float64) @ kk) / 8.0) < 1e-12
+    # identical keys: uniform weights, out = mean of v, lse = logit + log(n)
+    K2 = K.copy()
+    K2[:, 0, :, :] = K[0, 0, 0]
+    n = 37
+    out, lse = orc.attn_verify(q, K2, V, bt, np.array([0, 1], np.int32), np.array([n - 1], np.int32))
+    vs = _dense(V, bt[0], n, 0)
+    for g in range(hq):
+        np.testing.assert_allclose(out[0, g], vs.mean(axis=0), atol=1e-12)
+        logit = float(q[0, g].astype(np.float64) @ K[0, 0, 0].astype(np.float64)) / 8.0
+        assert abs(lse[0, g] - (logit + math.log(n))) < 1e-12
+
+
+def test_verify_is_causal_and_matches_sdpa(orc):
+    R, hq, hkv, d = 2, 8, 2, 64
+    ctx = (70, 100)
+    rng, bt, K, V = _toy(14, R, hq, hkv, d, ctx, extra=8)
+    nq = [3, 5]
+    qo = np.array([0, 3, 8], np.int32)
+    qs = np.array([ctx[0], ctx[1] - 2], np.int32)
+    q = rng.standard_normal((8, hq, d)).astype(np.float32)
+    out, lse = orc.attn_verify(q, K, V, bt, qo, qs)
+    G = hq // hkv
+    for r in range(R):
+        last = qs[r] + nq[r] - 1
+        for h in range(hkv):
+            k = _dense(K, bt[r], last + 1, h)
+            v = _dense(V, bt[r], last + 1, h)
+            for i in range(nq[r]):
+                mask = np.arange(last + 1) <= qs[r] + i
+                for g in range(G):
+                    o, l = _sdpa(q[qo[r] + i, h * G + g].astype(np.float64), k, v, mask)
+                    np.testing.assert_allclose(out[qo[r] + i, h * G + g], o, atol=1e-12)
+                    assert abs(lse[qo[r] + i, h * G + g] - l) < 1e-12
+    # changing the KV of a later candidate leaves earlier rows unchanged
+    K3, V3 = K.copy(), V.copy()
+    p = qs[1] + 3
+    K3[bt[1, p // 16], :, p % 16] += 5.0
+    V3[bt[1, p // 16], :, p % 16] -= 5.0
+    out3, lse3 = orc.attn_verify(q, K3, V3, bt, qo, qs)
+    np.testing.assert_array_equal(out3[:3 + 3], out[:3 + 3])
+    assert not np.allclose(out3[3 + 3], out[3 + 3])
+
+
+def test_verify_row_equals_decode_with_every_page(orc):
+    R, hq, hkv, d = 1, 8, 2, 64
+    rng, bt, K, V = _toy(15, 1, hq, hkv, d, (90,), extra=6)
+    q = rng.standard_normal((4, hq, d)).astype(np.float32)
+    out, lse = orc.attn_verify(q, K, V, bt, np.array([0, 4], np.int32), np.array([90], np.int32))
+    for i in range(4):
+        N = (90 + 15) // 16
+        sel = np.arange(N, dtype=np.int32).reshape(1, 1, N)
+        o2, l2 = orc.attn_propose(q[i:i + 1], K, V, bt, np.array([90], np.int32), np.array([91 + i], np.int32), sel,
+                                  np.array([[N]], np.int32))
+        np.testing.assert_allclose(out[i], o2[0], atol=1e-13)
+        np.testing.assert_allclose(lse[i], l2[0], atol=1e-13)
+
+
+# ------------------------------------------------------------------------------------------- cost model
+def test_cost_model_boundary_algebra():
+    from oracle import cost_model as cm
+    rng = np.random.default_rng(16)
+    for _ in range(2000):
+        k = int(rng.integers(1, 12))
+        h, s = float(rng.uniform(0, 1)), float(rng.uniform(0.001, 1))
+        w, kv = float(rng.uniform(0.1, 10)), float(rng.uniform(0.1, 10))
+        diff = cm.cost_base(k, h, w, kv) - cm.cost_plan(k, s, w, w, kv)
+        assert abs(diff - k * ((h - s) * kv - (1 - h) * w)) < 1e-9 * (1 + abs(diff))
+        if abs(diff) > 1e-9:
+            assert (diff > 0) == cm.plan_wins(h, s, w, kv)
+    # at KV_crit the two costs meet
+    h, s, w = 0.95, 0.055, 3.0
+    kvc = cm.kv_crit(h, s, w)
+    assert abs(cm.cost_base(6, h, w, kvc) - cm.cost_plan(6, s, w, w, kvc)) < 1e-9
+    assert cm.kv_crit(0.3, 0.4, 1.0) == float("inf")     # h <= s: no context length pays off
+
+
+def test_cost_model_against_printed_points():
+    from oracle import cost_model as cm
+    pts = {}
+    for line in open(os.path.join(GOLDEN, "kap_cost_points.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        f = line.split()
+        pts[f[0]] = [float(x) for x in f[1:]]
+    lo, hi = pts["h_range"]
+    k = int(pts["k"][0])
+    for ctx in ("4K", "128K"):
+        s, margin, speedup = pts[ctx]
+        h = s + margin
+        assert lo - 0.01 <= h <= hi + 0.01             # printed s and h - s give the stated acceptance range
+        assert h > s                                     # the necessary condition of the boundary
+        # a measured speedup > 1 means the plan sits on the winning side: W_main / KV below (h - s) / (1 - h)
+        assert speedup > 1.0
+        w_over_kv_max = margin / (1.0 - h)
+        assert cm.plan_wins(h, s, 0.99 * w_over_kv_max, 1.0)
+        assert not cm.plan_wins(h, s, 1.01 * w_over_kv_max, 1.0)
+    # the cycle's KV traffic at 128K retention: k proposals of s*KV plus one full read
+    assert abs(cm.cycle_kv_bytes(k, 0.055, 1.0) - (1 + 6 * 0.055)) < 1e-12
