@@ -1,0 +1,439 @@
+#!/usr/bin/env python
+"""Benchmark of the selected-KV sparse decode hot path on GB300.
+
+One step = one proposal/verification cycle of the whole hot path over `--layers` independent attention layers
+(replicas with their own KV pools), on the Llama-3-8B-shaped workload: 4 requests x 32768-token prompts, Hq=32,
+Hkv=8, d=128, bf16 KV, per-KV-head K-summary scoring with A1R2K125 selection (s = 6.25%), 4 proposal steps (q=1)
+and a verify window of 4 (causal). Per layer and cycle: score + top-K, view compilation, two slot mappings, then
+4 x (KV append + proposal attention), then window append + verification attention.
+
+Output: one JSON line (rank 0). `value` is the algorithmic HBM bytes of every hot-path kernel in a step divided by
+the device time of the step (GB/s, whole job); the phase times come from CUDA events recorded between CUDA-graph
+replays of each phase on the launch stream. `--impl reference` times the CPU oracle instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "sparse paged attention HBM GB/s (% of roofline); proposal & verify steps/s"
+PAGE = 16
+CONFIG = "llama"
+WORKLOAD = ("Llama-3-8B-shaped attention layer: 4 requests x 32768-token prompts (2048 pages of 16), Hq=32, Hkv=8, "
+            "d=128, bf16 KV, fp32 accumulation, per-KV-head A1R2K125 (s=6.25%), 16 needle pages/request, "
+            "4 proposal steps (q=1) + verify window 4 (causal)")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["kap", "reference"], default="kap")
+    ap.add_argument("--layers", type=int, default=8)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def reduce_max(value: float, dist=None) -> float:
+    """Max of a per-rank scalar over all ranks (timing only, not on the data path)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(value: float, dist=None) -> float:
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------------------- clock sampling
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def start(self):
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "20"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons, n = [], [], set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            n += 1
+            for nm, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": n}
+
+
+# --------------------------------------------------------------------------------------------- byte model
+def step_bytes(w, cyc, sel_ids, n_sel):
+    """Algorithmic HBM bytes of one cycle on one layer, per kernel family (SURVEY-style unit counts):
+    scores read every prompt page's fp32 summary; proposal step i reads K and V of every visible token of the
+    view (selected prompt tokens + generated tokens up to the step's position); verification reads K and V of
+    every position up to the last window row; appends write K and V of the new tokens."""
+    import numpy as np
+    kv_tok = w.d * 2 * 2  # bytes of K+V of one token of one KV head (bf16)
+    ctx = w.ctx_len.cpu().numpy().astype(np.int64)
+    seq0 = w.seq_len0.cpu().numpy().astype(np.int64)
+    N = (ctx + PAGE - 1) // PAGE
+    score = int((N * w.Hkv * w.d * 4).sum())
+    sel = sel_ids.cpu().numpy()
+    ns = n_sel.cpu().numpy()
+    rows = sel.shape[1]
+    prop = []
+    for i in range(w.k_prop):
+        tot = 0
+        for r in range(w.R):
+            for h in range(w.Hkv):
+                v = 0 if rows == 1 else h
+                pages = sel[r, v, :ns[r, v]]
+                tok = np.minimum(PAGE, ctx[r] - PAGE * pages.astype(np.int64)).clip(min=0).sum()
+                tok += (seq0[r] + i + 1) - ctx[r]   # generated positions ctx .. seq0 + i
+                tot += int(tok) * kv_tok
+        prop.append(tot)
+    nq = w.n_q.cpu().numpy().astype(np.int64)
+    ver = int(((seq0 + nq) * w.Hkv * kv_tok).sum())
+    app = int((w.k_prop * w.R + nq.sum()) * w.Hkv * w.d * 2 * 2)
+    return dict(score=score, propose=prop, verify=ver, append=app)
+
+
+# ------------------------------------------------------------------------------------------------ oracle arm
+def oracle_sample(w_cpu, nthreads: int, r: int = 0):
+    """Runs the oracle on one request of one layer for one full cycle; returns (seconds, algorithmic bytes)."""
+    import numpy as np
+    import oracle
+    bt = w_cpu.block_table.numpy()
+    ctx = w_cpu.ctx_len.numpy()
+    seq0 = w_cpu.seq_len0.numpy()
+    npg = (int(ctx[r]) + max(w_cpu.k_prop, int(w_cpu.n_q[r])) + PAGE - 1) // PAGE
+    pages = bt[r, :npg]
+    K = w_cpu.K[pages].float().numpy()
+    V = w_cpu.V[pages].float().numpy()
+    lbt = np.arange(npg, dtype=np.int32)[None]
+    lctx, lseq = ctx[r:r + 1], seq0[r:r + 1]
+    qr = w_cpu.q_route[r:r + 1].float().numpy()
+    a, rr, k = (int(x) for x in w_cpu.ark[r].tolist())
+    t0 = time.perf_counter()
+    S = oracle.build_summaries(K, lbt, lctx)
+    sc, _ = oracle.scores(qr, S, lbt, lctx, per_head=True)
+    N = (int(lctx[0]) + PAGE - 1) // PAGE
+    sels = [oracle.topk_ark(sc[0, h], N, a, rr, k) for h in range(w_cpu.Hkv)]
+    cap = max(len(s) for s in sels)
+    sel = np.zeros((1, w_cpu.Hkv, cap), np.int32)
+    nsel = np.zeros((1, w_cpu.Hkv), np.int32)
+    for h, s in enumerate(sels):
+        sel[0, h, :len(s)] = s
+        nsel[0, h] = len(s)
+    prop_bytes = 0
+    for i in range(w_cpu.k_prop):
+        q = w_cpu.q_prop[i, r:r + 1].float().numpy()
+        oracle.attn_propose(q, K, V, lbt, lctx, lseq + i + 1, sel, nsel, nthreads=nthreads)
+    nq = int(w_cpu.n_q[r])
+    qv = w_cpu.q_ver[int(w_cpu.q_offsets[r]):int(w_cpu.q_offsets[r]) + nq].float().numpy()
+    oracle.attn_verify(qv, K, V, lbt, np.array([0, nq], np.int32), lseq, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    kv_tok = w_cpu.d * 2 * 2
+    for i in range(w_cpu.k_prop):
+        for h in range(w_cpu.Hkv):
+            p = sel[0, h, :nsel[0, h]].astype(np.int64)
+            prop_bytes += int((np.minimum(PAGE, int(lctx[0]) - PAGE * p).clip(min=0).sum() + i + 1) * kv_tok)
+    ver_bytes = (int(lseq[0]) + nq) * w_cpu.Hkv * kv_tok
+    score_bytes = N * w_cpu.Hkv * w_cpu.d * 4
+    return dt, prop_bytes + ver_bytes + score_bytes
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    import torch
+    import oracle
+    from workloads import make_workload
+    oracle.build()
+    nthreads = oracle.hardware_threads()
+    w = make_workload(CONFIG, device="cpu", poison=False)
+    for _ in range(args.warmup):
+        oracle_sample(w, nthreads)
+    times, nbytes = [], 0
+    for _ in range(args.steps):
+        dt, b = oracle_sample(w, nthreads)
+        times.append(dt)
+        nbytes = b
+    tot = sum(times)
+    val = nbytes * args.steps / tot / 1e9
+    sample = (f"one request of one layer per step: block-mean summaries, fixed-order scores and A1R2K125 top-K for "
+              f"8 KV heads, 4 proposal attentions and one verify window of 4 over the 32772-token context, fp64")
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD},
+            "cpu_baseline": {"value": val, "unit": "GB/s", "cores": nthreads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------------------------------- GPU arm
+def run_kap(args, world, rank, local):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl", device_id=dev)
+    import selected_kv_sparse_gb300 as kap
+    from workloads import make_workload
+    kap.load()
+
+    L = args.layers
+    layers = []
+    for l in range(L):
+        w = make_workload(CONFIG, device=dev, seed_offset=rank * 1000 + l, poison=False)
+        ksum = torch.zeros(w.num_pages, w.Hkv, w.d, dtype=torch.float32, device=dev)
+        pool = kap.KVPool(w.K, w.V, w.Hq, ksum)
+        kap.kap_build_summaries(pool, kap.PageMap(w.block_table, w.ctx_len, w.seq_len0))
+        a, r, k = (int(x) for x in w.ark[0].tolist())
+        pol = kap.AccessPolicy(a, r, k, True, w.sel_cap())
+        cyc = kap.DecodeCycle(pool, w.block_table, w.ctx_len, w.seq_len0, w.k_prop, w.n_q,
+                              kap.rope_inv_freq(w.d, w.theta, dev), policy=pol)
+        ins = dict(q_route=w.q_route.clone(), q_prop=w.q_prop.clone(), k_prop=w.k_new_prop.clone(),
+                   v_prop=w.v_new_prop.clone(), q_ver=w.q_ver.clone(), k_ver=w.k_new_ver.clone(),
+                   v_ver=w.v_new_ver.clone())
+        layers.append((w, cyc, ins))
+    k_prop = layers[0][0].k_prop
+
+    phases = [("plan", lambda: [c.plan(x["q_route"]) for _, c, x in layers])]
+    for i in range(k_prop):
+        phases.append((f"app{i}", lambda i=i: [c.append_step(i, x["q_prop"][i], x["k_prop"][i], x["v_prop"][i])
+                                                for _, c, x in layers]))
+        phases.append((f"prop{i}", lambda i=i: [c.propose(i, x["q_prop"][i]) for _, c, x in layers]))
+    phases.append(("vapp", lambda: [c.append_window(x["q_ver"], x["k_ver"], x["v_ver"]) for _, c, x in layers]))
+    phases.append(("ver", lambda: [c.verify(x["q_ver"]) for _, c, x in layers]))
+
+    # eager pass (sets kernel attributes, caches tensor maps), then one CUDA graph per phase
+    for _, fn in phases:
+        fn()
+    torch.cuda.synchronize()
+    graphs = []
+    for name, fn in phases:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        graphs.append((name, g))
+    torch.cuda.synchronize()
+    launches_per_step = sum(c.launches_per_cycle() for _, c, _ in layers)
+
+    # algorithmic bytes (selection is fixed across cycles: the routing query is not modified by a cycle)
+    by = [step_bytes(w, c, c.sel_ids, c.n_sel) for w, c, _ in layers]
+    b_score = sum(b["score"] for b in by)
+    b_prop = [sum(b["propose"][i] for b in by) for i in range(k_prop)]
+    b_ver = sum(b["verify"] for b in by)
+    b_app = sum(b["append"] for b in by)
+    b_step = b_score + sum(b_prop) + b_ver + b_app
+    ws_bytes = sum(x.K.numel() * 2 * 2 for x, _, _ in layers)
+
+    def replay_step(evs=None):
+        if evs is not None:
+            evs[0].record()
+        for j, (_, g) in enumerate(graphs):
+            g.replay()
+            if evs is not None:
+                evs[j + 1].record()
+
+    for _ in range(args.warmup):
+        replay_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(graphs) + 1)] for _ in range(K)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.05)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t_start.record()
+    for s in range(K):
+        replay_step(evs[s])
+    t_end.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if world > 1:
+        dist.barrier()
+    total_ms_local = t_start.elapsed_time(t_end)
+    phase_ms = {name: 0.0 for name, _ in graphs}
+    for s in range(K):
+        for j, (name, _) in enumerate(graphs):
+            phase_ms[name] += evs[s][j].elapsed_time(evs[s][j + 1])
+    total_ms = reduce_max(total_ms_local, dist)
+    ms_step = total_ms / K
+    bytes_all = reduce_sum(float(b_step), dist)
+    value = bytes_all / (ms_step * 1e-3) / 1e9
+
+    hbm_peak, peak_kind = measured_peaks()
+    ver_launch_ms = phase_ms["ver"] / (K * L)
+    prop_launch_ms = sum(phase_ms[f"prop{i}"] for i in range(k_prop)) / (K * k_prop * L)
+    ver_bytes_launch = b_ver / L
+    prop_bytes_launch = sum(b_prop) / (k_prop * L)
+    ver_gbs = ver_bytes_launch / (ver_launch_ms * 1e-3) / 1e9
+    prop_gbs = prop_bytes_launch / (prop_launch_ms * 1e-3) / 1e9
+    plan_ms = phase_ms["plan"] / (K * L)
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "verify_traffic.json")
+    if os.path.exists(tpath):
+        try:
+            traffic = json.load(open(tpath)).get("dram_bytes_per_launch")
+        except Exception:
+            traffic = None
+
+    # end to end: inputs from pinned host memory, results back, through the same calls
+    e2e = None
+    if not args.no_e2e:
+        host_in = []
+        for _, _, x in layers:
+            host_in.append({k2: v.detach().cpu().pin_memory() for k2, v in x.items()})
+        outs = [(c.o_prop, c.lse_prop, c.o_ver, c.lse_ver) for _, c, _ in layers]
+        host_out = [tuple(torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in o) for o in outs]
+        h2d = sum(v.numel() * v.element_size() for d_ in host_in for v in d_.values())
+        d2h = sum(t.numel() * t.element_size() for o in outs for t in o)
+        n_e2e = max(3, min(K, 50))
+
+        def e2e_step():
+            for (_, _, x), hx in zip(layers, host_in):
+                for k2, v in x.items():
+                    v.copy_(hx[k2], non_blocking=True)
+            replay_step()
+            for o, ho in zip(outs, host_out):
+                for t, ht in zip(o, ho):
+                    ht.copy_(t, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+        for _ in range(2):
+            e2e_step()
+        if world > 1:
+            dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record()
+        torch.cuda.synchronize()
+        e_ms = reduce_max(e0.elapsed_time(e1), dist) / n_e2e
+        e2e = {"value": bytes_all / (e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": n_e2e, "ms_per_step": e_ms}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        nth = oracle.hardware_threads()
+        w_cpu = make_workload(CONFIG, device="cpu", poison=False)
+        dt, b = oracle_sample(w_cpu, nth)
+        cpu = {"value": b / dt / 1e9, "unit": "GB/s", "cores": nth, "kind": "oracle",
+               "sample": "one request of one layer, one full cycle (summaries, scores, A1R2K125 top-K, 4 proposals, "
+                         f"verify window 4) in fp64, {dt:.2f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "layers_per_step": L, "parallelism": "replicas" if world > 1 else "1 GPU",
+                       "l2": f"inputs larger than L2: {ws_bytes / 2**30:.1f} GiB of KV per rank, "
+                             f"{b_step / 2**30:.2f} GiB read per step"},
+            "pct_of_hbm_roofline": 100.0 * value / (hbm_peak * world),
+            "propose": {"gbs": prop_gbs, "pct_of_roofline": 100 * prop_gbs / hbm_peak,
+                        "us_per_launch": prop_launch_ms * 1e3, "bytes_per_launch": prop_bytes_launch,
+                        "steps_per_s": 1e3 / (prop_launch_ms)},
+            "verify": {"gbs": ver_gbs, "pct_of_roofline": 100 * ver_gbs / hbm_peak,
+                       "us_per_launch": ver_launch_ms * 1e3, "bytes_per_launch": ver_bytes_launch,
+                       "steps_per_s": 1e3 / ver_launch_ms},
+            "plan_us_per_layer": plan_ms * 1e3,
+            "phase_ms_per_step": {k2: v / K for k2, v in phase_ms.items()},
+            "roofline": {"bound": "hbm", "kernel": "verify_tc_kernel", "achieved": ver_gbs, "peak": hbm_peak,
+                         "peak_kind": peak_kind, "unit": "GB/s", "frac": ver_gbs / hbm_peak, "traffic": traffic},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * K,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_kap(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,14 @@
+"""GB300-native selected-KV sparse decode hot path.
+
+Page scoring and A<a>R<r>K<k> top-K over a K-summary cache, compact selected-KV views with slot mappings that keep
+logical positions, RoPE'd KV append, paged GQA proposal attention (q = 1) over the selected pages, and paged causal
+verification attention (q = n) over the full block table. Every step is a hand-written sm_103a CUDA kernel behind
+the C ABI in include/kap.h; this package is its thin Python binding.
+"""
+from ._binding import (  # noqa: F401
+    AccessPolicy, KapError, KVPool, PageMap, VerifyPolicy, View, kap_append_kv, kap_attn_propose, kap_attn_verify,
+    kap_build_summaries, kap_compile_view, kap_device_error, kap_propose_workspace_size, kap_score_topk,
+    kap_score_workspace_size, kap_select_spans, kap_slot_mapping, kap_verify_workspace_size, load, parse_ark,
+    rope_inv_freq, workspace, LIB_PATH,
+)
+from .pipeline import DecodeCycle  # noqa: F401

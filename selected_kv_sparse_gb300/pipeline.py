@@ -1,0 +1,127 @@
+"""One proposal/verification cycle of the selected-KV decode loop over one attention layer, on the library calls.
+
+KAP paper, executor and verifier: the plan (selection, compact view, slot mapping) is compiled once per cycle;
+each of the k proposal steps appends the step's token KV (RoPE at its logical position) and runs q = 1 attention
+over the compact view; the verifier appends the window's KV into the full-context slots and runs causal q = n
+attention over the full block table. Every buffer is allocated here, once; the calls themselves allocate nothing,
+so a cycle can be captured in a CUDA graph.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import _binding as kb
+
+PAGE = 16
+
+
+class DecodeCycle:
+    def __init__(self, pool: kb.KVPool, block_table: torch.Tensor, ctx_len: torch.Tensor, seq_len0: torch.Tensor,
+                 k_prop: int, n_q: torch.Tensor, inv_freq: torch.Tensor, policy: Optional[kb.AccessPolicy] = None,
+                 spans: Optional[torch.Tensor] = None, span_offsets: Optional[torch.Tensor] = None,
+                 sel_cap: Optional[int] = None, s_max: float = 1.0):
+        dev = block_table.device
+        self.pool = pool
+        self.R = int(block_table.shape[0])
+        self.Hq = pool.num_q_heads
+        self.Hkv = int(pool.k_pages.shape[1])
+        self.d = int(pool.k_pages.shape[3])
+        self.k_prop = int(k_prop)
+        self.inv_freq = inv_freq
+        self.policy = policy
+        self.spans, self.span_offsets = spans, span_offsets
+        if policy is None or (spans is None and policy is None):
+            raise ValueError("a policy is required")
+        self.rows = self.Hkv if (policy.per_kv_head and spans is None) else 1
+        n_q_host = [int(x) for x in n_q.cpu().tolist()]
+        self.max_q = max(n_q_host)
+        self.total_q = sum(n_q_host)
+        self.horizon = max(self.k_prop, self.max_q)
+        self.sel_cap = int(sel_cap if sel_cap is not None else policy.cap)
+        self.view_cap = self.sel_cap + (self.horizon + PAGE - 1) // PAGE + 1
+        self.s_max = s_max
+        i32 = dict(dtype=torch.int32, device=dev)
+        # page maps: the plan's (committed length) and one per proposal step (query at seq_len0 + i)
+        self.map_plan = kb.PageMap(block_table, ctx_len, seq_len0)
+        self.seq_steps = [(seq_len0 + i + 1).to(torch.int32).contiguous() for i in range(self.k_prop)]
+        self.map_steps = [kb.PageMap(block_table, ctx_len, s) for s in self.seq_steps]
+        self.map_full = kb.PageMap(block_table, ctx_len, seq_len0)
+        # selection, view, fallback flags
+        self.sel_ids = torch.zeros(self.R, self.rows, self.sel_cap, **i32)
+        self.n_sel = torch.zeros(self.R, self.rows, **i32)
+        self.view = kb.View.empty(self.R, self.rows, self.view_cap, dev)
+        self.fallback = torch.zeros(self.R, **i32)
+        # slot mappings: proposals [R][k_prop], verify window [total_q]
+        self.tok_off_prop = (torch.arange(self.R + 1, **i32) * self.k_prop).contiguous()
+        self.slots_prop = torch.zeros(self.R * self.k_prop, dtype=torch.int64, device=dev)
+        self.pos_prop = torch.zeros(self.R * self.k_prop, **i32)
+        q_off = torch.zeros(self.R + 1, dtype=torch.int32)
+        q_off[1:] = torch.cumsum(torch.tensor(n_q_host, dtype=torch.int32), 0)
+        self.q_offsets = q_off.to(dev)
+        self.q_start = seq_len0.to(torch.int32).contiguous()
+        self.slots_ver = torch.zeros(self.total_q, dtype=torch.int64, device=dev)
+        self.pos_ver = torch.zeros(self.total_q, **i32)
+        self.vpol = kb.VerifyPolicy(self.q_offsets, self.q_start, self.max_q, self.total_q)
+        # workspaces (zero-filled once)
+        mp = int(block_table.shape[1])
+        self.ws_score = kb.workspace(kb.kap_score_workspace_size(self.R, self.rows, mp), dev)
+        self.ws_prop = kb.workspace(kb.kap_propose_workspace_size(self.R, self.Hkv, self.Hq, self.d), dev)
+        self.ws_ver = kb.workspace(kb.kap_verify_workspace_size(self.R, self.Hkv, self.Hq, self.d, self.max_q), dev)
+        # outputs
+        dt = pool.dtype
+        self.o_prop = torch.empty(self.k_prop, self.R, self.Hq, self.d, dtype=dt, device=dev)
+        self.lse_prop = torch.empty(self.k_prop, self.R, self.Hq, dtype=torch.float32, device=dev)
+        self.o_ver = torch.empty(self.total_q, self.Hq, self.d, dtype=dt, device=dev)
+        self.lse_ver = torch.empty(self.total_q, self.Hq, dtype=torch.float32, device=dev)
+
+    # -------------------------------------------------------------------------------------------------- phases
+    def plan(self, q_route: torch.Tensor, stream=None):
+        """Selection (scores + A/R/K top-K, or spans), compact view and both slot mappings."""
+        if self.spans is not None:
+            kb.kap_select_spans(self.map_plan, self.spans, self.span_offsets, self.policy, self.sel_ids, self.n_sel,
+                                stream)
+        else:
+            kb.kap_score_topk(self.pool, self.map_plan, q_route, self.policy, self.sel_ids, self.n_sel, self.ws_score,
+                              stream)
+        kb.kap_compile_view(self.map_plan, self.sel_ids, self.n_sel, self.horizon, self.view, self.fallback,
+                            self.s_max, stream)
+        kb.kap_slot_mapping(self.map_plan, self.tok_off_prop, self.map_plan.seq_len, self.slots_prop, self.pos_prop,
+                            stream)
+        kb.kap_slot_mapping(self.map_plan, self.q_offsets, self.q_start, self.slots_ver, self.pos_ver, stream)
+
+    def append_step(self, i: int, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
+        """Proposal step i, first half: the step token's KV at its logical position (q rotated in place)."""
+        kb.kap_append_kv(self.pool, k_new, v_new, q, self.pos_prop[i:], self.slots_prop[i:], self.inv_freq,
+                         num_tokens=self.R, tok_stride=self.k_prop, stream=stream)
+
+    def propose(self, i: int, q: torch.Tensor, stream=None):
+        """Proposal step i, second half: q = 1 attention over the compact view."""
+        kb.kap_attn_propose(self.pool, self.map_steps[i], self.view, q, self.o_prop[i], self.lse_prop[i], self.ws_prop,
+                            stream)
+
+    def propose_step(self, i: int, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
+        self.append_step(i, q, k_new, v_new, stream)
+        self.propose(i, q, stream)
+
+    def append_window(self, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
+        """The verify window's KV into the full-context slots (q rotated in place)."""
+        kb.kap_append_kv(self.pool, k_new, v_new, q, self.pos_ver, self.slots_ver, self.inv_freq, stream=stream)
+
+    def verify(self, q: torch.Tensor, k_new: torch.Tensor = None, v_new: torch.Tensor = None, stream=None):
+        """Causal attention of the window over the full table (after append_window when k_new/v_new are given)."""
+        if k_new is not None:
+            self.append_window(q, k_new, v_new, stream)
+        kb.kap_attn_verify(self.pool, self.map_full, self.vpol, q, self.o_ver, self.lse_ver, self.ws_ver, stream)
+
+    def run(self, q_route, q_prop, k_new_prop, v_new_prop, q_ver, k_new_ver, v_new_ver, stream=None):
+        self.plan(q_route, stream)
+        for i in range(self.k_prop):
+            self.propose_step(i, q_prop[i], k_new_prop[i], v_new_prop[i], stream)
+        self.verify(q_ver, k_new_ver, v_new_ver, stream)
+
+    def launches_per_cycle(self) -> int:
+        """Kernel launches of one run(): plan (2 or 1 selection + view + 2 slot maps) + 2 per step + 2 verify."""
+        sel = 1 if self.spans is not None else 2
+        return sel + 1 + 2 + 2 * self.k_prop + 2

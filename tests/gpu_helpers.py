@@ -1,0 +1,147 @@
+"""Helpers shared by the GPU parity tests: run the library on a workload, and run the oracle on the same inputs.
+
+Only data movement lives here (copies, gathers of one request's pages, slicing); every number the oracle compares
+against is computed by the oracle package.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import selected_kv_sparse_gb300 as kap
+from workloads import make_workload
+
+PAGE = 16
+TOL = {torch.bfloat16: 2e-2, torch.float32: 1e-4}
+LSE_TOL = 1e-3
+
+
+def f32(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to("cpu", torch.float32).numpy()
+
+
+def i32(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().numpy().astype(np.int32)
+
+
+def policy_of(w, cap=None):
+    a, r, k = (int(x) for x in w.ark[0].tolist())
+    same = bool((w.ark == w.ark[0]).all())
+    cap = cap if cap is not None else w.sel_cap()
+    return kap.AccessPolicy(a, r, k, w.per_kv_head, cap, None if same else w.ark.contiguous())
+
+
+def make_cycle(w, cap=None):
+    pool = kap.KVPool(w.K, w.V, w.Hq, torch.zeros(w.num_pages, w.Hkv, w.d, dtype=torch.float32, device=w.K.device))
+    inv = kap.rope_inv_freq(w.d, w.theta, w.K.device)
+    pol = policy_of(w, cap)
+    cyc = kap.DecodeCycle(pool, w.block_table, w.ctx_len, w.seq_len0, w.k_prop, w.n_q, inv, policy=pol,
+                          spans=w.spans, span_offsets=w.span_offsets, sel_cap=pol.cap)
+    return pool, cyc
+
+
+def oracle_selection(w, S_np, q_route_np):
+    """Oracle scores (fixed order) and A/R/K selection, or span selection, as [R][rows][cap] + counts."""
+    bt, ctx = i32(w.block_table), i32(w.ctx_len)
+    R = w.R
+    if w.spans is not None:
+        sp = i32(w.spans)
+        so = i32(w.span_offsets)
+        rows = 1
+        sels = []
+        for r in range(R):
+            N = (int(ctx[r]) + PAGE - 1) // PAGE
+            a, rr, _ = (int(x) for x in w.ark[r].tolist())
+            sels.append([oracle.select_spans(N, sp[so[r]:so[r + 1]], a, rr)])
+    else:
+        rows = w.Hkv if w.per_kv_head else 1
+        sc, _ = oracle.scores(q_route_np, S_np, bt, ctx, per_head=w.per_kv_head)
+        sels = []
+        for r in range(R):
+            N = (int(ctx[r]) + PAGE - 1) // PAGE
+            a, rr, k = (int(x) for x in w.ark[r].tolist())
+            sels.append([oracle.topk_ark(sc[r, v], N, a, rr, k) for v in range(rows)])
+    cap = max(1, max(len(s) for row in sels for s in row))
+    sel = np.zeros((R, rows, cap), np.int32)
+    nsel = np.zeros((R, rows), np.int32)
+    for r in range(R):
+        for v in range(rows):
+            sel[r, v, :len(sels[r][v])] = sels[r][v]
+            nsel[r, v] = len(sels[r][v])
+    return sel, nsel
+
+
+def run_cycle_and_oracle(w, check_rows=None, nthreads=8):
+    """Runs one full cycle on the GPU and the oracle on identical inputs.
+
+    Returns a dict with GPU and oracle results for selection, view, proposal (every step) and verify.
+    The oracle sees the pool exactly as the GPU kernels saw it at each point: proposal step i sees the proposal
+    tokens 0..i appended (RoPE'd by the oracle itself), verify sees the window tokens appended.
+    """
+    dev = w.K.device
+    pool, cyc = make_cycle(w)
+    kap.kap_build_summaries(pool, kap.PageMap(w.block_table, w.ctx_len, w.seq_len0))
+    # snapshot inputs before the cycle mutates them (q is rotated in place, the pool receives new tokens)
+    K0, V0 = f32(w.K), f32(w.V)
+    q_route = w.q_route.clone()
+    q_prop_raw, q_ver_raw = f32(w.q_prop), f32(w.q_ver)
+    q_prop = w.q_prop.clone()
+    q_ver = w.q_ver.clone()
+    cyc.run(q_route, q_prop, w.k_new_prop, w.v_new_prop, q_ver, w.k_new_ver, w.v_new_ver)
+    torch.cuda.synchronize()
+    res = dict(cycle=cyc, pool=pool)
+    res["S_gpu"] = pool.k_summary.cpu().numpy()
+    bt, ctx, seq0 = i32(w.block_table), i32(w.ctx_len), i32(w.seq_len0)
+    S = oracle.build_summaries(K0, bt, ctx)
+    res["S_orc"] = S
+    sel, nsel = oracle_selection(w, S, f32(w.q_route))
+    res["sel_orc"], res["nsel_orc"] = sel, nsel
+    res["sel_gpu"], res["nsel_gpu"] = i32(cyc.sel_ids), i32(cyc.n_sel)
+    inv = oracle.inv_freq(w.d, w.theta)
+    # proposal steps: oracle appends token i (RoPE'd) at position seq0 + i and attends from there
+    K, V = K0.copy(), V0.copy()
+    kp, vp = f32(w.k_new_prop), f32(w.v_new_prop)
+    res["prop"] = []
+    for i in range(w.k_prop):
+        pos = seq0 + i
+        krot = oracle.rope(kp[i], pos, inv)
+        qrot = oracle.rope(q_prop_raw[i], pos, inv)
+        for r in range(w.R):
+            s = oracle.slot(bt[r], int(pos[r]))
+            K[s // PAGE, :, s % PAGE] = krot[r].astype(np.float32) if w.dtype == torch.float32 else \
+                torch.from_numpy(krot[r]).to(torch.bfloat16).float().numpy()
+            V[s // PAGE, :, s % PAGE] = vp[i, r]
+        qin = qrot.astype(np.float32) if w.dtype == torch.float32 else \
+            torch.from_numpy(qrot).to(torch.bfloat16).float().numpy()
+        out, lse = oracle.attn_propose(qin, K, V, bt, ctx, seq0 + i + 1, sel, nsel, nthreads=nthreads)
+        res["prop"].append(dict(o_orc=out, lse_orc=lse, o_gpu=f32(cyc.o_prop[i]), lse_gpu=f32(cyc.lse_prop[i]),
+                                q_gpu=f32(q_prop[i]), q_orc=qrot))
+    # verify: window tokens appended at seq0 .. seq0 + n_q - 1 (overwriting proposal slots)
+    qo = i32(w.q_offsets)
+    kv_, vv_ = f32(w.k_new_ver), f32(w.v_new_ver)
+    posv = np.concatenate([seq0[r] + np.arange(qo[r + 1] - qo[r]) for r in range(w.R)]).astype(np.int32)
+    krot = oracle.rope(kv_, posv, inv)
+    qrot = oracle.rope(q_ver_raw, posv, inv)
+    for r in range(w.R):
+        for j in range(qo[r], qo[r + 1]):
+            s = oracle.slot(bt[r], int(posv[j]))
+            K[s // PAGE, :, s % PAGE] = krot[j].astype(np.float32) if w.dtype == torch.float32 else \
+                torch.from_numpy(krot[j]).to(torch.bfloat16).float().numpy()
+            V[s // PAGE, :, s % PAGE] = vv_[j]
+    qin = qrot.astype(np.float32) if w.dtype == torch.float32 else \
+        torch.from_numpy(qrot).to(torch.bfloat16).float().numpy()
+    out, lse = oracle.attn_verify(qin, K, V, bt, qo, seq0, nthreads=nthreads)
+    res["ver"] = dict(o_orc=out, lse_orc=lse, o_gpu=f32(cyc.o_ver), lse_gpu=f32(cyc.lse_ver))
+    res["K_after_orc"], res["K_after_gpu"] = K, f32(w.K)
+    res["V_after_orc"], res["V_after_gpu"] = V, f32(w.V)
+    return res
+
+
+def assert_close_attn(o_gpu, o_orc, lse_gpu, lse_orc, dtype, what=""):
+    tol = TOL[dtype]
+    assert np.isfinite(o_gpu).all(), f"{what}: non-finite output"
+    err = np.abs(o_gpu.astype(np.float64) - o_orc).max()
+    assert err <= tol, f"{what}: max |o - oracle| = {err:.3e} > {tol}"
+    lerr = np.abs(lse_gpu.astype(np.float64) - lse_orc).max()
+    assert lerr <= LSE_TOL, f"{what}: max |lse - oracle| = {lerr:.3e} > {LSE_TOL}"

@@ -1,0 +1,82 @@
+"""Host-side checks (no GPU): the C-ABI library builds, loads and exports every symbol include/kap.h declares;
+the binding's host helpers agree with the pages' definitions."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "kap.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kap_[a-z_0-9]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from selected_kv_sparse_gb300 import build as kbuild
+    path = kbuild.build()
+    import torch  # noqa: F401  (makes the CUDA runtime library resolvable)
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_five_calls():
+    names = _declared()
+    for n in ("kap_score_topk", "kap_compile_view", "kap_append_kv", "kap_attn_propose", "kap_attn_verify"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings_and_size_queries(lib):
+    lib.kap_status_str.restype = ctypes.c_char_p
+    for s in (0, 1, -1, -2, -3, -4, -5):
+        assert lib.kap_status_str(s)
+    lib.kap_propose_workspace_size.restype = ctypes.c_size_t
+    lib.kap_verify_workspace_size.restype = ctypes.c_size_t
+    lib.kap_score_workspace_size.restype = ctypes.c_size_t
+    assert lib.kap_score_workspace_size(4, 8, 2049) == 4 * 8 * 2049 * 4
+    assert lib.kap_propose_workspace_size(4, 8, 32, 128) > 0
+    assert lib.kap_verify_workspace_size(4, 8, 32, 128, 4) > 0
+    assert lib.kap_verify_workspace_size(0, 8, 32, 128, 4) == 0
+
+
+def test_null_arguments_are_rejected_without_a_gpu(lib):
+    # argument checks run on the host before any CUDA call
+    assert lib.kap_attn_propose(None, None, None, None, None, None, None, ctypes.c_size_t(0), None) == -1
+    assert lib.kap_score_topk(None, None, None, None, None, None, None, ctypes.c_size_t(0), None) == -1
+
+
+def test_parse_ark():
+    from selected_kv_sparse_gb300 import parse_ark
+    assert parse_ark("A1R2K13") == (1, 2, 13)
+    assert parse_ark("A0R0K16") == (0, 0, 16)
+    with pytest.raises(ValueError):
+        parse_ark("R2K13")
+
+
+def test_rope_inv_freq_matches_oracle(orc):
+    from selected_kv_sparse_gb300 import rope_inv_freq
+    for d in (64, 128):
+        assert np.array_equal(rope_inv_freq(d).numpy(), orc.inv_freq(d, 1.0e4))
+
+
+def test_long_spans_recipe():
+    import torch
+    from workloads.gen import _spans_long
+    g = torch.Generator().manual_seed(3)
+    sp = _spans_long(g, 8192)
+    assert len(sp) == 30
+    pages = [(a // 16, n // 16) for a, n in sp]
+    assert sum(n for _, n in pages) == 446
+    assert all(8 <= n <= 32 for _, n in pages)
+    for (a0, n0), (a1, _) in zip(pages, pages[1:]):
+        assert a0 + n0 < a1          # non-overlapping and non-adjacent
+    assert pages[0][0] >= 1 and pages[-1][0] + pages[-1][1] <= 8188
