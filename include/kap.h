@@ -184,6 +184,24 @@ kap_status kap_attn_verify(const kap_kv_pool *pool, const kap_page_map *map, con
 size_t kap_verify_workspace_size(int32_t num_seqs, int32_t num_kv_heads, int32_t num_q_heads, int32_t head_dim,
                                  int32_t max_q);
 
+/* Proposal attention without a caller workspace, for callers that cannot allocate device memory (a serving host
+ * that fixes its device memory budget at start-up and owns the only allocator, a plug-in without access to that
+ * allocator, or a loop where an allocation and its implicit device synchronisation are not allowed). The pages have
+ * no counterpart to this call: it is a deployment variant of kap_attn_propose with identical arguments and results,
+ * minus the workspace.
+ *   - Scratch: a fixed array of kap_noalloc_scratch_bytes() = 16 MiB inside the library, present on every GPU that
+ *     loads the library until the process exits. Shapes whose kap_propose_workspace_size exceeds it are rejected
+ *     with KAP_ECAPACITY.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine. Each call clears the scratch's
+ *     counters with cudaMemsetAsync on `stream`, then launches the same kernel as kap_attn_propose.
+ *   - The first call on a device looks up the scratch's device address (cudaGetSymbolAddress) with that device
+ *     current; make that first call before any stream capture.
+ *   - Every call on a device shares the one scratch array and it keeps the last call's contents: calls that overlap
+ *     on the GPU (different streams, no ordering between them) race and give wrong results. */
+kap_status kap_attn_propose_noalloc(const kap_kv_pool *pool, const kap_page_map *map, const kap_view *view,
+                                    const void *q_dev, void *out, float *lse, kap_stream stream);
+size_t kap_noalloc_scratch_bytes(void);
+
 /* Diagnostics. */
 const char *kap_status_str(kap_status s);
 const char *kap_last_cuda_error(void);   /* text of the last CUDA error seen by this thread, "" if none */

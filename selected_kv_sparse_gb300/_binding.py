@@ -78,6 +78,8 @@ def _declare(lib):
         "kap_status_str": ([I], ctypes.c_char_p),
         "kap_last_cuda_error": ([], ctypes.c_char_p),
         "kap_device_error": ([P], I),
+        "kap_attn_propose_noalloc": ([P, P, P, P, P, P, P], I),
+        "kap_noalloc_scratch_bytes": ([], Z),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -315,6 +317,22 @@ def kap_attn_propose(pool: KVPool, pmap: PageMap, view: View, q: torch.Tensor, o
     _check("kap_attn_propose", lib.kap_attn_propose(ctypes.byref(p), ctypes.byref(m), ctypes.byref(v), _ptr(q),
                                                     _ptr(out), _ptr(lse), _ptr(workspace),
                                                     workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def kap_attn_propose_noalloc(pool: KVPool, pmap: PageMap, view: View, q: torch.Tensor, out: torch.Tensor,
+                             lse: torch.Tensor, stream=None):
+    """kap_attn_propose without a workspace argument: the library's own fixed scratch array is used instead (for
+    callers that may not allocate device memory). Calls that overlap on the GPU share that scratch and race."""
+    lib = load()
+    if q.dtype != pool.dtype or out.dtype != pool.dtype or lse.dtype != torch.float32:
+        raise TypeError("q/out must have the pool dtype and lse fp32")
+    p, m, v = pool._c(), pmap._c(), view._c()
+    _check("kap_attn_propose_noalloc", lib.kap_attn_propose_noalloc(ctypes.byref(p), ctypes.byref(m), ctypes.byref(v),
+                                                                    _ptr(q), _ptr(out), _ptr(lse), _stream(stream)))
+
+
+def kap_noalloc_scratch_bytes() -> int:
+    return int(load().kap_noalloc_scratch_bytes())
 
 
 def kap_verify_workspace_size(R: int, hkv: int, hq: int, d: int, max_q: int) -> int:
