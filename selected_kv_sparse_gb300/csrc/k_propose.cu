@@ -132,25 +132,50 @@ __global__ void __launch_bounds__(kThreads, 3) propose_kernel(const Params p) {
   const int64_t cta_end = static_cast<int64_t>(blockIdx.x + 1) * E / nb;
   if (cta_begin >= cta_end) return;
 
-  // Producer state (thread 0 only): row walk and cursor.
-  int pr_row = 0;
-  int64_t pr_row_begin = 0, pr_row_end = 0, pr_cursor = cta_begin;
-  if (tid == 0) {
-    pr_row_end = row_entries(p, 0);
-    while (pr_row_end <= cta_begin) {  // rows with zero entries are skipped
-      ++pr_row;
-      pr_row_begin = pr_row_end;
-      pr_row_end += row_entries(p, pr_row);
+  // First row of this CTA's range: warp-parallel prefix over the rows' entry counts (no per-row round trips).
+  __shared__ int s_row0;
+  __shared__ int64_t s_rb0, s_re0;
+  if (warp == 0) {
+    int64_t base = 0;
+    for (int b = 0; b < p.nrows; b += 32) {
+      const int row = b + lane;
+      const int c = row < p.nrows ? row_entries(p, row) : 0;
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int nb_ = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += nb_;
+      }
+      const int64_t rb = base + incl - c, re = base + incl;
+      const unsigned hit = __ballot_sync(0xffffffffu, c > 0 && rb <= cta_begin && cta_begin < re);
+      if (hit) {
+        if (lane == __ffs(hit) - 1) {
+          s_row0 = row;
+          s_rb0 = rb;
+          s_re0 = re;
+        }
+        break;
+      }
+      base += __shfl_sync(0xffffffffu, incl, 31);
     }
   }
+  __syncthreads();
+
+  // Producer (all lanes of warp 0, uniform control flow): plan() advances the cursor and starts the loads of the
+  // next chunk's view metadata (lane e loads entry e); commit(buf) consumes them one chunk later, so the load
+  // latency overlaps the compute of the chunk in between.
+  int pr_row = s_row0;
+  int64_t pr_row_begin = s_rb0, pr_row_end = s_re0, pr_cursor = cta_begin;
+  int row_r = -1, row_h = 0, row_vr = 0, row_L = 0, row_S = 0, row_nsel = 0;
+  int pl_n = 0, pl_row = 0, pl_l0 = 0, pl_first = 0, pl_last = 0, pl_lp = 0, pl_page = -1;
+  int pl_L = 0, pl_S = 0, pl_nsel = 0, pl_h = 0;
+  int64_t pl_rb = 0, pl_re = 0;
   const T *Kp = static_cast<const T *>(p.k);
   const T *Vp = static_cast<const T *>(p.v);
 
-  // Issues the next chunk of this CTA's range into ring slot `buf` (thread 0).
-  auto issue = [&](int buf) {
-    Meta<CH> &m = meta[buf];
+  auto plan = [&]() {
     if (pr_cursor >= cta_end) {
-      m.n = 0;
+      pl_n = 0;
       return;
     }
     while (pr_cursor >= pr_row_end) {
@@ -158,56 +183,80 @@ __global__ void __launch_bounds__(kThreads, 3) propose_kernel(const Params p) {
       pr_row_begin = pr_row_end;
       pr_row_end += row_entries(p, pr_row);
     }
-    const int64_t seg_end = min(pr_row_end, cta_end);
-    const int n = static_cast<int>((seg_end - pr_cursor < CH) ? seg_end - pr_cursor : CH);
-    const int l0 = static_cast<int>(pr_cursor - pr_row_begin);
-    m.rb = pr_row_begin;
-    m.re = pr_row_end;
-    m.n = n;
-    m.row = pr_row;
-    m.l0 = l0;
-    m.first = (pr_cursor == pr_row_begin || pr_cursor == cta_begin) ? 1 : 0;
-    m.last = (pr_cursor + n == seg_end) ? 1 : 0;
-    const int r = pr_row / p.hkv, h = pr_row - r * p.hkv;
-    const int vr = view_row(p, pr_row);
-    const int L = p.ctx_len[r], S = p.seq_len[r], nsel = p.vnsel[vr];
-#pragma unroll 1
-    for (int e = 0; e < CH; ++e) {
-      int tlo = 0, thi = 0;
-      if (e < n) {
-        const int i = l0 + e;
-        const int lp = p.vlp[static_cast<size_t>(vr) * p.vcap + i];
-        const int page = p.vbt[static_cast<size_t>(vr) * p.vcap + i];
-        const int base = lp * kPage;
-        thi = min(kPage, S - base);
-        tlo = (i < nsel) ? 0 : max(0, L - base);
-        if (thi > tlo && (page < 0 || page >= p.num_pages)) {
-          set_error(p.err, kErrPage);
-          tlo = thi = 0;
-        }
-        if (thi > tlo) {
-          const size_t off = (static_cast<size_t>(page) * p.hkv + h) * kPage * D;
-          mbar_arrive_expect_tx(&barK[buf * CH + e], C::CHUNK);
-          bulk_g2s(kbuf + (buf * CH + e) * C::CHUNK, Kp + off, C::CHUNK, &barK[buf * CH + e]);
-          mbar_arrive_expect_tx(&barV[buf * CH + e], C::CHUNK);
-          bulk_g2s(vbuf + (buf * CH + e) * C::CHUNK, Vp + off, C::CHUNK, &barV[buf * CH + e]);
-        } else {
-          tlo = thi = 0;
-        }
-      }
-      if (thi <= tlo) {  // keep every slot's barrier phase in step with the ring
-        mbar_arrive(&barK[buf * CH + e]);
-        mbar_arrive(&barV[buf * CH + e]);
-      }
-      m.tlo[e] = tlo;
-      m.thi[e] = thi;
+    if (row_r != pr_row) {  // row-level metadata, loaded once per row
+      row_r = pr_row;
+      const int r = pr_row / p.hkv;
+      row_h = pr_row - r * p.hkv;
+      row_vr = view_row(p, pr_row);
+      row_L = p.ctx_len[r];
+      row_S = p.seq_len[r];
+      row_nsel = p.vnsel[row_vr];
     }
-    pr_cursor += n;
+    const int64_t seg_end = min(pr_row_end, cta_end);
+    pl_n = static_cast<int>((seg_end - pr_cursor < CH) ? seg_end - pr_cursor : CH);
+    pl_l0 = static_cast<int>(pr_cursor - pr_row_begin);
+    pl_row = pr_row;
+    pl_rb = pr_row_begin;
+    pl_re = pr_row_end;
+    pl_first = (pr_cursor == pr_row_begin || pr_cursor == cta_begin) ? 1 : 0;
+    pl_last = (pr_cursor + pl_n == seg_end) ? 1 : 0;
+    pl_L = row_L;
+    pl_S = row_S;
+    pl_nsel = row_nsel;
+    pl_h = row_h;
+    if (lane < pl_n) {
+      const size_t o = static_cast<size_t>(row_vr) * p.vcap + pl_l0 + lane;
+      pl_lp = p.vlp[o];
+      pl_page = p.vbt[o];
+    }
+    pr_cursor += pl_n;
   };
 
-  if (tid == 0) {
-    issue(0);
-    issue(1);
+  auto commit = [&](int buf) {
+    Meta<CH> &m = meta[buf];
+    if (lane == 0) {
+      m.n = pl_n;
+      m.row = pl_row;
+      m.l0 = pl_l0;
+      m.first = pl_first;
+      m.last = pl_last;
+      m.rb = pl_rb;
+      m.re = pl_re;
+    }
+    if (pl_n == 0 || lane >= CH) return;
+    const int e = lane;
+    int tlo = 0, thi = 0;
+    if (e < pl_n) {
+      const int i = pl_l0 + e;
+      const int base = pl_lp * kPage;
+      thi = min(kPage, pl_S - base);
+      tlo = (i < pl_nsel) ? 0 : max(0, pl_L - base);
+      if (thi > tlo && (pl_page < 0 || pl_page >= p.num_pages)) {
+        set_error(p.err, kErrPage);
+        tlo = thi = 0;
+      }
+    }
+    if (thi > tlo) {
+      const size_t off = (static_cast<size_t>(pl_page) * p.hkv + pl_h) * kPage * D;
+      mbar_arrive_expect_tx(&barK[buf * CH + e], C::CHUNK);
+      bulk_g2s(kbuf + (buf * CH + e) * C::CHUNK, Kp + off, C::CHUNK, &barK[buf * CH + e]);
+      mbar_arrive_expect_tx(&barV[buf * CH + e], C::CHUNK);
+      bulk_g2s(vbuf + (buf * CH + e) * C::CHUNK, Vp + off, C::CHUNK, &barV[buf * CH + e]);
+    } else {  // keep every slot's barrier phase in step with the ring
+      tlo = thi = 0;
+      mbar_arrive(&barK[buf * CH + e]);
+      mbar_arrive(&barV[buf * CH + e]);
+    }
+    m.tlo[e] = tlo;
+    m.thi[e] = thi;
+  };
+
+  if (warp == 0) {
+    plan();
+    commit(0);
+    plan();
+    commit(1);
+    plan();
   }
   __syncthreads();
 
@@ -349,7 +398,10 @@ __global__ void __launch_bounds__(kThreads, 3) propose_kernel(const Params p) {
       }
     }
     __syncthreads();
-    if (tid == 0) issue(buf);  // refill this ring slot with chunk c + 2
+    if (warp == 0) {  // refill this ring slot with chunk c + 2, then start loading chunk c + 3's metadata
+      commit(buf);
+      plan();
+    }
     if (!m.last) continue;
 
     // ---- segment end: reduce o over lanes and warps, then finish or hand over a partial
@@ -400,27 +452,74 @@ __global__ void __launch_bounds__(kThreads, 3) propose_kernel(const Params p) {
       }
       __syncthreads();
       if (s_flag) {
+        // Merge of the row's partial records (m, l, o) from CTAs b_first..b_last, with independent loads in
+        // flight: a block-wide max per head, then weights per group of 32 contributors staged in shared memory.
         __threadfence();
-        for (int i = tid; i < G * D; i += kThreads) {
-          const int g = i / D;
-          float M = -INFINITY;
-          for (int b = b_first; b <= b_last; ++b)
-            M = fmaxf(M, __ldcg(p.ml + (static_cast<size_t>(b + m.row) * G + g) * 2));
-          float Lsum = 0.0f, acc = 0.0f;
-          if (M != -INFINITY) {
-            for (int b = b_first; b <= b_last; ++b) {
-              const size_t sl2 = static_cast<size_t>(b + m.row);
-              const float mb = __ldcg(p.ml + (sl2 * G + g) * 2);
-              const float lb = __ldcg(p.ml + (sl2 * G + g) * 2 + 1);
-              const float w = (mb == -INFINITY) ? 0.0f : exp2f(mb - M);
-              Lsum += lb * w;
-              acc += __ldcg(p.part + sl2 * G * D + i) * w;
+        constexpr int kElems = (G * D + kThreads - 1) / kThreads;
+        float mloc[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) mloc[g] = -INFINITY;
+        for (int b = b_first + tid; b <= b_last; b += kThreads)
+#pragma unroll
+          for (int g = 0; g < G; ++g)
+            mloc[g] = fmaxf(mloc[g], __ldcg(p.ml + (static_cast<size_t>(b + m.row) * G + g) * 2));
+        __syncthreads();  // red is free: its content is already in this CTA's partial record
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float v = warp_max(mloc[g]);
+          if (lane == 0) red[warp * G + g] = v;
+        }
+        __syncthreads();
+        float Mg[G], Lg[G], acc[kElems];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          Mg[g] = fmaxf(fmaxf(red[g], red[G + g]), fmaxf(red[2 * G + g], red[3 * G + g]));
+          Lg[g] = 0.0f;
+        }
+#pragma unroll
+        for (int k = 0; k < kElems; ++k) acc[k] = 0.0f;
+        float *wsm = sl;           // [32][G] weights exp2(m_b - M)
+        float *lsm = sl + 32 * G;  // [32][G] l_b * weight
+        for (int b0 = b_first; b0 <= b_last; b0 += 32) {
+          const int nbb = min(32, b_last - b0 + 1);
+          __syncthreads();
+          for (int t = tid; t < nbb * G; t += kThreads) {
+            const int bb = t / G, g = t - (t / G) * G;
+            const size_t slot = static_cast<size_t>(b0 + bb + m.row);
+            const float mb = __ldcg(p.ml + (slot * G + g) * 2);
+            const float lb = __ldcg(p.ml + (slot * G + g) * 2 + 1);
+            const float w = (mb == -INFINITY || Mg[g] == -INFINITY) ? 0.0f : exp2f(mb - Mg[g]);
+            wsm[bb * G + g] = w;
+            lsm[bb * G + g] = lb * w;
+          }
+          __syncthreads();
+#pragma unroll
+          for (int k = 0; k < kElems; ++k) {
+            const int i = tid + k * kThreads;
+            if (i < G * D) {
+              const int g = i / D;
+              float a = 0.0f;
+#pragma unroll 8
+              for (int bb = 0; bb < nbb; ++bb)
+                a = fmaf(__ldcg(p.part + static_cast<size_t>(b0 + bb + m.row) * G * D + i), wsm[bb * G + g], a);
+              acc[k] += a;
             }
           }
-          outp[out_base + i] = from_f<T>(Lsum > 0.0f ? acc / Lsum : 0.0f);
-          if ((i % D) == 0) {
-            p.lse[static_cast<size_t>(r) * p.hq + h * G + g] = Lsum > 0.0f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
-            if (!(Lsum > 0.0f)) set_error(p.err, kErrLength);
+#pragma unroll
+          for (int g = 0; g < G; ++g)
+            for (int bb = 0; bb < nbb; ++bb) Lg[g] += lsm[bb * G + g];
+        }
+#pragma unroll
+        for (int k = 0; k < kElems; ++k) {
+          const int i = tid + k * kThreads;
+          if (i < G * D) {
+            const int g = i / D;
+            const float Ls = Lg[g];
+            outp[out_base + i] = from_f<T>(Ls > 0.0f ? acc[k] / Ls : 0.0f);
+            if ((i % D) == 0) {
+              p.lse[static_cast<size_t>(r) * p.hq + h * G + g] = Ls > 0.0f ? (Mg[g] + log2f(Ls)) * kLn2 : -INFINITY;
+              if (!(Ls > 0.0f)) set_error(p.err, kErrLength);
+            }
           }
         }
       }

@@ -63,35 +63,67 @@ __device__ __forceinline__ int fkey(float x) {
 __device__ __forceinline__ float ffrom(int k) { return __int_as_float(k >= 0 ? k : (k ^ 0x7fffffff)); }
 
 // ============================================================================================ tensor cores
+// Warp roles (224 threads): warps 0-3 softmax + output merge (thread = token row of a tile for the softmax,
+// thread = head-dim row for the merge), warps 4 and 6 TMA producers (K and V), warp 5 tcgen05 issuer. S, P and O are double
+// buffered so that MMA1 of tile t+1 and MMA2 of tile t overlap the softmax of tile t and the merge of tile t-1.
 constexpr int kTileTok = 128;
 constexpr int kHalfBytes = 8 * kPage * 128;  // one 64-column half of a tile: 8 pages x 16 rows x 128 B = 16 KiB
 constexpr int kStageBytes = 2 * kHalfBytes;   // 32 KiB of K (or V) per stage
+constexpr int kTcThreads = 224;
+constexpr float kRescaleThreshold = 8.0f;     // log2 units: keep a running max until a tile exceeds it by 2^8
 
 struct TileMeta {
   int64_t rb, re;
-  int valid, row, tile, first, last, npg, seq;
+  int valid, row, tile, first, last, npg, seg, nq, qpos0, qoff, pad;
 };
 
 template <int NPMAX>
 struct TcSmem {
-  static constexpr int kStages = NPMAX <= 48 ? 3 : 2;  // stay under 227 KB of shared memory
+  static constexpr int KATOM = NPMAX * 128;  // bytes of one 64-column K-atom of an [NPMAX x 128] bf16 operand
+  static constexpr int QP_BYTES = 4 * 2 * KATOM;  // Q[2] and P[2]
+  static constexpr int kStages = (3 * 2 * kStageBytes + QP_BYTES + 4096 <= 227 * 1024) ? 3 : 2;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + kStages * kStageBytes;
-  static constexpr int OFF_Q = OFF_V + kStages * kStageBytes;
-  static constexpr int KATOM = NPMAX * 128;  // bytes of one 64-column K-atom of an [NPMAX x 128] operand
-  static constexpr int OFF_P = OFF_Q + 2 * KATOM;
-  static constexpr int OFF_CM = OFF_P + 2 * KATOM;       // column maxima [4][NPMAX]
-  static constexpr int OFF_ST = OFF_CM + 4 * NPMAX * 4;  // m_run, m_new, alpha, lsum [4][NPMAX]
-  static constexpr int OFF_BAR = OFF_ST + 4 * NPMAX * 4;
-  static constexpr int OFF_META = OFF_BAR + (2 * kStages + 2) * 8;
-  static constexpr int OFF_TMEM = OFF_META + kStages * static_cast<int>(sizeof(TileMeta));
+  static constexpr int OFF_Q = OFF_V + kStages * kStageBytes;     // Q[2] (segment parity)
+  static constexpr int OFF_P = OFF_Q + 2 * 2 * KATOM;              // P[2] (tile parity)
+  static constexpr int OFF_CM = OFF_P + 2 * 2 * KATOM;             // column maxima [4][NPMAX]
+  static constexpr int OFF_ST = OFF_CM + 4 * NPMAX * 4;            // m_run, lsum, alpha[2] : [4][NPMAX]
+  static constexpr int OFF_FLAG = OFF_ST + 4 * NPMAX * 4;          // rescale flag per tile parity [2]
+  static constexpr int OFF_BAR = OFF_FLAG + 16;
+  static constexpr int kMetaRing = 2 * kStages;  // tile metadata outlives its K stage (read until MMA2 and softmax)
+  // kfull, vfull, kempty, vempty [kStages]; sfull, sfree, pfull, ofull, ofree, qfull, qempty [2];
+  // mfull, mfree [kMetaRing]
+  static constexpr int NBAR = 4 * kStages + 14 + 2 * kMetaRing;
+  static constexpr int OFF_META = OFF_BAR + NBAR * 8;
+  static constexpr int OFF_TMEM = OFF_META + kMetaRing * static_cast<int>(sizeof(TileMeta));
   static constexpr int BYTES = OFF_TMEM + 16;
   static constexpr int ALLOC = BYTES + 1024;  // room to align the base to 1024 bytes
-  static constexpr int TMEM_COLS = (2 * NPMAX <= 32) ? 32 : (2 * NPMAX <= 64 ? 64 : 128);
+  static constexpr int TMEM_COLS = (4 * NPMAX <= 32) ? 32 : (4 * NPMAX <= 64 ? 64 : (4 * NPMAX <= 128 ? 128 : 256));
 };
 
+// 2^x with the hardware approximation (relative error about 2^-22; the result is rounded to bf16 for P anyway).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void named_sync_128() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ bool named_or_128(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(v ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
+
 template <int NPMAX>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(kTcThreads, 1)
     verify_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const VParams p) {
   using L = TcSmem<NPMAX>;
@@ -105,21 +137,23 @@ __global__ void __launch_bounds__(128, 1)
   unsigned char *Ps = sm + L::OFF_P;
   float *colmax = reinterpret_cast<float *>(sm + L::OFF_CM);
   float *m_run = reinterpret_cast<float *>(sm + L::OFF_ST);
-  float *m_new = m_run + NPMAX;
-  float *alpha = m_new + NPMAX;
-  float *lsum = alpha + NPMAX;
-  uint64_t *barK = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
-  uint64_t *barV = barK + kStages;
-  uint64_t *bar_s = barV + kStages;
-  uint64_t *bar_o = bar_s + 1;
+  float *lsum = m_run + NPMAX;
+  float *alpha_s = lsum + NPMAX;  // [2][NPMAX]
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
+  constexpr int kMR = L::kMetaRing;
+  uint64_t *kfull = bars, *vfull = bars + kStages, *kempty = bars + 2 * kStages, *vempty = bars + 3 * kStages;
+  uint64_t *sfull = bars + 4 * kStages, *sfree = sfull + 2, *pfull = sfree + 2, *ofull = pfull + 2;
+  uint64_t *ofree = ofull + 2, *qfull = ofree + 2, *qempty = qfull + 2, *mfree = qempty + 2;
+  uint64_t *mfull = mfree + kMR;
   TileMeta *meta = reinterpret_cast<TileMeta *>(sm + L::OFF_META);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::OFF_TMEM);
   __shared__ int64_t s_total;
-  __shared__ int s_flag, s_abort;
+  __shared__ int s_flag, s_abort, s_row0;
+  volatile int *abort_flag = &s_abort;
+  __shared__ int64_t s_rb0, s_re0;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = p.hq / p.hkv;
-  if (tid == 0) s_abort = 0;
 
   if (warp == 0) {
     int64_t tot = 0;
@@ -132,15 +166,15 @@ __global__ void __launch_bounds__(128, 1)
     if (lane == 0) s_total = tot;
   }
   if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(&barK[i], 1);
-      mbar_init(&barV[i], 1);
+    s_abort = 0;
+    for (int i = 0; i < L::NBAR; ++i) mbar_init(&bars[i], 1);
+    for (int b = 0; b < 2; ++b) {  // barriers the 4 softmax warps arrive on (one elected lane per warp)
+      mbar_init(&sfree[b], 4);
+      mbar_init(&pfull[b], 4);
+      mbar_init(&ofree[b], 4);
     }
-    mbar_init(bar_s, 1);
-    mbar_init(bar_o, 1);
+    for (int i = 0; i < kMR; ++i) mbar_init(&mfree[i], 5);  // 4 softmax warps + the MMA issuer
     fence_barrier_init();
-    prefetch_tmap(&tmK);
-    prefetch_tmap(&tmV);
   }
   __syncthreads();
   const int64_t E = s_total;
@@ -150,7 +184,30 @@ __global__ void __launch_bounds__(128, 1)
   const int64_t cta_begin = static_cast<int64_t>(blockIdx.x) * E / nb;
   const int64_t cta_end = static_cast<int64_t>(blockIdx.x + 1) * E / nb;
 
+  // First row of this CTA's range: warp-parallel prefix over the rows' tile counts.
   if (warp == 0) {
+    int64_t base = 0;
+    for (int b = 0; b < p.nrows; b += 32) {
+      const int row = b + lane;
+      const int c = row < p.nrows ? row_tiles(p, row) : 0;
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      const int64_t rb = base + incl - c, re = base + incl;
+      const unsigned hit = __ballot_sync(0xffffffffu, c > 0 && rb <= cta_begin && cta_begin < re);
+      if (hit) {
+        if (lane == __ffs(hit) - 1) {
+          s_row0 = row;
+          s_rb0 = rb;
+          s_re0 = re;
+        }
+        break;
+      }
+      base += __shfl_sync(0xffffffffu, incl, 31);
+    }
     tmem_alloc(tmem_slot, L::TMEM_COLS);
     tmem_relinquish();
   }
@@ -158,312 +215,490 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_S = tmem;
-  const uint32_t tmem_O = tmem + NPMAX;
 
-  // producer state (thread 0)
-  int pr_row = 0, pr_seq = 0;
-  int64_t pr_rb = 0, pr_re = 0, pr_cur = cta_begin;
-  if (tid == 0) {
-    pr_re = row_tiles(p, 0);
-    while (pr_re <= cta_begin) {
-      ++pr_row;
-      pr_rb = pr_re;
-      pr_re += row_tiles(p, pr_row);
+  if (warp == 4 || warp == 6) {
+    // ============================================================================================== producers
+    // Warp 4 issues the K boxes of each tile (and writes the tile metadata and the Q operand), warp 6 the V
+    // boxes: both walk the same tile sequence, so their 16 TMA requests per tile are issued in parallel.
+    const bool kprod = (warp == 4);
+    int pr_row = s_row0, seg = -1;
+    int64_t pr_rb = s_rb0, pr_re = s_re0, pr_cur = cta_begin;
+    int row_r = -1, row_kvp = 0, row_nq_ = 0, row_qpos0 = 0, row_qoff = 0;
+    int pl_row = 0, pl_tile = 0, pl_first = 0, pl_last = 0, pl_npg = 0, pl_h = 0, pl_page = -1, pl_valid = 0;
+    int64_t pl_rb = 0, pl_re = 0;
+    auto plan = [&]() {
+      if (pr_cur >= cta_end) {
+        pl_valid = 0;
+        return;
+      }
+      while (pr_cur >= pr_re) {
+        ++pr_row;
+        pr_rb = pr_re;
+        pr_re += row_tiles(p, pr_row);
+      }
+      const int r = pr_row / p.hkv;
+      if (row_r != r) {
+        row_r = r;
+        row_nq_ = row_nq(p, r);
+        row_qpos0 = p.q_start[r];
+        row_qoff = p.q_offsets[r];
+        row_kvp = (row_qpos0 + row_nq_ + kPage - 1) / kPage;
+      }
+      const int64_t seg_end = min(pr_re, cta_end);
+      pl_valid = 1;
+      pl_row = pr_row;
+      pl_h = pr_row - r * p.hkv;
+      pl_tile = static_cast<int>(pr_cur - pr_rb);
+      pl_rb = pr_rb;
+      pl_re = pr_re;
+      pl_first = (pr_cur == pr_rb || pr_cur == cta_begin) ? 1 : 0;
+      pl_last = (pr_cur + 1 == seg_end) ? 1 : 0;
+      pl_npg = min(8, row_kvp - pl_tile * 8);
+      pl_page = -1;
+      if (lane < pl_npg && pl_tile * 8 + lane < p.max_pages)
+        pl_page = p.bt[static_cast<size_t>(r) * p.max_pages + pl_tile * 8 + lane];
+      ++pr_cur;
+    };
+    plan();
+    int t = 0;
+    for (;; ++t) {
+      const int st = t % kStages, mi = t % kMR;
+      if (t >= kStages && !mbar_wait(kprod ? &kempty[st] : &vempty[st], ((t / kStages) - 1) & 1, p.err)) {
+        *abort_flag = 1;
+        break;
+      }
+      if (kprod && t >= kMR && !mbar_wait(&mfree[mi], ((t / kMR) - 1) & 1, p.err)) {
+        *abort_flag = 1;
+        break;
+      }
+      if (*abort_flag) break;
+      TileMeta &m = meta[mi];
+      if (!pl_valid) {
+        if (kprod && lane == 0) {
+          m.valid = 0;
+          mbar_arrive(&mfull[mi]);
+          mbar_arrive(&kfull[st]);
+        }
+        break;
+      }
+      if (pl_first && kprod) {
+        // Q rows n = i*G + g of this (request, KV head) into Q[seg parity], K-major with 128-byte swizzle.
+        ++seg;
+        const int qb = seg & 1;
+        if (seg >= 2 && !mbar_wait(&qempty[qb], ((seg >> 1) - 1) & 1, p.err)) {
+          *abort_flag = 1;
+          break;
+        }
+        const int nreal = row_nq_ * G;
+        const int qoff = row_qoff;
+        const __nv_bfloat16 *qg = static_cast<const __nv_bfloat16 *>(p.q);
+        unsigned char *qd = Qs + qb * 2 * L::KATOM;
+        for (int idx = lane; idx < NPMAX * 16; idx += 32) {
+          const int n = idx >> 4, c = idx & 15;
+          uint4 val = make_uint4(0, 0, 0, 0);
+          if (n < nreal) {
+            const int i = n / G, g = n - (n / G) * G;
+            val = *reinterpret_cast<const uint4 *>(qg + (static_cast<size_t>(qoff + i) * p.hq + pl_h * G + g) * 128 +
+                                                   c * 8);
+          }
+          const int katom = c >> 3, cc = c & 7;
+          *reinterpret_cast<uint4 *>(qd + katom * L::KATOM + (n >> 3) * 1024 + (n & 7) * 128 + ((cc ^ (n & 7)) << 4)) =
+              val;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&qfull[qb]);
+      }
+      const bool in_tile = lane < pl_npg;
+      const bool ok = in_tile && pl_page >= 0 && pl_page < p.num_pages;
+      if (in_tile && !ok) set_error(p.err, kErrPage);
+      const int nvalid = __popc(__ballot_sync(0xffffffffu, ok));
+      if (!kprod) {
+        if (lane == 0) mbar_arrive_expect_tx(&vfull[st], nvalid * 2 * 2048);
+        __syncwarp();
+        if (ok) {
+          unsigned char *vd = Vs + st * kStageBytes;
+          const int row0 = (pl_page * p.hkv + pl_h) * kPage;
+          tma_load_2d(vd + lane * 2048, &tmV, 0, row0, &vfull[st]);
+          tma_load_2d(vd + kHalfBytes + lane * 2048, &tmV, 64, row0, &vfull[st]);
+        }
+        plan();
+        continue;
+      }
+      if (lane == 0) {
+        m.valid = 1;
+        m.rb = pl_rb;
+        m.re = pl_re;
+        m.row = pl_row;
+        m.tile = pl_tile;
+        m.first = pl_first;
+        m.last = pl_last;
+        m.npg = pl_npg;
+        m.seg = seg;
+        m.nq = row_nq_;
+        m.qpos0 = row_qpos0;
+        m.qoff = row_qoff;
+        mbar_arrive(&mfull[mi]);
+        mbar_arrive_expect_tx(&kfull[st], nvalid * 2 * 2048);
+      }
+      __syncwarp();
+      if (ok) {
+        unsigned char *kd = Ks + st * kStageBytes;
+        const int row0 = (pl_page * p.hkv + pl_h) * kPage;
+        tma_load_2d(kd + lane * 2048, &tmK, 0, row0, &kfull[st]);
+        tma_load_2d(kd + kHalfBytes + lane * 2048, &tmK, 64, row0, &kfull[st]);
+      }
+      plan();
     }
-  }
-  auto issue = [&](int st) {
-    TileMeta &m = meta[st];
-    if (pr_cur >= cta_end) {
-      m.valid = 0;
-      return;
-    }
-    while (pr_cur >= pr_re) {
-      ++pr_row;
-      pr_rb = pr_re;
-      pr_re += row_tiles(p, pr_row);
-    }
-    const int64_t seg_end = min(pr_re, cta_end);
-    const int r = pr_row / p.hkv, h = pr_row - r * p.hkv;
-    const int tile = static_cast<int>(pr_cur - pr_rb);
-    const int kv_pages = (p.q_start[r] + row_nq(p, r) + kPage - 1) / kPage;
-    const int npg = min(8, kv_pages - tile * 8);
-    m.valid = 1;
-    m.rb = pr_rb;
-    m.re = pr_re;
-    m.row = pr_row;
-    m.tile = tile;
-    m.first = (pr_cur == pr_rb || pr_cur == cta_begin) ? 1 : 0;
-    m.last = (pr_cur + 1 == seg_end) ? 1 : 0;
-    m.npg = npg;
-    m.seq = pr_seq++;
-    int pages[8];
-    int nvalid = 0;
-    const int32_t *btr = p.bt + static_cast<size_t>(r) * p.max_pages;
-    for (int i = 0; i < 8; ++i) {
-      pages[i] = -1;
-      if (i < npg && tile * 8 + i < p.max_pages) {
-        const int pg = btr[tile * 8 + i];
-        if (pg >= 0 && pg < p.num_pages) {
-          pages[i] = pg;
-          ++nvalid;
-        } else {
-          set_error(p.err, kErrPage);
+    // copies still in flight after an abort are waited for (bounded) before the CTA leaves
+    if (*abort_flag && lane == 0)
+      for (int u = max(0, t - kStages + 1); u <= t; ++u)
+        mbar_wait(kprod ? &kfull[u % kStages] : &vfull[u % kStages], (u / kStages) & 1, nullptr);
+  } else if (warp == 5) {
+    // ============================================================================================ MMA issuer
+    // Issues whichever MMA is ready first: MMA1(t1) as soon as K(t1) has landed and S[t1 parity] is free, MMA2(t2)
+    // as soon as P(t2) is written. Issuing MMA2 early frees the K/V stage (kvempty) for the producer sooner.
+    if (lane == 0) {
+      int seg = -1, t1 = 0, t2 = 0;
+      bool done1 = false, okrun = true;
+      uint32_t idle = 0;
+      while (true) {
+        if (*abort_flag) {
+          okrun = false;
+          break;
+        }
+        bool progressed = false;
+        if (!done1) {
+          const int st = t1 % kStages, b = t1 & 1;
+          if (mbar_test(&kfull[st], (t1 / kStages) & 1)) {
+            const TileMeta m = meta[t1 % kMR];
+            if (!m.valid) {
+              done1 = true;
+              progressed = true;
+            } else if ((!m.first || mbar_test(&qfull[(seg + 1) & 1], ((seg + 1) >> 1) & 1)) &&
+                       (t1 < 2 || mbar_test(&sfree[b], ((t1 >> 1) - 1) & 1))) {
+              if (m.first) ++seg;
+              tc_fence_after();
+              const int npad = (m.nq * G + 15) & ~15;
+              const uint32_t idesc = idesc_bf16(128, npad, 0, 0);
+              const uint32_t kb = smem_u32(Ks + st * kStageBytes), qb = smem_u32(Qs + (seg & 1) * 2 * L::KATOM);
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t ad = smem_desc(kb + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024, 2);
+                const uint64_t bd = smem_desc(qb + (kk >> 2) * L::KATOM + (kk & 3) * 32, 16, 1024, 2);
+                umma_bf16(tmem + b * NPMAX, ad, bd, idesc, kk > 0 ? 1u : 0u);
+              }
+              umma_commit(&sfull[b]);
+              umma_commit(&kempty[st]);
+              if (m.last) umma_commit(&qempty[seg & 1]);
+              ++t1;
+              progressed = true;
+            }
+          }
+        }
+        if (t2 < t1) {
+          const int su = t2 % kStages, b = t2 & 1;
+          if (mbar_test(&pfull[b], (t2 >> 1) & 1) && mbar_test(&vfull[su], (t2 / kStages) & 1) &&
+              (t2 < 2 || mbar_test(&ofree[b], ((t2 >> 1) - 1) & 1))) {
+            tc_fence_after();
+            // meta of tile t2 stays valid until this issuer (and the softmax warps) release its ring slot
+            const int npad = (meta[t2 % kMR].nq * G + 15) & ~15;
+            const uint32_t idesc = idesc_bf16(128, npad, 1, 0);
+            const uint32_t vb = smem_u32(Vs + su * kStageBytes), pb = smem_u32(Ps + b * 2 * L::KATOM);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t ad = smem_desc(vb + kk * 2048, kHalfBytes, 1024, 2);
+              const uint64_t bd = smem_desc(pb + (kk >> 2) * L::KATOM + (kk & 3) * 32, 16, 1024, 2);
+              umma_bf16(tmem + 2 * NPMAX + b * NPMAX, ad, bd, idesc, kk > 0 ? 1u : 0u);
+            }
+            umma_commit(&ofull[b]);
+            umma_commit(&vempty[su]);
+            mbar_arrive(&mfree[t2 % kMR]);
+            ++t2;
+            progressed = true;
+          }
+        }
+        if (done1 && t2 == t1) break;
+        if (progressed) {
+          idle = 0;
+        } else if (++idle > 16u * kWaitPolls) {
+          set_error(p.err, kErrTimeout);
+          okrun = false;
+          break;
         }
       }
+      if (!okrun) *abort_flag = 1;
     }
-    mbar_arrive_expect_tx(&barK[st], nvalid * 2 * 2048);
-    mbar_arrive_expect_tx(&barV[st], nvalid * 2 * 2048);
-    unsigned char *kd = Ks + st * kStageBytes;
-    unsigned char *vd = Vs + st * kStageBytes;
-    for (int i = 0; i < 8; ++i) {
-      if (pages[i] < 0) continue;
-      const int row0 = (pages[i] * p.hkv + h) * kPage;
-      tma_load_2d(kd + i * 2048, &tmK, 0, row0, &barK[st]);
-      tma_load_2d(kd + kHalfBytes + i * 2048, &tmK, 64, row0, &barK[st]);
-      tma_load_2d(vd + i * 2048, &tmV, 0, row0, &barV[st]);
-      tma_load_2d(vd + kHalfBytes + i * 2048, &tmV, 64, row0, &barV[st]);
-    }
-    ++pr_cur;
-  };
-  if (tid == 0)
-    for (int st = 0; st < kStages; ++st) issue(st);
-  __syncthreads();
-
-  const float scale2 = rsqrtf(128.0f) * kLog2e;
-  float lt[NPMAX];  // softmax role (thread = token): this token's share of each column's sum
-  float oreg[NPMAX];  // merge role (thread = head-dim row): running output of each column
-#pragma unroll
-  for (int n = 0; n < NPMAX; ++n) {
-    lt[n] = 0.0f;
-    oreg[n] = 0.0f;
-  }
-  bool abort = false;
-  int t_end = 0;
-
-  for (int t = 0;; ++t) {
-    t_end = t;
-    const int st = t % kStages;
-    const uint32_t ph = (t / kStages) & 1;
-    const TileMeta m = meta[st];
-    if (!m.valid) break;
-    const int r = m.row / p.hkv, h = m.row - r * p.hkv;
-    const int nq = row_nq(p, r);
-    const int nreal = nq * G;
-    const int npad = (nreal + 15) & ~15;
-    const int qpos0 = p.q_start[r];
-    const int qoff = p.q_offsets[r];
-    if (m.first) {
-      // Q rows n = i*G + g of this (request, KV head), K-major with 128-byte swizzle; zero padding rows.
-      const __nv_bfloat16 *qg = static_cast<const __nv_bfloat16 *>(p.q);
-      for (int idx = tid; idx < NPMAX * 16; idx += 128) {
-        const int n = idx >> 4, c = idx & 15;
-        uint4 val = make_uint4(0, 0, 0, 0);
-        if (n < nreal) {
-          const int i = n / G, g = n - (n / G) * G;
-          val = *reinterpret_cast<const uint4 *>(qg + (static_cast<size_t>(qoff + i) * p.hq + h * G + g) * 128 + c * 8);
-        }
-        const int katom = c >> 3, cc = c & 7;
-        *reinterpret_cast<uint4 *>(Qs + katom * L::KATOM + (n >> 3) * 1024 + (n & 7) * 128 + ((cc ^ (n & 7)) << 4)) = val;
-      }
-      fence_proxy_async_smem();
-      if (tid < NPMAX) {
-        m_run[tid] = -INFINITY;
-        lsum[tid] = 0.0f;
-      }
-#pragma unroll
-      for (int n = 0; n < NPMAX; ++n) {
-        lt[n] = 0.0f;
-        oreg[n] = 0.0f;
-      }
-    }
-    __syncthreads();
-    // ---- S^T = K . Q^T
-    if (tid == 0) {
-      if (!mbar_wait(&barK[st], ph, p.err)) abort = true;
-      tc_fence_after();
-      const uint32_t idesc = idesc_bf16(128, npad, 0, 0);
-      const uint32_t kb = smem_u32(Ks + st * kStageBytes), qb = smem_u32(Qs);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint64_t ad = smem_desc(kb + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024, 2);
-        const uint64_t bd = smem_desc(qb + (kk >> 2) * L::KATOM + (kk & 3) * 32, 16, 1024, 2);
-        umma_bf16(tmem_S, ad, bd, idesc, kk > 0 ? 1u : 0u);
-      }
-      umma_commit(bar_s);
-    }
-    if (!mbar_wait(bar_s, t & 1, p.err)) abort = true;
-    tc_fence_after();
-    // ---- softmax over the tile's tokens (thread = token)
-    const int pos = m.tile * kTileTok + tid;
-    float x[NPMAX];
+    __syncwarp();
+  } else if (warp < 4) {
+    // ==================================================================================== softmax and merge
+    const float scale2 = rsqrtf(128.0f) * kLog2e;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-#pragma unroll
-    for (int c = 0; c < NPMAX / 16; ++c)
-      if (c * 16 < npad) tmem_ld16(tmem_S + lane_base + c * 16, x + c * 16);
-    tmem_wait_ld();
-    tc_fence_before();
+    float lt[NPMAX];    // softmax role (thread = token): this token's share of each column's sum
+    float oreg[NPMAX];  // merge role (thread = head-dim row): running output of each column
 #pragma unroll
     for (int n = 0; n < NPMAX; ++n) {
-      const int i = n / G;
-      const bool vis = n < nreal && pos <= qpos0 + i;
-      x[n] = vis ? x[n] * scale2 : -INFINITY;
-      const int wmax = __reduce_max_sync(0xffffffffu, fkey(x[n]));
-      if (lane == 0) colmax[warp * NPMAX + n] = ffrom(wmax);
+      lt[n] = 0.0f;
+      oreg[n] = 0.0f;
     }
-    __syncthreads();
-    if (tid < NPMAX) {
-      const float cm = fmaxf(fmaxf(colmax[tid], colmax[NPMAX + tid]), fmaxf(colmax[2 * NPMAX + tid], colmax[3 * NPMAX + tid]));
-      const float mo = m_run[tid];
-      const float mn = fmaxf(mo, cm);
-      alpha[tid] = (mn == -INFINITY) ? 1.0f : exp2f(mo - mn);
-      m_new[tid] = mn;
-      m_run[tid] = mn;
-    }
-    __syncthreads();
-    {
-      const int katom = tid >> 6, c = (tid & 63) >> 3, e = tid & 7;
-#pragma unroll
-      for (int n = 0; n < NPMAX; ++n) {
-        const float pv = (x[n] == -INFINITY) ? 0.0f : exp2f(x[n] - m_new[n]);
-        lt[n] = lt[n] * alpha[n] + pv;
-        *reinterpret_cast<__nv_bfloat16 *>(Ps + katom * L::KATOM + (n >> 3) * 1024 + (n & 7) * 128 +
-                                          ((c ^ (n & 7)) << 4) + e * 2) = __float2bfloat16_rn(pv);
-      }
-    }
-    // tokens past the last query position carry no weight; their V rows may hold anything (even NaN) and
-    // must not reach the tensor core: zero them
-    if (pos > qpos0 + nq - 1) {
-      if (!mbar_wait(&barV[st], ph, p.err)) abort = true;
-      unsigned char *vrow0 = Vs + st * kStageBytes + (tid >> 4) * 2048 + (tid & 15) * 128;
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4 *>(vrow0 + hh * kHalfBytes + c * 16) = make_uint4(0, 0, 0, 0);
-    }
-    fence_proxy_async_smem();
-    __syncthreads();
-    // ---- O^T = V^T . P^T
-    if (tid == 0) {
-      if (!mbar_wait(&barV[st], ph, p.err)) abort = true;
+    auto merge = [&](int u, int npad_u, bool resc_u) -> bool {
+      const int b = u & 1;
+      if (!mbar_wait(&ofull[b], (u >> 1) & 1, p.err)) return false;
       tc_fence_after();
-      const uint32_t idesc = idesc_bf16(128, npad, 1, 0);
-      const uint32_t vb = smem_u32(Vs + st * kStageBytes), pb = smem_u32(Ps);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint64_t ad = smem_desc(vb + kk * 2048, kHalfBytes, 1024, 2);
-        const uint64_t bd = smem_desc(pb + (kk >> 2) * L::KATOM + (kk & 3) * 32, 16, 1024, 2);
-        umma_bf16(tmem_O, ad, bd, idesc, kk > 0 ? 1u : 0u);
-      }
-      umma_commit(bar_o);
-    }
-    if (!mbar_wait(bar_o, t & 1, p.err)) abort = true;
-    tc_fence_after();
-    {
       float ot[NPMAX];
 #pragma unroll
       for (int c = 0; c < NPMAX / 16; ++c)
-        if (c * 16 < npad) tmem_ld16(tmem_O + lane_base + c * 16, ot + c * 16);
+        if (c * 16 < npad_u) tmem_ld16(tmem + 2 * NPMAX + b * NPMAX + lane_base + c * 16, ot + c * 16);
       tmem_wait_ld();
       tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ofree[b]);
+      if (resc_u) {
 #pragma unroll
-      for (int n = 0; n < NPMAX; ++n)
-        if (n < npad) oreg[n] = oreg[n] * alpha[n] + ot[n];
-    }
-    if (abort) s_abort = 1;
-    __syncthreads();
-    if (s_abort) {
-      t_end = t + 1;
-      break;
-    }
-    if (tid == 0) issue(st);  // tile t + kStages into this stage
-    if (!m.last) continue;
-
-    // ---- end of this row segment: column sums, then finish or hand over a partial record
+        for (int n = 0; n < NPMAX; ++n)
+          if (n < npad_u) oreg[n] = fmaf(oreg[n], alpha_s[b * NPMAX + n], ot[n]);
+      } else {
 #pragma unroll
-    for (int n = 0; n < NPMAX; ++n) {
-      if (n < npad) {
-        const float v = warp_sum(lt[n]);
-        if (lane == 0) atomicAdd(&lsum[n], v);
+        for (int n = 0; n < NPMAX; ++n)
+          if (n < npad_u) oreg[n] += ot[n];
       }
-    }
-    __syncthreads();
-    const int b_first = owner_cta(m.rb, E, nb), b_last = owner_cta(m.re - 1, E, nb);
-    const int ncontrib = b_last - b_first + 1;
-    __nv_bfloat16 *outp = static_cast<__nv_bfloat16 *>(p.out);
-    if (ncontrib == 1) {
+      return true;
+    };
+    int pending = -1, pending_npad = 16;  // tile whose O is not merged yet
+    bool pending_resc = false;
+    bool okrun = true;
+    for (int t = 0;; ++t) {
+      const int st = t % kStages, b = t & 1;
+      if (*abort_flag || !mbar_wait(&mfull[t % kMR], (t / kMR) & 1, p.err)) {
+        okrun = false;
+        break;
+      }
+      const TileMeta m = meta[t % kMR];
+      if (!m.valid) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&mfree[t % kMR]);
+      const int r = m.row / p.hkv, h = m.row - r * p.hkv;
+      const int nq = m.nq;
+      const int nreal = nq * G;
+      const int npad = (nreal + 15) & ~15;
+      const int qpos0 = m.qpos0;
+      const int qoff = m.qoff;
+      if (m.first) {
+        if (tid < NPMAX) {
+          m_run[tid] = -INFINITY;
+          lsum[tid] = 0.0f;
+        }
+#pragma unroll
+        for (int n = 0; n < NPMAX; ++n) {
+          lt[n] = 0.0f;
+          oreg[n] = 0.0f;
+        }
+        named_sync_128();
+      }
+      // ---- S tile from TMEM (thread = token)
+      if (!mbar_wait(&sfull[b], (t >> 1) & 1, p.err)) {
+        okrun = false;
+        break;
+      }
+      tc_fence_after();
+      float x[NPMAX];
+#pragma unroll
+      for (int c = 0; c < NPMAX / 16; ++c)
+        if (c * 16 < npad) tmem_ld16(tmem + b * NPMAX + lane_base + c * 16, x + c * 16);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sfree[b]);
+      const int pos = m.tile * kTileTok + tid;
+      float mr[NPMAX];
+      bool over = false;
+      // column n is window row n / G: visible when this token's position is at most qpos0 + n / G
+      const int rel = pos - qpos0;  // the token is visible to window rows i >= rel
+      const int n_first = rel <= 0 ? 0 : rel * G;
 #pragma unroll
       for (int n = 0; n < NPMAX; ++n) {
-        if (n < nreal) {
-          const int i = n / G, g = n - (n / G) * G;
-          const float l = lsum[n];
-          outp[(static_cast<size_t>(qoff + i) * p.hq + h * G + g) * 128 + tid] =
-              __float2bfloat16_rn(l > 0.0f ? oreg[n] / l : 0.0f);
+        const bool vis = n < nreal && n >= n_first;
+        x[n] = vis ? x[n] * scale2 : -INFINITY;
+        mr[n] = m_run[n];
+        over |= x[n] > mr[n] + kRescaleThreshold;
+      }
+      // ---- running max: only when some logit of this tile exceeds it by more than 2^8
+      const bool rescale = named_or_128(over);
+      if (rescale) {
+#pragma unroll
+        for (int n = 0; n < NPMAX; ++n) {
+          const int wmax = __reduce_max_sync(0xffffffffu, fkey(x[n]));
+          if (lane == 0) colmax[warp * NPMAX + n] = ffrom(wmax);
+        }
+        named_sync_128();
+        if (tid < NPMAX) {
+          const float cm = fmaxf(fmaxf(colmax[tid], colmax[NPMAX + tid]),
+                                 fmaxf(colmax[2 * NPMAX + tid], colmax[3 * NPMAX + tid]));
+          const float mo = m_run[tid];
+          const float mn = fmaxf(mo, cm);
+          alpha_s[b * NPMAX + tid] = (mn == -INFINITY) ? 1.0f : exp2f(mo - mn);
+          m_run[tid] = mn;
+        }
+        named_sync_128();
+#pragma unroll
+        for (int n = 0; n < NPMAX; ++n) mr[n] = m_run[n];
+      }
+      // ---- P = exp2(x - m_run) as bf16, K-major with 128-byte swizzle (row n, column = token)
+      {
+        unsigned char *pd = Ps + b * 2 * L::KATOM;
+        const int katom = tid >> 6, c = (tid & 63) >> 3, e = tid & 7;
+#pragma unroll
+        for (int n = 0; n < NPMAX; ++n) {
+          const float pv = (x[n] == -INFINITY) ? 0.0f : fast_exp2(x[n] - mr[n]);
+          lt[n] = rescale ? fmaf(lt[n], alpha_s[b * NPMAX + n], pv) : lt[n] + pv;
+          *reinterpret_cast<__nv_bfloat16 *>(pd + katom * L::KATOM + (n >> 3) * 1024 + (n & 7) * 128 +
+                                            ((c ^ (n & 7)) << 4) + e * 2) = __float2bfloat16_rn(pv);
         }
       }
-      if (tid < nreal) {
-        const int i = tid / G, g = tid - (tid / G) * G;
-        const float l = lsum[tid];
-        p.lse[static_cast<size_t>(qoff + i) * p.hq + h * G + g] = l > 0.0f ? (m_run[tid] + log2f(l)) * kLn2 : -INFINITY;
-      }
-    } else {
-      const int slot = static_cast<int>(blockIdx.x) + m.row;
-      float *pp = p.part + static_cast<size_t>(slot) * p.npad_ws * 128;
+      // tokens past the last query position carry no weight; their V rows may hold anything (even NaN) and must
+      // not reach the tensor core: zero them
+      if (pos > qpos0 + nq - 1) {
+        if (!mbar_wait(&vfull[st], (t / kStages) & 1, p.err)) okrun = false;
+        unsigned char *vrow0 = Vs + st * kStageBytes + (tid >> 4) * 2048 + (tid & 15) * 128;
 #pragma unroll
-      for (int n = 0; n < NPMAX; ++n)
-        if (n < npad) __stcg(pp + n * 128 + tid, oreg[n]);
-      if (tid < npad) {
-        __stcg(p.ml + (static_cast<size_t>(slot) * p.npad_ws + tid) * 2, m_run[tid]);
-        __stcg(p.ml + (static_cast<size_t>(slot) * p.npad_ws + tid) * 2 + 1, lsum[tid]);
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4 *>(vrow0 + hh * kHalfBytes + c * 16) = make_uint4(0, 0, 0, 0);
       }
-      __threadfence();
-      __syncthreads();
-      if (tid == 0) {
-        const int old = atomicAdd(&p.counters[m.row], 1);
-        s_flag = (old == ncontrib - 1) ? 1 : 0;
-        if (s_flag) p.counters[m.row] = 0;
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pfull[b]);
+      // ---- merge the previous tile's O (its MMA2 overlapped this softmax)
+      if (pending >= 0) {
+        if (!merge(pending, pending_npad, pending_resc)) {
+          okrun = false;
+          break;
+        }
+        pending = -1;
       }
-      __syncthreads();
-      if (s_flag) {
+      pending = t;
+      pending_npad = npad;
+      pending_resc = rescale;
+      if (!m.last) continue;
+
+      // ---- end of this row segment: drain, column sums, then finish or hand over a partial record
+      if (!merge(pending, pending_npad, pending_resc)) {
+        okrun = false;
+        break;
+      }
+      pending = -1;
+#pragma unroll
+      for (int n = 0; n < NPMAX; ++n) {
+        if (n < npad) {
+          const float v = warp_sum(lt[n]);
+          if (lane == 0) atomicAdd(&lsum[n], v);
+        }
+      }
+      named_sync_128();
+      const int b_first = owner_cta(m.rb, E, nb), b_last = owner_cta(m.re - 1, E, nb);
+      const int ncontrib = b_last - b_first + 1;
+      __nv_bfloat16 *outp = static_cast<__nv_bfloat16 *>(p.out);
+      if (ncontrib == 1) {
+#pragma unroll
+        for (int n = 0; n < NPMAX; ++n) {
+          if (n < nreal) {
+            const int i = n / G, g = n - (n / G) * G;
+            const float l = lsum[n];
+            outp[(static_cast<size_t>(qoff + i) * p.hq + h * G + g) * 128 + tid] =
+                __float2bfloat16_rn(l > 0.0f ? oreg[n] / l : 0.0f);
+          }
+        }
+        if (tid < nreal) {
+          const int i = tid / G, g = tid - (tid / G) * G;
+          const float l = lsum[tid];
+          p.lse[static_cast<size_t>(qoff + i) * p.hq + h * G + g] =
+              l > 0.0f ? (m_run[tid] + log2f(l)) * kLn2 : -INFINITY;
+        }
+      } else {
+        const int slot = static_cast<int>(blockIdx.x) + m.row;
+        float *pp = p.part + static_cast<size_t>(slot) * p.npad_ws * 128;
+#pragma unroll
+        for (int n = 0; n < NPMAX; ++n)
+          if (n < npad) __stcg(pp + n * 128 + tid, oreg[n]);
+        if (tid < npad) {
+          __stcg(p.ml + (static_cast<size_t>(slot) * p.npad_ws + tid) * 2, m_run[tid]);
+          __stcg(p.ml + (static_cast<size_t>(slot) * p.npad_ws + tid) * 2 + 1, lsum[tid]);
+        }
         __threadfence();
-        for (int n = 0; n < nreal; ++n) {
-          float M = -INFINITY;
-          for (int b = b_first; b <= b_last; ++b)
-            M = fmaxf(M, __ldcg(p.ml + (static_cast<size_t>(b + m.row) * p.npad_ws + n) * 2));
-          float Ls = 0.0f, acc = 0.0f;
-          if (M != -INFINITY) {
-            for (int b = b_first; b <= b_last; ++b) {
-              const size_t s2 = static_cast<size_t>(b + m.row);
-              const float mb = __ldcg(p.ml + (s2 * p.npad_ws + n) * 2);
-              const float lb = __ldcg(p.ml + (s2 * p.npad_ws + n) * 2 + 1);
-              const float w = (mb == -INFINITY) ? 0.0f : exp2f(mb - M);
-              Ls += lb * w;
-              acc += __ldcg(p.part + (s2 * p.npad_ws + n) * 128 + tid) * w;
+        named_sync_128();
+        if (tid == 0) {
+          const int old = atomicAdd(&p.counters[m.row], 1);
+          s_flag = (old == ncontrib - 1) ? 1 : 0;
+          if (s_flag) p.counters[m.row] = 0;  // every contributor has arrived: leave the counter at zero
+        }
+        named_sync_128();
+        if (s_flag) {
+          // Merge of the row's partial records from CTAs b_first..b_last with independent loads in flight: the
+          // per-column max first, then weights per group of 8 contributors staged in shared memory.
+          __threadfence();
+          float *Ms = colmax;          // [NPMAX]
+          float *Ls = colmax + NPMAX;  // [NPMAX]
+          if (tid < nreal) {
+            float M = -INFINITY;
+#pragma unroll 8
+            for (int bb = b_first; bb <= b_last; ++bb)
+              M = fmaxf(M, __ldcg(p.ml + (static_cast<size_t>(bb + m.row) * p.npad_ws + tid) * 2));
+            Ms[tid] = M;
+            Ls[tid] = 0.0f;
+          }
+#pragma unroll
+          for (int n = 0; n < NPMAX; ++n) oreg[n] = 0.0f;
+          float *wsm = reinterpret_cast<float *>(Ps);  // [8][NPMAX]: both P buffers are idle at a segment end
+          float wl[8];
+          for (int b0 = b_first; b0 <= b_last; b0 += 8) {
+            const int nbb = min(8, b_last - b0 + 1);
+            named_sync_128();
+            for (int q = tid; q < nbb * nreal; q += 128) {
+              const int bb = q / nreal, n = q - (q / nreal) * nreal;
+              const size_t slot2 = static_cast<size_t>(b0 + bb + m.row);
+              const float mb = __ldcg(p.ml + (slot2 * p.npad_ws + n) * 2);
+              const float w = (mb == -INFINITY || Ms[n] == -INFINITY) ? 0.0f : exp2f(mb - Ms[n]);
+              wsm[bb * NPMAX + n] = w;
+            }
+            named_sync_128();
+            for (int bb = 0; bb < nbb; ++bb) {
+              const float *src = p.part + static_cast<size_t>(b0 + bb + m.row) * p.npad_ws * 128 + tid;
+#pragma unroll
+              for (int n = 0; n < NPMAX; ++n)
+                if (n < nreal) oreg[n] = fmaf(__ldcg(src + n * 128), wsm[bb * NPMAX + n], oreg[n]);
+            }
+            if (tid < nreal) {
+#pragma unroll
+              for (int bb = 0; bb < 8; ++bb)
+                wl[bb] = bb < nbb ? __ldcg(p.ml + (static_cast<size_t>(b0 + bb + m.row) * p.npad_ws + tid) * 2 + 1)
+                                  : 0.0f;
+#pragma unroll
+              for (int bb = 0; bb < 8; ++bb) Ls[tid] += wl[bb] * (bb < nbb ? wsm[bb * NPMAX + tid] : 0.0f);
             }
           }
-          const int i = n / G, g = n - (n / G) * G;
-          outp[(static_cast<size_t>(qoff + i) * p.hq + h * G + g) * 128 + tid] =
-              __float2bfloat16_rn(Ls > 0.0f ? acc / Ls : 0.0f);
-          if (tid == 0)
-            p.lse[static_cast<size_t>(qoff + i) * p.hq + h * G + g] = Ls > 0.0f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+          named_sync_128();
+#pragma unroll
+          for (int n = 0; n < NPMAX; ++n) {
+            if (n < nreal) {
+              const int i = n / G, g = n - (n / G) * G;
+              const float l = Ls[n];
+              outp[(static_cast<size_t>(qoff + i) * p.hq + h * G + g) * 128 + tid] =
+                  __float2bfloat16_rn(l > 0.0f ? oreg[n] / l : 0.0f);
+            }
+          }
+          if (tid < nreal) {
+            const int i = tid / G, g = tid - (tid / G) * G;
+            const float l = Ls[tid];
+            p.lse[static_cast<size_t>(qoff + i) * p.hq + h * G + g] = l > 0.0f ? (Ms[tid] + log2f(l)) * kLn2 : -INFINITY;
+          }
         }
       }
+      named_sync_128();
     }
-    __syncthreads();
+    if (!okrun) *abort_flag = 1;
   }
 
-  // After a bounded wait ran out, the copies still in flight (tiles issued but not consumed) are waited for,
-  // again with a bound, before the CTA leaves.
-  if (tid == 0 && s_abort) {
-    for (int st = 0; st < kStages; ++st) {
-      const TileMeta &mm = meta[st];
-      if (!mm.valid || mm.seq < t_end) continue;
-      const uint32_t ph = (mm.seq / kStages) & 1;
-      mbar_wait(&barK[st], ph, nullptr);
-      mbar_wait(&barV[st], ph, nullptr);
-    }
-  }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, L::TMEM_COLS);
@@ -571,7 +806,7 @@ cudaError_t launch_tc(const PoolArgs &pa, const VParams &prm, cudaStream_t s) {
     attr_set[dev & 63] = true;
   }
   const int nb = device_sm_count();
-  verify_tc_kernel<NPMAX><<<nb, 128, L::ALLOC, s>>>(tmK, tmV, prm);
+  verify_tc_kernel<NPMAX><<<nb, kTcThreads, L::ALLOC, s>>>(tmK, tmV, prm);
   return cudaGetLastError();
 }
 
