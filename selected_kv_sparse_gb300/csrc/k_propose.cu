@@ -452,45 +452,47 @@ __global__ void __launch_bounds__(kThreads, 3) propose_kernel(const Params p) {
       }
       __syncthreads();
       if (s_flag) {
-        // Merge of the row's partial records (m, l, o) from CTAs b_first..b_last, with independent loads in
-        // flight: a block-wide max per head, then weights per group of 32 contributors staged in shared memory.
+        // Last arriver: merge the row's partial records from CTAs b_first..b_last. The (m, l) pairs of up to 32
+        // contributors are staged in shared memory by one parallel load pass; the partial outputs are loaded with
+        // up to 16 loads in flight per element before any is used.
         __threadfence();
         constexpr int kElems = (G * D + kThreads - 1) / kThreads;
-        float mloc[G];
-#pragma unroll
-        for (int g = 0; g < G; ++g) mloc[g] = -INFINITY;
-        for (int b = b_first + tid; b <= b_last; b += kThreads)
-#pragma unroll
-          for (int g = 0; g < G; ++g)
-            mloc[g] = fmaxf(mloc[g], __ldcg(p.ml + (static_cast<size_t>(b + m.row) * G + g) * 2));
-        __syncthreads();  // red is free: its content is already in this CTA's partial record
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float v = warp_max(mloc[g]);
-          if (lane == 0) red[warp * G + g] = v;
+        float *sm_m = sl;           // [32][G]
+        float *sm_w = sl + 32 * G;  // [32][G]
+        float *Mg = red, *Lg = red + G, *Rg = red + 2 * G;  // red is free: its content is in the partial record
+        if (tid < G) {
+          Mg[tid] = -INFINITY;
+          Lg[tid] = 0.0f;
         }
-        __syncthreads();
-        float Mg[G], Lg[G], acc[kElems];
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          Mg[g] = fmaxf(fmaxf(red[g], red[G + g]), fmaxf(red[2 * G + g], red[3 * G + g]));
-          Lg[g] = 0.0f;
-        }
+        float acc[kElems];
 #pragma unroll
         for (int k = 0; k < kElems; ++k) acc[k] = 0.0f;
-        float *wsm = sl;           // [32][G] weights exp2(m_b - M)
-        float *lsm = sl + 32 * G;  // [32][G] l_b * weight
-        for (int b0 = b_first; b0 <= b_last; b0 += 32) {
-          const int nbb = min(32, b_last - b0 + 1);
+        const int nc = b_last - b_first + 1;
+        for (int g0 = 0; g0 < nc; g0 += 32) {
+          const int ng = min(32, nc - g0);
           __syncthreads();
-          for (int t = tid; t < nbb * G; t += kThreads) {
-            const int bb = t / G, g = t - (t / G) * G;
-            const size_t slot = static_cast<size_t>(b0 + bb + m.row);
-            const float mb = __ldcg(p.ml + (slot * G + g) * 2);
-            const float lb = __ldcg(p.ml + (slot * G + g) * 2 + 1);
-            const float w = (mb == -INFINITY || Mg[g] == -INFINITY) ? 0.0f : exp2f(mb - Mg[g]);
-            wsm[bb * G + g] = w;
-            lsm[bb * G + g] = lb * w;
+          for (int q = tid; q < ng * G; q += kThreads) {
+            const int bb = q / G, g = q - (q / G) * G;
+            const size_t o = (static_cast<size_t>(b_first + g0 + bb + m.row) * G + g) * 2;
+            sm_m[bb * G + g] = __ldcg(p.ml + o);
+            sm_w[bb * G + g] = __ldcg(p.ml + o + 1);
+          }
+          __syncthreads();
+          if (tid < G) {
+            const float Mo = Mg[tid];
+            float M = Mo;
+            for (int bb = 0; bb < ng; ++bb) M = fmaxf(M, sm_m[bb * G + tid]);
+            const float resc = (Mo == -INFINITY || M == -INFINITY) ? 0.0f : exp2f(Mo - M);
+            float Ls = Lg[tid] * resc;
+            for (int bb = 0; bb < ng; ++bb) {
+              const float mb = sm_m[bb * G + tid];
+              const float w = (mb == -INFINITY || M == -INFINITY) ? 0.0f : exp2f(mb - M);
+              Ls += sm_w[bb * G + tid] * w;
+              sm_w[bb * G + tid] = w;
+            }
+            Mg[tid] = M;
+            Lg[tid] = Ls;
+            Rg[tid] = resc;
           }
           __syncthreads();
 #pragma unroll
@@ -498,16 +500,21 @@ __global__ void __launch_bounds__(kThreads, 3) propose_kernel(const Params p) {
             const int i = tid + k * kThreads;
             if (i < G * D) {
               const int g = i / D;
-              float a = 0.0f;
-#pragma unroll 8
-              for (int bb = 0; bb < nbb; ++bb)
-                a = fmaf(__ldcg(p.part + static_cast<size_t>(b0 + bb + m.row) * G * D + i), wsm[bb * G + g], a);
-              acc[k] += a;
+              float a = (g0 > 0) ? acc[k] * Rg[g] : 0.0f;
+              for (int b0 = 0; b0 < ng; b0 += 16) {
+                float v[16];
+#pragma unroll
+                for (int bb = 0; bb < 16; ++bb)
+                  v[bb] = (b0 + bb < ng)
+                              ? __ldcg(p.part + static_cast<size_t>(b_first + g0 + b0 + bb + m.row) * G * D + i)
+                              : 0.0f;
+#pragma unroll
+                for (int bb = 0; bb < 16; ++bb)
+                  if (b0 + bb < ng) a = fmaf(v[bb], sm_w[(b0 + bb) * G + g], a);
+              }
+              acc[k] = a;
             }
           }
-#pragma unroll
-          for (int g = 0; g < G; ++g)
-            for (int bb = 0; bb < nbb; ++bb) Lg[g] += lsm[bb * G + g];
         }
 #pragma unroll
         for (int k = 0; k < kElems; ++k) {

@@ -634,48 +634,73 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         named_sync_128();
         if (s_flag) {
-          // Merge of the row's partial records from CTAs b_first..b_last with independent loads in flight: the
-          // per-column max first, then weights per group of 8 contributors staged in shared memory.
+          // Last arriver: merge the row's partial records from CTAs b_first..b_last. The (m, l) pairs of up to 8
+          // contributors are staged in the idle P buffers by one parallel load pass; the partial outputs of the
+          // group are then loaded with every load in flight before any is used.
           __threadfence();
+          float *sm_m = reinterpret_cast<float *>(Ps);  // [8][NPMAX]: both P buffers are idle at a segment end
+          float *sm_w = sm_m + 8 * NPMAX;               // [8][NPMAX]
+          float Mrun = -INFINITY, Lrun = 0.0f;          // column tid (tid < nreal)
+#pragma unroll
+          for (int n = 0; n < NPMAX; ++n) oreg[n] = 0.0f;
+          const int nc = b_last - b_first + 1;
+          for (int g0 = 0; g0 < nc; g0 += 8) {
+            const int ng = min(8, nc - g0);
+            named_sync_128();
+            for (int q = tid; q < ng * nreal; q += 128) {
+              const int bb = q / nreal, n = q - (q / nreal) * nreal;
+              const size_t o = (static_cast<size_t>(b_first + g0 + bb + m.row) * p.npad_ws + n) * 2;
+              sm_m[bb * NPMAX + n] = __ldcg(p.ml + o);
+              sm_w[bb * NPMAX + n] = __ldcg(p.ml + o + 1);
+            }
+            named_sync_128();
+            if (tid < nreal) {
+              float M = Mrun;
+              for (int bb = 0; bb < ng; ++bb) M = fmaxf(M, sm_m[bb * NPMAX + tid]);
+              const float resc = (Mrun == -INFINITY || M == -INFINITY) ? 0.0f : exp2f(Mrun - M);
+              float Lsum = Lrun * resc;
+              for (int bb = 0; bb < ng; ++bb) {
+                const float mb = sm_m[bb * NPMAX + tid];
+                const float w = (mb == -INFINITY || M == -INFINITY) ? 0.0f : exp2f(mb - M);
+                Lsum += sm_w[bb * NPMAX + tid] * w;
+                sm_w[bb * NPMAX + tid] = w;
+              }
+              colmax[tid] = resc;
+              Mrun = M;
+              Lrun = Lsum;
+            }
+            named_sync_128();
+            if (g0 > 0) {
+#pragma unroll
+              for (int n = 0; n < NPMAX; ++n) oreg[n] *= colmax[n];
+            }
+#pragma unroll
+            for (int n0 = 0; n0 < NPMAX; n0 += 16) {
+              if (n0 < nreal) {
+                float v[8][16];
+#pragma unroll
+                for (int bb = 0; bb < 8; ++bb)
+#pragma unroll
+                  for (int n = 0; n < 16; ++n)
+                    v[bb][n] = (bb < ng && n0 + n < nreal)
+                                   ? __ldcg(p.part +
+                                            (static_cast<size_t>(b_first + g0 + bb + m.row) * p.npad_ws + n0 + n) * 128 +
+                                            tid)
+                                   : 0.0f;
+#pragma unroll
+                for (int bb = 0; bb < 8; ++bb)
+#pragma unroll
+                  for (int n = 0; n < 16; ++n)
+                    if (bb < ng) oreg[n0 + n] = fmaf(v[bb][n], sm_w[bb * NPMAX + n0 + n], oreg[n0 + n]);
+              }
+            }
+          }
+          named_sync_128();
           float *Ms = colmax;          // [NPMAX]
           float *Ls = colmax + NPMAX;  // [NPMAX]
           if (tid < nreal) {
-            float M = -INFINITY;
-#pragma unroll 8
-            for (int bb = b_first; bb <= b_last; ++bb)
-              M = fmaxf(M, __ldcg(p.ml + (static_cast<size_t>(bb + m.row) * p.npad_ws + tid) * 2));
-            Ms[tid] = M;
-            Ls[tid] = 0.0f;
-          }
-#pragma unroll
-          for (int n = 0; n < NPMAX; ++n) oreg[n] = 0.0f;
-          float *wsm = reinterpret_cast<float *>(Ps);  // [8][NPMAX]: both P buffers are idle at a segment end
-          float wl[8];
-          for (int b0 = b_first; b0 <= b_last; b0 += 8) {
-            const int nbb = min(8, b_last - b0 + 1);
-            named_sync_128();
-            for (int q = tid; q < nbb * nreal; q += 128) {
-              const int bb = q / nreal, n = q - (q / nreal) * nreal;
-              const size_t slot2 = static_cast<size_t>(b0 + bb + m.row);
-              const float mb = __ldcg(p.ml + (slot2 * p.npad_ws + n) * 2);
-              const float w = (mb == -INFINITY || Ms[n] == -INFINITY) ? 0.0f : exp2f(mb - Ms[n]);
-              wsm[bb * NPMAX + n] = w;
-            }
-            named_sync_128();
-            for (int bb = 0; bb < nbb; ++bb) {
-              const float *src = p.part + static_cast<size_t>(b0 + bb + m.row) * p.npad_ws * 128 + tid;
-#pragma unroll
-              for (int n = 0; n < NPMAX; ++n)
-                if (n < nreal) oreg[n] = fmaf(__ldcg(src + n * 128), wsm[bb * NPMAX + n], oreg[n]);
-            }
-            if (tid < nreal) {
-#pragma unroll
-              for (int bb = 0; bb < 8; ++bb)
-                wl[bb] = bb < nbb ? __ldcg(p.ml + (static_cast<size_t>(b0 + bb + m.row) * p.npad_ws + tid) * 2 + 1)
-                                  : 0.0f;
-#pragma unroll
-              for (int bb = 0; bb < 8; ++bb) Ls[tid] += wl[bb] * (bb < nbb ? wsm[bb * NPMAX + tid] : 0.0f);
-            }
+            Ms[tid] = Mrun;
+            Ls[tid] = Lrun;
           }
           named_sync_128();
 #pragma unroll
