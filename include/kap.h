@@ -139,10 +139,13 @@ kap_status kap_select_spans(const kap_page_map *map, const int32_t *spans_dev, c
  *   sel_rows_per_seq/sel_cap give the layout of sel_ids; view->rows_per_seq must equal sel_rows_per_seq.
  *   fallback_dev     optional [R] out: 1 when request r's retained prompt fraction n_sel/N exceeds s_max,
  *                    else 0 (KAP paper, fallback: "retains too much KV").
+ *   slot_out/pos_out optional [R][horizon_tokens] out: the slot mapping of the tokens the cycle will append,
+ *                    at positions seq_len[r] + i (same rule as kap_slot_mapping); NULL to skip.
  * Returns KAP_ECAPACITY when view->cap < sel_cap + ceil(horizon/16) + 1. */
 kap_status kap_compile_view(const kap_page_map *map, const int32_t *sel_ids, const int32_t *n_sel,
                             int32_t sel_rows_per_seq, int32_t sel_cap, int32_t horizon_tokens,
-                            const kap_view *view, int32_t *fallback_dev, float s_max, kap_stream stream);
+                            const kap_view *view, int32_t *fallback_dev, float s_max, int64_t *slot_out,
+                            int32_t *pos_out, kap_stream stream);
 
 /* Slot mapping. KAP paper, selected-KV view ("slot mappings place newly scheduled tokens into their
  * physical KV slots"). Request r owns tokens tok_offsets[r] .. tok_offsets[r+1]-1; token j sits at

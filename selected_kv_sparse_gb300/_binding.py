@@ -68,7 +68,7 @@ def _declare(lib):
         "kap_score_topk": ([P, P, P, P, P, P, P, Z, P], I),
         "kap_score_workspace_size": ([I, I, I], Z),
         "kap_select_spans": ([P, P, P, P, P, P, P], I),
-        "kap_compile_view": ([P, P, P, I, I, I, P, P, F, P], I),
+        "kap_compile_view": ([P, P, P, I, I, I, P, P, F, P, P, P], I),
         "kap_slot_mapping": ([P, P, P, I, P, P, P], I),
         "kap_append_kv": ([P, P, P, P, P, P, I, I, P, P], I),
         "kap_attn_propose": ([P, P, P, P, P, P, P, Z, P], I),
@@ -265,16 +265,23 @@ def kap_select_spans(pmap: PageMap, spans: torch.Tensor, span_offsets: torch.Ten
 
 
 def kap_compile_view(pmap: PageMap, sel_ids: torch.Tensor, n_sel: torch.Tensor, horizon_tokens: int, view: View,
-                     fallback: Optional[torch.Tensor] = None, s_max: float = 1.0, stream=None):
+                     fallback: Optional[torch.Tensor] = None, s_max: float = 1.0,
+                     slot_out: Optional[torch.Tensor] = None, pos_out: Optional[torch.Tensor] = None, stream=None):
+    """Compact view; optionally also the slot mapping [R][horizon_tokens] of the tokens the cycle appends."""
     lib = load()
     if sel_ids.dim() != 3:
         raise ValueError("sel_ids must be [R][rows][cap]")
+    if slot_out is not None and (slot_out.dtype != torch.int64 or slot_out.numel() < pmap.block_table.shape[0] *
+                                 horizon_tokens):
+        raise ValueError("slot_out must be int64 with R * horizon_tokens elements")
     m, v = pmap._c(), view._c()
     _check("kap_compile_view", lib.kap_compile_view(ctypes.byref(m), _i32(sel_ids, "sel_ids"), _i32(n_sel, "n_sel"),
                                                     sel_ids.shape[1], sel_ids.shape[2], horizon_tokens,
                                                     ctypes.byref(v),
                                                     _i32(fallback, "fallback") if fallback is not None else None,
-                                                    float(s_max), _stream(stream)))
+                                                    float(s_max), _ptr(slot_out),
+                                                    _i32(pos_out, "pos_out") if pos_out is not None else None,
+                                                    _stream(stream)))
 
 
 def kap_slot_mapping(pmap: PageMap, tok_offsets: torch.Tensor, start_pos: torch.Tensor, slot_out: torch.Tensor,

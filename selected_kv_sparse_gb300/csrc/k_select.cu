@@ -37,9 +37,11 @@ __global__ void __launch_bounds__(128) summaries_kernel(const T *__restrict__ K,
 }
 
 // ---------------------------------------------------------------------------------------------- scores
-// grid.x: chunks of 256 logical pages; grid.y: (request, selection row). 8 warps; each warp scores 4 pages at a
-// time. Dot products follow the fixed order: lane l accumulates fmaf over i = l, l+32, ...; xor-butterfly 16..1.
-constexpr int kScorePagesPerCta = 256;
+// grid.x: chunks of 64 logical pages; grid.y: (request, selection row). 8 warps; each warp scores 8 pages with all
+// of their summary loads in flight at once. Dot products follow the fixed order: lane l accumulates fmaf over
+// i = l, l+32, ...; then an xor-butterfly 16, 8, 4, 2, 1.
+constexpr int kScorePagesPerWarp = 8;
+constexpr int kScorePagesPerCta = 8 * kScorePagesPerWarp;
 constexpr int kMaxPooledHeads = 16;
 
 template <class T, int D>
@@ -64,44 +66,45 @@ __global__ void __launch_bounds__(256) score_kernel(const T *__restrict__ q, con
   }
   __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int j_end = min(N, j0 + kScorePagesPerCta);
+  const int jb = j0 + warp * kScorePagesPerWarp;
+  if (jb >= N) return;
   const int32_t *btr = bt + static_cast<size_t>(r) * max_pages;
-  for (int jb = j0 + warp * 4; jb < j_end; jb += 32) {
-    int pg[4];
-    bool ok[4];
+  int pg[kScorePagesPerWarp];
+  bool ok[kScorePagesPerWarp];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int j = jb + u;
-      ok[u] = j < j_end;
-      pg[u] = ok[u] ? btr[j] : 0;
-      if (ok[u] && (pg[u] < 0 || pg[u] >= num_pages)) {
-        ok[u] = false;
-        if (lane == 0) set_error(err, kErrPage);
-      }
+  for (int u = 0; u < kScorePagesPerWarp; ++u) {
+    const int j = jb + u;
+    ok[u] = j < N;
+    pg[u] = ok[u] ? btr[j] : 0;
+    if (ok[u] && (pg[u] < 0 || pg[u] >= num_pages)) {
+      ok[u] = false;
+      if (lane == 0) set_error(err, kErrPage);
     }
-    float tot[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int hh = h_lo; hh < h_hi; ++hh) {
-      float a[4] = {0.f, 0.f, 0.f, 0.f};
+  }
+  float tot[kScorePagesPerWarp];
+  for (int hh = h_lo; hh < h_hi; ++hh) {
+    float sv[kScorePagesPerWarp][D / 32];
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        const int i = lane + 32 * c;
-        const float qb = qbar[hh - h_lo][i];
+    for (int u = 0; u < kScorePagesPerWarp; ++u)
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          if (ok[u]) a[u] = __fmaf_rn(qb, __ldg(S + (static_cast<size_t>(pg[u]) * hkv + hh) * D + i), a[u]);
-      }
+      for (int c = 0; c < D / 32; ++c)
+        sv[u][c] = ok[u] ? __ldg(S + (static_cast<size_t>(pg[u]) * hkv + hh) * D + lane + 32 * c) : 0.0f;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < kScorePagesPerWarp; ++u) {
+      float a = 0.0f;
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) a[u] = __fadd_rn(a[u], __shfl_xor_sync(0xffffffffu, a[u], o));
-        tot[u] = (hh == h_lo) ? a[u] : __fadd_rn(tot[u], a[u]);
-      }
+      for (int c = 0; c < D / 32; ++c) a = __fmaf_rn(qbar[hh - h_lo][lane + 32 * c], sv[u][c], a);
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, o));
+      tot[u] = (hh == h_lo) ? a : __fadd_rn(tot[u], a);
     }
-    if (lane == 0) {
+  }
+  if (lane < kScorePagesPerWarp && ok[lane]) {
+    float val = tot[0];
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (ok[u]) scores[static_cast<size_t>(row) * max_pages + jb + u] = tot[u];
-    }
+    for (int u = 1; u < kScorePagesPerWarp; ++u)
+      if (lane == u) val = tot[u];
+    scores[static_cast<size_t>(row) * max_pages + jb + lane] = val;
   }
 }
 
@@ -306,7 +309,9 @@ __global__ void __launch_bounds__(128) view_kernel(const int32_t *__restrict__ b
                                                    int rows, int sel_cap, int horizon, int32_t *__restrict__ vbt,
                                                    int32_t *__restrict__ vlp, int32_t *__restrict__ vn,
                                                    int32_t *__restrict__ vnsel, int vcap,
-                                                   int32_t *__restrict__ fallback, float s_max, int *err) {
+                                                   int32_t *__restrict__ fallback, float s_max,
+                                                   int64_t *__restrict__ slot_out, int32_t *__restrict__ pos_out,
+                                                   int *err) {
   const int row = blockIdx.x;
   const int r = row / rows;
   const int L = ctx_len[r];
@@ -346,6 +351,18 @@ __global__ void __launch_bounds__(128) view_kernel(const int32_t *__restrict__ b
     const int j = first_tail + skip + t;
     olp[n_keep + t] = j;
     obt[n_keep + t] = btr[j];
+  }
+  if (slot_out && row % rows == 0) {  // slot mapping of the horizon tokens, once per request
+    for (int t = threadIdx.x; t < horizon; t += blockDim.x) {
+      const int pos = seq_len[r] + t;
+      int64_t slot = -1;
+      if (pos >= 0 && pos / kPage < max_pages) {
+        const int page = btr[pos / kPage];
+        if (page >= 0) slot = static_cast<int64_t>(page) * kPage + pos % kPage;
+      }
+      slot_out[static_cast<size_t>(r) * horizon + t] = slot;
+      if (pos_out) pos_out[static_cast<size_t>(r) * horizon + t] = pos;
+    }
   }
   if (threadIdx.x == 0) {
     vn[row] = n_keep + n_tail;
@@ -440,9 +457,10 @@ cudaError_t launch_select_spans(const MapArgs &m, const int32_t *spans, const in
 
 cudaError_t launch_compile_view(const MapArgs &m, const int32_t *sel, const int32_t *n_sel, int rows, int sel_cap,
                                 int horizon, int32_t *vbt, int32_t *vlp, int32_t *vn, int32_t *vnsel, int vcap,
-                                int32_t *fallback, float s_max, int *err, cudaStream_t s) {
+                                int32_t *fallback, float s_max, int64_t *slot_out, int32_t *pos_out, int *err,
+                                cudaStream_t s) {
   view_kernel<<<m.R * rows, 128, 0, s>>>(m.bt, m.max_pages, m.ctx_len, m.seq_len, sel, n_sel, rows, sel_cap,
-                                         horizon, vbt, vlp, vn, vnsel, vcap, fallback, s_max, err);
+                                         horizon, vbt, vlp, vn, vnsel, vcap, fallback, s_max, slot_out, pos_out, err);
   return cudaGetLastError();
 }
 

@@ -164,7 +164,8 @@ kap_status kap_select_spans(const kap_page_map *map, const int32_t *spans_dev, c
 
 kap_status kap_compile_view(const kap_page_map *map, const int32_t *sel_ids, const int32_t *n_sel,
                             int32_t sel_rows_per_seq, int32_t sel_cap, int32_t horizon_tokens, const kap_view *view,
-                            int32_t *fallback_dev, float s_max, kap_stream stream) {
+                            int32_t *fallback_dev, float s_max, int64_t *slot_out, int32_t *pos_out,
+                            kap_stream stream) {
   kap_status st = check_map(map, true);
   if (st != KAP_OK) return st;
   if (!sel_ids || !n_sel || !view) return KAP_EINVAL;
@@ -175,7 +176,8 @@ kap_status kap_compile_view(const kap_page_map *map, const int32_t *sel_ids, con
     return KAP_ECAPACITY;
   return cuda_status(launch_compile_view(map_args(map), sel_ids, n_sel, sel_rows_per_seq, sel_cap, horizon_tokens,
                                          view->block_table, view->logical_page, view->n_entries, view->n_selected,
-                                         view->cap, fallback_dev, s_max, error_word(), cs(stream)));
+                                         view->cap, fallback_dev, s_max, slot_out, pos_out, error_word(),
+                                         cs(stream)));
 }
 
 kap_status kap_slot_mapping(const kap_page_map *map, const int32_t *tok_offsets_dev, const int32_t *start_pos_dev,

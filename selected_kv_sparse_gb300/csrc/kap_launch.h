@@ -34,7 +34,8 @@ cudaError_t launch_select_spans(const MapArgs &m, const int32_t *spans, const in
                                 cudaStream_t s);
 cudaError_t launch_compile_view(const MapArgs &m, const int32_t *sel, const int32_t *n_sel, int rows, int sel_cap,
                                 int horizon, int32_t *vbt, int32_t *vlp, int32_t *vn, int32_t *vnsel, int vcap,
-                                int32_t *fallback, float s_max, int *err, cudaStream_t s);
+                                int32_t *fallback, float s_max, int64_t *slot_out, int32_t *pos_out, int *err,
+                                cudaStream_t s);
 cudaError_t launch_slot_mapping(const MapArgs &m, const int32_t *tok_offsets, const int32_t *start_pos, int T,
                                 int64_t *slot_out, int32_t *pos_out, cudaStream_t s);
 

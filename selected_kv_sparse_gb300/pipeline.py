@@ -53,16 +53,20 @@ class DecodeCycle:
         self.n_sel = torch.zeros(self.R, self.rows, **i32)
         self.view = kb.View.empty(self.R, self.rows, self.view_cap, dev)
         self.fallback = torch.zeros(self.R, **i32)
-        # slot mappings: proposals [R][k_prop], verify window [total_q]
-        self.tok_off_prop = (torch.arange(self.R + 1, **i32) * self.k_prop).contiguous()
-        self.slots_prop = torch.zeros(self.R * self.k_prop, dtype=torch.int64, device=dev)
-        self.pos_prop = torch.zeros(self.R * self.k_prop, **i32)
+        # slot mappings: the horizon tokens [R][horizon] come with the view; the verify window [total_q] reuses
+        # them when every window spans exactly the horizon, else gets its own mapping
+        self.slots_prop = torch.zeros(self.R * self.horizon, dtype=torch.int64, device=dev)
+        self.pos_prop = torch.zeros(self.R * self.horizon, **i32)
+        self.window_is_horizon = all(n == self.horizon for n in n_q_host)
         q_off = torch.zeros(self.R + 1, dtype=torch.int32)
         q_off[1:] = torch.cumsum(torch.tensor(n_q_host, dtype=torch.int32), 0)
         self.q_offsets = q_off.to(dev)
         self.q_start = seq_len0.to(torch.int32).contiguous()
-        self.slots_ver = torch.zeros(self.total_q, dtype=torch.int64, device=dev)
-        self.pos_ver = torch.zeros(self.total_q, **i32)
+        if self.window_is_horizon:
+            self.slots_ver, self.pos_ver = self.slots_prop, self.pos_prop
+        else:
+            self.slots_ver = torch.zeros(self.total_q, dtype=torch.int64, device=dev)
+            self.pos_ver = torch.zeros(self.total_q, **i32)
         self.vpol = kb.VerifyPolicy(self.q_offsets, self.q_start, self.max_q, self.total_q)
         # workspaces (zero-filled once)
         mp = int(block_table.shape[1])
@@ -86,15 +90,14 @@ class DecodeCycle:
             kb.kap_score_topk(self.pool, self.map_plan, q_route, self.policy, self.sel_ids, self.n_sel, self.ws_score,
                               stream)
         kb.kap_compile_view(self.map_plan, self.sel_ids, self.n_sel, self.horizon, self.view, self.fallback,
-                            self.s_max, stream)
-        kb.kap_slot_mapping(self.map_plan, self.tok_off_prop, self.map_plan.seq_len, self.slots_prop, self.pos_prop,
-                            stream)
-        kb.kap_slot_mapping(self.map_plan, self.q_offsets, self.q_start, self.slots_ver, self.pos_ver, stream)
+                            self.s_max, self.slots_prop, self.pos_prop, stream)
+        if not self.window_is_horizon:
+            kb.kap_slot_mapping(self.map_plan, self.q_offsets, self.q_start, self.slots_ver, self.pos_ver, stream)
 
     def append_step(self, i: int, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
         """Proposal step i, first half: the step token's KV at its logical position (q rotated in place)."""
         kb.kap_append_kv(self.pool, k_new, v_new, q, self.pos_prop[i:], self.slots_prop[i:], self.inv_freq,
-                         num_tokens=self.R, tok_stride=self.k_prop, stream=stream)
+                         num_tokens=self.R, tok_stride=self.horizon, stream=stream)
 
     def propose(self, i: int, q: torch.Tensor, stream=None):
         """Proposal step i, second half: q = 1 attention over the compact view."""
@@ -122,6 +125,9 @@ class DecodeCycle:
         self.verify(q_ver, k_new_ver, v_new_ver, stream)
 
     def launches_per_cycle(self) -> int:
-        """Kernel launches of one run(): plan (2 or 1 selection + view + 2 slot maps) + 2 per step + 2 verify."""
+        """Kernel launches of one run(): selection (score + top-K, or spans), the view (with the horizon's slot
+        mapping), a separate window slot mapping when the windows differ from the horizon, an append and a
+        proposal kernel per step, then the window append and verification."""
         sel = 1 if self.spans is not None else 2
-        return sel + 1 + 2 + 2 * self.k_prop + 2
+        slots = 0 if self.window_is_horizon else 1
+        return sel + 1 + slots + 2 * self.k_prop + 2

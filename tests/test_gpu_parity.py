@@ -75,9 +75,11 @@ def test_view_and_slots_bit_exact(results, case):
                                                       res["sel_orc"][r, v, :n])
             assert vn[r, v] == len(cbt) and vns[r, v] == nsel
             assert np.array_equal(vbt[r, v, :len(cbt)], cbt) and np.array_equal(vlp[r, v, :len(clog)], clog)
-    slots = cyc.slots_prop.cpu().numpy().reshape(w.R, w.k_prop)
+    slots = cyc.slots_prop.cpu().numpy().reshape(w.R, cyc.horizon)
+    pos = cyc.pos_prop.cpu().numpy().reshape(w.R, cyc.horizon)
     for r in range(w.R):
-        for i in range(w.k_prop):
+        for i in range(cyc.horizon):
+            assert pos[r, i] == seq0[r] + i
             assert slots[r, i] == oracle.slot(bt[r], int(seq0[r]) + i)
     qo = w.q_offsets.cpu().numpy()
     sv = cyc.slots_ver.cpu().numpy()
