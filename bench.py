@@ -5,7 +5,9 @@ One step = one proposal/verification cycle of the whole hot path over `--layers`
 (replicas with their own KV pools), on the Llama-3-8B-shaped workload: 4 requests x 32768-token prompts, Hq=32,
 Hkv=8, d=128, bf16 KV, per-KV-head K-summary scoring with A1R2K125 selection (s = 6.25%), 4 proposal steps (q=1)
 and a verify window of 4 (causal). Per layer and cycle: score + top-K, view compilation, two slot mappings, then
-4 x (KV append + proposal attention), then window append + verification attention.
+4 x (KV append + proposal attention), then window append + verification attention. View compilation also
+writes the slot mapping of the cycle's new tokens, so no separate slot-mapping launch runs when every verify
+window equals the proposal horizon.
 
 Output: one JSON line (rank 0). `value` is the algorithmic HBM bytes of every hot-path kernel in a step divided by
 the device time of the step (GB/s, whole job); the phase times come from CUDA events recorded between CUDA-graph
@@ -42,6 +44,7 @@ def parse_args(argv=None):
     ap.add_argument("--layers", type=int, default=8)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clock-log", default=None, help="CSV file for the nvidia-smi samples of the timed region")
     return ap.parse_args(argv)
 
 
@@ -81,13 +84,18 @@ class ClockSampler:
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, path=None):
+        import tempfile
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+        if path is None:
+            fd, path = tempfile.mkstemp(prefix=f"kap_clocks{index}_", suffix=".csv")
+            os.close(fd)
+        self.path = path
 
     def start(self):
-        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        if os.path.dirname(self.path):
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
@@ -126,7 +134,7 @@ class ClockSampler:
 
 # --------------------------------------------------------------------------------------------- byte model
 def step_bytes(w, cyc, sel_ids, n_sel):
-    """Algorithmic HBM bytes of one cycle on one layer, per kernel family (SURVEY-style unit counts):
+    """Algorithmic HBM bytes of one cycle on one layer, per kernel family:
     scores read every prompt page's fp32 summary; proposal step i reads K and V of every visible token of the
     view (selected prompt tokens + generated tokens up to the step's position); verification reads K and V of
     every position up to the last window row; appends write K and V of the new tokens."""
@@ -154,6 +162,38 @@ def step_bytes(w, cyc, sel_ids, n_sel):
     ver = int(((seq0 + nq) * w.Hkv * kv_tok).sum())
     app = int((w.k_prop * w.R + nq.sum()) * w.Hkv * w.d * 2 * 2)
     return dict(score=score, propose=prop, verify=ver, append=app)
+
+
+# ------------------------------------------------------------------------------------------ recorded counters
+KERNEL_SOURCES = {"verify_tc_kernel": ["k_verify.cu", "kap_device.cuh"],
+                  "propose_kernel": ["k_propose.cu", "kap_device.cuh"]}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """SHA-256 of the kernel's sources with comments and blank space removed (a comment edit keeps the record)."""
+    import hashlib
+    import re
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "selected_kv_sparse_gb300", "csrc", f)) as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
+    return h.hexdigest()
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes (read + write) per launch of `kernel` from the ncu capture summarised in profiles/, or None when
+    no capture exists or the kernel's source has changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        rec = json.load(open(path))[kernel]
+        if rec.get("source_sha256") != kernel_source_hash(kernel):
+            return None
+        return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        return None
 
 
 # ------------------------------------------------------------------------------------------------ oracle arm
@@ -307,7 +347,7 @@ def run_kap(args, world, rank, local):
         dist.barrier()
     K = args.steps
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(graphs) + 1)] for _ in range(K)]
-    sampler = ClockSampler(local)
+    sampler = ClockSampler(local, args.clock_log)
     sampler.start()
     time.sleep(0.05)
     t_start = torch.cuda.Event(enable_timing=True)
@@ -339,13 +379,7 @@ def run_kap(args, world, rank, local):
     ver_gbs = ver_bytes_launch / (ver_launch_ms * 1e-3) / 1e9
     prop_gbs = prop_bytes_launch / (prop_launch_ms * 1e-3) / 1e9
     plan_ms = phase_ms["plan"] / (K * L)
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "verify_traffic.json")
-    if os.path.exists(tpath):
-        try:
-            traffic = json.load(open(tpath)).get("dram_bytes_per_launch")
-        except Exception:
-            traffic = None
+    traffic = recorded_traffic("verify_tc_kernel")
 
     # end to end: inputs from pinned host memory, results back, through the same calls
     e2e = None
@@ -389,10 +423,16 @@ def run_kap(args, world, rank, local):
         oracle.build()
         nth = oracle.hardware_threads()
         w_cpu = make_workload(CONFIG, device="cpu", poison=False)
-        dt, b = oracle_sample(w_cpu, nth)
+        dt = b = 0.0
+        n_cyc = 0
+        while dt < 10.0:     # about ten seconds of oracle work, cycling over the requests
+            t_, b_ = oracle_sample(w_cpu, nth, r=n_cyc % w_cpu.R)
+            dt += t_
+            b += b_
+            n_cyc += 1
         cpu = {"value": b / dt / 1e9, "unit": "GB/s", "cores": nth, "kind": "oracle",
-               "sample": "one request of one layer, one full cycle (summaries, scores, A1R2K125 top-K, 4 proposals, "
-                         f"verify window 4) in fp64, {dt:.2f} s"}
+               "sample": f"{n_cyc} full cycles, each one request of one layer (summaries, fixed-order scores, "
+                         f"A1R2K125 top-K, 4 proposals, verify window 4) in fp64: {dt:.1f} s"}
 
     if rank == 0:
         line = {

@@ -81,8 +81,8 @@ typedef struct {
 
 /* Compact selected-KV view, written by kap_compile_view and read by kap_attn_propose.
  * Row (r, v) with v < rows_per_seq lists the visible pages of request r for KV head v (or for all heads when
- * rows_per_seq == 1): first the n_selected selected prompt pages in ascending logical order ("compacted in
- * access order"), then the tail pages holding positions >= ctx_len, up to the horizon given at compile time. */
+ * rows_per_seq == 1): first the n_selected selected prompt pages in ascending logical order (the order in which
+ * they are accessed), then the tail pages holding positions >= ctx_len, up to the horizon given at compile time. */
 typedef struct {
   int32_t rows_per_seq;   /* Hkv (per-head views) or 1 (one view shared by all heads) */
   int32_t cap;            /* entries per row */
@@ -110,7 +110,7 @@ typedef struct {
 kap_status kap_build_summaries(const kap_kv_pool *pool, const kap_page_map *map, kap_stream stream);
 
 /* Page scoring and A/R/K top-K. KRI page (KRI-Q row; A<a>R<r>K<k> tag and its 128-block example) and
- * EarlySelectKV page (score and top-k over the K-summary cache, proxy query allowed).
+ * EarlySelectKV page (routing ranks pages by their K summaries, possibly against a proxy query).
  *   q_dev     [R][Hq][d] pool dtype: the routing query (the real query or a proxy).
  *   qbar[h]   = sum over g < G of q[h*G+g] (fp32, g ascending).
  *   score     = dot(qbar[h], k_summary[page][h]) in the fixed 32-lane order: lane l accumulates fmaf over
@@ -138,7 +138,7 @@ kap_status kap_select_spans(const kap_page_map *map, const int32_t *spans_dev, c
  * j >= floor(ctx_len/16) with 16j < seq_len + horizon_tokens that is not already selected.
  *   sel_rows_per_seq/sel_cap give the layout of sel_ids; view->rows_per_seq must equal sel_rows_per_seq.
  *   fallback_dev     optional [R] out: 1 when request r's retained prompt fraction n_sel/N exceeds s_max,
- *                    else 0 (KAP paper, fallback: "retains too much KV").
+ *                    else 0 (KAP paper, fallback: the plan keeps too large a share of the KV).
  *   slot_out/pos_out optional [R][horizon_tokens] out: the slot mapping of the tokens the cycle will append,
  *                    at positions seq_len[r] + i (same rule as kap_slot_mapping); NULL to skip.
  * Returns KAP_ECAPACITY when view->cap < sel_cap + ceil(horizon/16) + 1. */
@@ -147,10 +147,10 @@ kap_status kap_compile_view(const kap_page_map *map, const int32_t *sel_ids, con
                             const kap_view *view, int32_t *fallback_dev, float s_max, int64_t *slot_out,
                             int32_t *pos_out, kap_stream stream);
 
-/* Slot mapping. KAP paper, selected-KV view ("slot mappings place newly scheduled tokens into their
- * physical KV slots"). Request r owns tokens tok_offsets[r] .. tok_offsets[r+1]-1; token j sits at
- * pos = start_pos[r] + (j - tok_offsets[r]) and slot = block_table[r][pos/16]*16 + pos%16 (-1 when the page is
- * outside the table or negative). Writes slot_out[j] and pos_out[j]. */
+/* Slot mapping. KAP paper, selected-KV view (each newly scheduled token is sent to its physical KV slot).
+ * Request r owns tokens tok_offsets[r] .. tok_offsets[r+1]-1; token j sits at pos = start_pos[r] + (j -
+ * tok_offsets[r]) and slot = block_table[r][pos/16]*16 + pos%16 (-1 when the page is outside the table or
+ * negative). Writes slot_out[j] and pos_out[j]. */
 kap_status kap_slot_mapping(const kap_page_map *map, const int32_t *tok_offsets_dev, const int32_t *start_pos_dev,
                             int32_t num_tokens, int64_t *slot_out, int32_t *pos_out, kap_stream stream);
 

@@ -1,7 +1,7 @@
 """Memory-traffic cost model of one proposal/verification cycle (test infrastructure only).
 
 KAP paper, Section 4 (cost model), with the equations as printed in its agifrontier.github.io tutorial:
-  Cost_base = (1 + k h) (W_main + KV)                 standard decoding for the same expected output
+  Cost_base = (1 + k h) (W_main + KV)                 plain decoding of as many tokens as a cycle yields
   Cost_plan = k (W_prop + s KV) + (W_main + KV)       k selected-KV proposals, then one full verification
   with W_prop = W_main the plan wins iff (h - s) KV > (1 - h) W_main     (Eq. 9, the phase boundary)
   KV_crit = (1 - h) W_main / (h - s)                  the context size at which the boundary is crossed

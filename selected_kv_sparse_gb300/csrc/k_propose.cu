@@ -2,8 +2,8 @@
 //
 // KAP paper, executor: each proposal step is a decode-like step (q_prop = 1) whose attention sees only the
 // selected prompt pages of the compact view, plus every generated token, at the original logical positions.
-// EarlySelectKV page: the main flow gathers KV at precomputed page indices and runs sparse attention with the real
-// query.
+// EarlySelectKV page: attention of the main flow reads only the pages the routing side chose in advance, and uses
+// the true query.
 //
 // Design (GB300):
 //  * Work = the concatenated entry lists of all (request, KV head) rows; CTA b owns the contiguous entry range
@@ -12,7 +12,7 @@
 //  * A producer warp streams the CTA's entries through a ring of page slots: per entry one 1-D bulk copy
 //    (cp.async.bulk) of the 4 KiB (page, head) chunk of K and one of V, completing on the slot's mbarrier. With
 //    ~20 slots most of a CTA's range is in flight at once.
-//  * Eight consumer warps take the entries of a row segment round-robin and work independently: lane l holds 16
+//  * Twelve consumer warps take the entries of a row segment round-robin and work independently: lane l holds 16
 //    bytes of each token row (coalesced, conflict-free), computes partial dot products for the G query heads of the
 //    KV head, and a reduce-scatter across the lanes of a row leaves each lane owning a few finished logits. Each
 //    warp keeps its own running max, sum and output; the max is only raised (and the state rescaled) when a page

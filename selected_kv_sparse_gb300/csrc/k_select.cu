@@ -1,7 +1,7 @@
 // k_select.cu - K-summary cache, page scoring, A<a>R<r>K<k> top-K, span selection, compact view compilation and
 // slot mapping for the selected-KV hot path (sm_103a).
 //
-// Sources: EarlySelectKV news page (score and top-k over a K-summary cache, proxy query), KRI page (KRI-Q:
+// Sources: EarlySelectKV news page (pages ranked by their K summaries, proxy query allowed), KRI page (KRI-Q:
 // Q . block-mean K; the A<a>R<r>K<k> tag), KAP paper (compiler: spans resolved to KV pages, compact view in access
 // order with logical positions, block tables and slot mappings).
 #include "kap_device.cuh"
