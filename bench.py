@@ -4,10 +4,9 @@
 One step = one proposal/verification cycle of the whole hot path over `--layers` independent attention layers
 (replicas with their own KV pools), on the Llama-3-8B-shaped workload: 4 requests x 32768-token prompts, Hq=32,
 Hkv=8, d=128, bf16 KV, per-KV-head K-summary scoring with A1R2K125 selection (s = 6.25%), 4 proposal steps (q=1)
-and a verify window of 4 (causal). Per layer and cycle: score + top-K, view compilation, two slot mappings, then
-4 x (KV append + proposal attention), then window append + verification attention. View compilation also
-writes the slot mapping of the cycle's new tokens, so no separate slot-mapping launch runs when every verify
-window equals the proposal horizon.
+and a verify window of 4 (causal). Per layer and cycle: score + top-K, view compilation (which also writes the slot
+mapping of the cycle's new tokens), then 4 proposal steps, each one kernel that appends the step token's KV and
+attends over the view (--unfused: a KV-append kernel and a proposal kernel), then window append + verification.
 
 Output: one JSON line (rank 0). `value` is the algorithmic HBM bytes of every hot-path kernel in a step divided by
 the device time of the step (GB/s, whole job); the phase times come from CUDA events recorded between CUDA-graph
@@ -44,6 +43,7 @@ def parse_args(argv=None):
     ap.add_argument("--layers", type=int, default=8)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--unfused", action="store_true", help="separate KV-append and proposal launches per step")
     ap.add_argument("--clock-log", default=None, help="CSV file for the nvidia-smi samples of the timed region")
     return ap.parse_args(argv)
 
@@ -295,7 +295,7 @@ def run_kap(args, world, rank, local):
         a, r, k = (int(x) for x in w.ark[0].tolist())
         pol = kap.AccessPolicy(a, r, k, True, w.sel_cap())
         cyc = kap.DecodeCycle(pool, w.block_table, w.ctx_len, w.seq_len0, w.k_prop, w.n_q,
-                              kap.rope_inv_freq(w.d, w.theta, dev), policy=pol)
+                              kap.rope_inv_freq(w.d, w.theta, dev), policy=pol, fused=not args.unfused)
         ins = dict(q_route=w.q_route.clone(), q_prop=w.q_prop.clone(), k_prop=w.k_new_prop.clone(),
                    v_prop=w.v_new_prop.clone(), q_ver=w.q_ver.clone(), k_ver=w.k_new_ver.clone(),
                    v_ver=w.v_new_ver.clone())
@@ -304,9 +304,13 @@ def run_kap(args, world, rank, local):
 
     phases = [("plan", lambda: [c.plan(x["q_route"]) for _, c, x in layers])]
     for i in range(k_prop):
-        phases.append((f"app{i}", lambda i=i: [c.append_step(i, x["q_prop"][i], x["k_prop"][i], x["v_prop"][i])
-                                                for _, c, x in layers]))
-        phases.append((f"prop{i}", lambda i=i: [c.propose(i, x["q_prop"][i]) for _, c, x in layers]))
+        if args.unfused:
+            phases.append((f"app{i}", lambda i=i: [c.append_step(i, x["q_prop"][i], x["k_prop"][i], x["v_prop"][i])
+                                                    for _, c, x in layers]))
+            phases.append((f"prop{i}", lambda i=i: [c.propose(i, x["q_prop"][i]) for _, c, x in layers]))
+        else:   # the step's KV append runs inside the proposal kernel
+            phases.append((f"prop{i}", lambda i=i: [c.propose_step(i, x["q_prop"][i], x["k_prop"][i], x["v_prop"][i])
+                                                    for _, c, x in layers]))
     phases.append(("vapp", lambda: [c.append_window(x["q_ver"], x["k_ver"], x["v_ver"]) for _, c, x in layers]))
     phases.append(("ver", lambda: [c.verify(x["q_ver"]) for _, c, x in layers]))
 
@@ -434,6 +438,7 @@ def run_kap(args, world, rank, local):
                "sample": f"{n_cyc} full cycles, each one request of one layer (summaries, fixed-order scores, "
                          f"A1R2K125 top-K, 4 proposals, verify window 4) in fp64: {dt:.1f} s"}
 
+    dev_err = kap.kap_device_error()   # nonzero: a kernel met a bad page, length or timed-out wait
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
@@ -456,6 +461,7 @@ def run_kap(args, world, rank, local):
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches_per_step * K,
+            "device_error": dev_err,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

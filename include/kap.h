@@ -177,6 +177,23 @@ kap_status kap_attn_propose(const kap_kv_pool *pool, const kap_page_map *map, co
                             kap_stream stream);
 size_t kap_propose_workspace_size(int32_t num_seqs, int32_t num_kv_heads, int32_t num_q_heads, int32_t head_dim);
 
+/* One proposal step with the step token's KV append fused in. KAP paper, executor (a proposal step writes its own
+ * token's KV at that token's logical position through the view's slots and attends over the compact view).
+ * Same pool, map, view, outputs and workspace as kap_attn_propose; in addition, for every request r:
+ *   - the step token sits at position P = seq_len[r] - 1, which must lie on a page of the view (view compiled with
+ *     a horizon that covers the step); a request whose P lies on no view page gets no append and sets device error
+ *     bit 4;
+ *   - k_new, v_new [R][Hkv][d] (pool dtype): the token's key before RoPE and its value. K = RoPE(k_new, P) and
+ *     V = v_new are written into the pool at P's slot and take part in this step's attention;
+ *   - q_dev [R][Hq][d] holds the step's queries BEFORE RoPE; they are rotated at P inside the call (the buffer is
+ *     only read);
+ *   - inv_freq_dev [d/2] fp32, as for kap_append_kv.
+ * The result equals kap_append_kv at positions seq_len-1 (q rotated) followed by kap_attn_propose: the rotation
+ * and its rounding into the pool dtype are the same. */
+kap_status kap_append_propose(const kap_kv_pool *pool, const kap_page_map *map, const kap_view *view,
+                              const void *q_dev, const void *k_new, const void *v_new, const float *inv_freq_dev,
+                              void *out, float *lse, void *workspace, size_t workspace_bytes, kap_stream stream);
+
 /* Full-context verification attention, q = n_q per request, causal among the candidates. KAP paper, verifier
  * (short contiguous query window over the full KV cache, full block table and original positions).
  *   q_dev [total_q][Hq][d], out [total_q][Hq][d] (pool dtype), lse [total_q][Hq] fp32.

@@ -11,5 +11,5 @@ from ._binding import (  # noqa: F401
     kap_score_workspace_size, kap_select_spans, kap_slot_mapping, kap_verify_workspace_size, load, parse_ark,
     rope_inv_freq, workspace, LIB_PATH,
 )
-from ._binding import kap_attn_propose_noalloc, kap_noalloc_scratch_bytes  # noqa: F401
+from ._binding import kap_append_propose, kap_attn_propose_noalloc, kap_noalloc_scratch_bytes  # noqa: F401
 from .pipeline import DecodeCycle  # noqa: F401

@@ -72,6 +72,7 @@ def _declare(lib):
         "kap_slot_mapping": ([P, P, P, I, P, P, P], I),
         "kap_append_kv": ([P, P, P, P, P, P, I, I, P, P], I),
         "kap_attn_propose": ([P, P, P, P, P, P, P, Z, P], I),
+        "kap_append_propose": ([P, P, P, P, P, P, P, P, P, P, Z, P], I),
         "kap_propose_workspace_size": ([I, I, I, I], Z),
         "kap_attn_verify": ([P, P, P, P, P, P, P, Z, P], I),
         "kap_verify_workspace_size": ([I, I, I, I, I], Z),
@@ -324,6 +325,24 @@ def kap_attn_propose(pool: KVPool, pmap: PageMap, view: View, q: torch.Tensor, o
     _check("kap_attn_propose", lib.kap_attn_propose(ctypes.byref(p), ctypes.byref(m), ctypes.byref(v), _ptr(q),
                                                     _ptr(out), _ptr(lse), _ptr(workspace),
                                                     workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def kap_append_propose(pool: KVPool, pmap: PageMap, view: View, q: torch.Tensor, k_new: torch.Tensor,
+                       v_new: torch.Tensor, inv_freq: torch.Tensor, out: torch.Tensor, lse: torch.Tensor,
+                       workspace: torch.Tensor, stream=None):
+    """One proposal step with the step token's KV append fused in: the token of request r sits at seq_len[r]-1;
+    q holds the step's queries before RoPE (read only)."""
+    lib = load()
+    if any(t.dtype != pool.dtype for t in (q, k_new, v_new, out)) or lse.dtype != torch.float32:
+        raise TypeError("q, k_new, v_new and out must have the pool dtype and lse fp32")
+    if inv_freq.dtype != torch.float32:
+        raise TypeError("inv_freq must be fp32")
+    p, m, v = pool._c(), pmap._c(), view._c()
+    _check("kap_append_propose", lib.kap_append_propose(ctypes.byref(p), ctypes.byref(m), ctypes.byref(v), _ptr(q),
+                                                        _ptr(k_new), _ptr(v_new), _ptr(inv_freq), _ptr(out),
+                                                        _ptr(lse), _ptr(workspace),
+                                                        workspace.numel() * workspace.element_size(),
+                                                        _stream(stream)))
 
 
 def kap_attn_propose_noalloc(pool: KVPool, pmap: PageMap, view: View, q: torch.Tensor, out: torch.Tensor,

@@ -19,6 +19,7 @@ __global__ void __launch_bounds__(256) append_kernel(T *__restrict__ Kp, T *__re
                                                      const float *__restrict__ inv_freq, int hkv, int hq,
                                                      int num_pages, int *err) {
   constexpr int HALF = D / 2;
+  grid_dependency_sync();
   const int warps_per_cta = blockDim.x >> 5;
   const int64_t wid = static_cast<int64_t>(blockIdx.x) * warps_per_cta + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -52,11 +53,8 @@ __global__ void __launch_bounds__(256) append_kernel(T *__restrict__ Kp, T *__re
   }
   for (int i = lane; i < HALF; i += 32) {
     const float x = to_f(src[i]), y = to_f(src[i + HALF]);
-    const float ang = static_cast<float>(p) * inv_freq[i];
-    float sn, cs;
-    sincosf(ang, &sn, &cs);
-    const float xr = x * cs - y * sn;
-    const float yr = x * sn + y * cs;
+    float xr, yr;
+    rope_pair(x, y, p, inv_freq[i], xr, yr);
     dst[i] = from_f<T>(xr);
     dst[i + HALF] = from_f<T>(yr);
   }
@@ -72,10 +70,10 @@ cudaError_t launch_append(const PoolArgs &p, const void *k_new, const void *v_ne
   const int64_t warps = static_cast<int64_t>(T) * rows;
   const int blocks = static_cast<int>((warps + 7) / 8);
 #define KAP_APPEND(TT, D)                                                                                       \
-  append_kernel<TT, D><<<blocks, 256, 0, s>>>(                                                                 \
-      static_cast<TT *>(const_cast<void *>(p.k)), static_cast<TT *>(const_cast<void *>(p.v)),                    \
-      static_cast<const TT *>(k_new), static_cast<const TT *>(v_new), static_cast<TT *>(q_inout), pos, slots, T, \
-      tok_stride, inv_freq, p.hkv, p.hq, p.num_pages, err)
+  launch_pdl(append_kernel<TT, D>, dim3(blocks), dim3(256), 0, s,                                               \
+             static_cast<TT *>(const_cast<void *>(p.k)), static_cast<TT *>(const_cast<void *>(p.v)),             \
+             static_cast<const TT *>(k_new), static_cast<const TT *>(v_new), static_cast<TT *>(q_inout), pos,     \
+             slots, T, tok_stride, inv_freq, p.hkv, p.hq, p.num_pages, err)
   if (p.dtype == 0 && p.d == 128) KAP_APPEND(__nv_bfloat16, 128);
   else if (p.dtype == 0 && p.d == 64) KAP_APPEND(__nv_bfloat16, 64);
   else if (p.dtype == 1 && p.d == 128) KAP_APPEND(float, 128);

@@ -1,7 +1,9 @@
-// k_propose.cu - selected-KV proposal attention, q = 1 per request (sm_103a).
+// k_propose.cu - selected-KV proposal attention, q = 1 per request (sm_103a), optionally fused with the step's
+// KV append.
 //
 // KAP paper, executor: each proposal step is a decode-like step (q_prop = 1) whose attention sees only the
-// selected prompt pages of the compact view, plus every generated token, at the original logical positions.
+// selected prompt pages of the compact view, plus every generated token, at the original logical positions; the
+// step writes its own token's KV at that token's logical position.
 // EarlySelectKV page: attention of the main flow reads only the pages the routing side chose in advance, and uses
 // the true query.
 //
@@ -10,33 +12,42 @@
 //    [b*E/nb, (b+1)*E/nb) (stream-K, one CTA per SM), so long and short rows balance across the SMs. A row split
 //    over several CTAs is merged by the last CTA to finish it (one atomic counter per row, no waiting).
 //  * A producer warp streams the CTA's entries through a ring of page slots: per entry one 1-D bulk copy
-//    (cp.async.bulk) of the 4 KiB (page, head) chunk of K and one of V, completing on the slot's mbarrier. With
-//    ~20 slots most of a CTA's range is in flight at once.
-//  * Twelve consumer warps take the entries of a row segment round-robin and work independently: lane l holds 16
-//    bytes of each token row (coalesced, conflict-free), computes partial dot products for the G query heads of the
-//    KV head, and a reduce-scatter across the lanes of a row leaves each lane owning a few finished logits. Each
-//    warp keeps its own running max, sum and output; the max is only raised (and the state rescaled) when a page
-//    exceeds it by more than 2^8, which is exact. Warps meet only at the end of a row segment, where their states
-//    are combined.
+//    (cp.async.bulk) of the 4 KiB (page, head) chunk of K and one of V, completing on the slot's mbarrier. A view
+//    entry and its row's lengths are loaded together, so a copy leaves two dependent loads after the kernel starts.
+//  * The range is cut into windows of at most 11 row segments. Each segment gets its own group of consumer warps
+//    (one at least, the others in proportion to its entries) that takes the segment's entries round-robin, so all
+//    segments of a window stream at once. Lane l holds 16 bytes of each token row; packed fp32 pair FMAs form the
+//    G heads' partial dot products and the P.V update, and a reduce-scatter across the lanes of a token row leaves
+//    each lane a few finished logits. Each warp keeps its own running max, sum and output; the max is only raised
+//    (and the state rescaled) when a page exceeds it by more than 2^8, which is exact.
+//  * A group that has finished its segment combines its warps' states behind its own named barrier and writes the
+//    row's output, or hands a partial record to the row's last CTA, while the other groups keep streaming.
+//  * Fused append: the step token of request r sits at position P = seq_len[r] - 1. Every warp rotates its copy of
+//    the query at P; the warp that consumes the page holding P rotates the token's key, writes K and V into the
+//    pool and patches its shared-memory copy of the page before using it.
 #include "kap_device.cuh"
 #include "kap_launch.h"
 
 namespace kap {
 namespace {
 
-constexpr int kNCW = 12;                     // consumer warps
+constexpr int kNCW = 11;                     // consumer warps (12 warps in all: 3 per SM sub-partition)
 constexpr int kThreads = (kNCW + 1) * 32;    // + the producer warp (warp kNCW)
 constexpr int kMaxSlotsExtraCtas = 4096;     // bound on the grid, for workspace sizing
-constexpr int kMaxSeg = 32;                  // row segments per window of a CTA's range
+constexpr int kMaxSeg = kNCW;                // row segments per window (each gets at least one warp)
 constexpr int kMaxRowsScan = 2048;           // rows whose entry offsets are scanned into shared memory at once
+constexpr int kBarSeg0 = 1;                  // named barriers kBarSeg0 .. kBarSeg0 + kMaxSeg - 1, one per segment
+constexpr int kMergeChunk = 8;               // partial records loaded at once by a merging CTA
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;    // log2 units
+static_assert(kBarSeg0 + kMaxSeg <= 16, "named barriers");
 
 template <class T, int D, int G>
 struct Cfg {
   static constexpr int ESZ = sizeof(T);
   static constexpr int EPL = 16 / ESZ;           // elements per 16-byte vector
+  static constexpr int EP2 = EPL / 2;            // fp32 pairs per vector
   static constexpr int LPT = D * ESZ / 16;       // lanes covering one token row
   static constexpr int TPI = 32 / LPT;           // token rows per warp-wide 16-byte load
   static constexpr int NI = kPage / TPI;         // 16-byte vectors per lane per (page, head) chunk
@@ -44,32 +55,33 @@ struct Cfg {
   static constexpr int NV = ((NI * G + LPT - 1) / LPT) * LPT;  // reduce-scatter values (padded)
   static constexpr int VPL = NV / LPT;           // finished logits owned by each lane
   static constexpr int LOG_LPT = LPT == 8 ? 3 : (LPT == 16 ? 4 : 5);
+  static constexpr int REC = G * D + 2 * G;      // floats of one warp's state record (o, m, l)
   // shared memory carve-up (bytes)
-  static constexpr int COMB = kNCW * (G * D + 2 * G) * 4;  // per-warp segment states
-  static constexpr int WLOG = kNCW * G * kPage * 4;        // per-warp logits / probabilities of one page
-  static constexpr int RES = (G * D + 4 * G) * 4;          // combined segment state (+ merge scalars)
-  static constexpr int SEGB = kMaxSeg * 56;                // segment table
-  static constexpr int ROWB = kMaxRowsScan * 4;            // per-row entry offsets (row scan)
-  static constexpr int FIXED = COMB + WLOG + RES + SEGB + ROWB + 2048;
-  static constexpr int SLOT = 2 * CHUNK;                   // K and V of one entry
-  static constexpr int SLOTS_FIT = (200 * 1024 - FIXED) / SLOT;
+  static constexpr int COMB = kNCW * REC * 4;             // per-warp state records
+  static constexpr int WLOG = kNCW * G * kPage * 4;       // per-warp logits / probabilities of one page
+  static constexpr int SWT = kMaxSeg * G * (kNCW + 2) * 4;  // per segment: warp weights, max and sum per head
+  static constexpr int SEGB = kMaxSeg * 48;               // segment table
+  static constexpr int ROWB = (kMaxRowsScan + 1) * 4;     // per-row entry offsets (row scan)
+  static constexpr int FIXED = COMB + WLOG + SWT + SEGB + ROWB + 1024;
+  static constexpr int SLOT = 2 * CHUNK;                  // K and V of one entry
+  static constexpr int SLOTS_FIT = (200 * 1024 - FIXED) / (SLOT + 32);
   static constexpr int SLOTS = SLOTS_FIT > 32 ? 32 : SLOTS_FIT;
-  static constexpr int BATCH = SLOTS < 16 ? SLOTS : 16;    // entries the producer handles per step
+  static constexpr int BATCH = SLOTS < 16 ? SLOTS : 16;   // entries the producer handles per step
   static constexpr int OFF_KV = 0;
   static constexpr int OFF_COMB = OFF_KV + SLOTS * SLOT;
   static constexpr int OFF_WLOG = OFF_COMB + COMB;
-  static constexpr int OFF_RES = OFF_WLOG + WLOG;
-  static constexpr int OFF_SEG = ((OFF_RES + RES + 15) / 16) * 16;
-  static constexpr int OFF_SMETA = ((OFF_SEG + SEGB + 15) / 16) * 16;  // [SLOTS] (tlo, thi)
-  static constexpr int OFF_BAR = OFF_SMETA + SLOTS * 8;                // full[SLOTS], empty[SLOTS]
-  static constexpr int OFF_ROWS = OFF_BAR + 2 * SLOTS * 8;             // [kMaxRowsScan + 1] int32
-  static constexpr int SMEM = OFF_ROWS + ROWB + 4;
+  static constexpr int OFF_SWT = OFF_WLOG + WLOG;
+  static constexpr int OFF_SEG = ((OFF_SWT + SWT + 15) / 16) * 16;
+  static constexpr int OFF_SMETA = OFF_SEG + SEGB;        // [SLOTS] int4 (tlo | thi << 16, step token, page, entry)
+  static constexpr int OFF_BAR = OFF_SMETA + SLOTS * 16;  // full[SLOTS], empty[SLOTS]
+  static constexpr int OFF_ROWS = OFF_BAR + 2 * SLOTS * 8;
+  static constexpr int SMEM = OFF_ROWS + ROWB;
   static_assert(SLOTS >= 4, "too few page slots");
-  static_assert(WLOG >= 2 * 32 * G * 4, "merge scratch does not fit");
+  static_assert(EPL % 2 == 0 && (D / 2) % EPL == 0, "vector layout");
 };
 
 struct Params {
-  const void *k, *v;
+  const void *k, *v;  // pool; written only by the fused append
   int num_pages, hkv, hq;
   const int32_t *ctx_len, *seq_len;
   const int32_t *vbt, *vlp, *vn, *vnsel;
@@ -82,15 +94,17 @@ struct Params {
   float *ml;      // [slots][G][2]
   float *part;    // [slots][G][D]
   int *err;
+  const void *k_new, *v_new;  // fused append: [R][Hkv][D] step-token keys (before RoPE) and values, or null
+  const float *inv_freq;      // [D/2]
 };
 
-// One row segment of a CTA's range: global entries [b, e) of attention row `row` (whose own range is [rb, re)),
-// with the row-level metadata the producer and the consumers need.
+// One row segment of a window: global entries [b, e) of attention row `row` (whose own range is [rb, re)),
+// consumed by warps [w0, w0 + nw).
 struct Seg {
   int64_t b, e, rb, re;
-  int row, vr, L, S, nsel, pad;
+  int row, vr, w0, nw;
 };
-static_assert(sizeof(Seg) == 56, "segment record size");
+static_assert(sizeof(Seg) == 48, "segment record size");
 
 __device__ __forceinline__ int view_row(const Params &p, int row) {
   const int r = row / p.hkv, h = row - r * p.hkv;
@@ -103,30 +117,94 @@ __device__ __forceinline__ int row_entries(const Params &p, int row) {
 __device__ __forceinline__ int owner_cta(int64_t x, int64_t E, int nb) {
   return static_cast<int>(((x + 1) * nb - 1) / E);
 }
-__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kNCW * 32) : "memory"); }
+__device__ __forceinline__ void group_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int *p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ int ld_acquire_shared(const int *p) {
+  int v;
+  asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+
+// Waits until ring entry kk (this CTA's entry index) has landed in its slot. Warp groups consume the ring out of
+// order, so the slot's previous occupant (entry kk - SLOTS) may not have landed yet, and the full barrier's phase
+// parity alone cannot tell the two apart: first wait for the producer to stamp the slot with kk (it does so only
+// after the previous occupant was consumed), then for the barrier phase. Both waits are bounded.
+__device__ __forceinline__ bool wait_entry(const int *stamp, uint64_t *full, int kk, uint32_t parity, int *err) {
+  for (uint32_t i = 0; ld_acquire_shared(stamp) != kk; ++i) {
+    if (i == kWaitPolls) {
+      set_error(err, kErrTimeout);
+      return false;
+    }
+    __nanosleep(32);
+  }
+  return mbar_wait(full, parity, err);
+}
+
+// Inverse frequencies of the EPL consecutive rotary pairs starting at pair index i0 (a multiple of EPL).
+template <int EPL>
+__device__ __forceinline__ void load_inv_freq(const float *inv_freq, int i0, float *fr) {
+#pragma unroll
+  for (int k = 0; k < EPL; k += 4) {
+    const float4 f = *reinterpret_cast<const float4 *>(inv_freq + i0 + k);
+    fr[k] = f.x;
+    fr[k + 1] = f.y;
+    fr[k + 2] = f.z;
+    fr[k + 3] = f.w;
+  }
+}
+
+// Rotary factors (cos, sin) at position pos of the EPL pairs whose elements this lane holds (dims base_dim ..).
+template <int EPL, int D>
+__device__ __forceinline__ void rope_lane_factors(int base_dim, int pos, const float *inv_freq, float *cs, float *sn) {
+  float fr[EPL];
+  load_inv_freq<EPL>(inv_freq, base_dim < D / 2 ? base_dim : base_dim - D / 2, fr);
+#pragma unroll
+  for (int k = 0; k < EPL; ++k) rope_factors(pos, fr[k], cs[k], sn[k]);
+}
+
+// RoPE of the EPL values a lane holds: the other element of each pair is held by the lane LPT/2 away. Results are
+// rounded to the pool dtype, as a stored key or query would be.
+template <class T, int EPL, int LPT, int D>
+__device__ __forceinline__ void rope_lane_apply(float *x, int base_dim, const float *cs, const float *sn) {
+  const bool first = base_dim < D / 2;
+#pragma unroll
+  for (int k = 0; k < EPL; ++k) {
+    const float y = __shfl_xor_sync(0xffffffffu, x[k], LPT / 2);
+    float a, b;
+    rope_rotate(first ? x[k] : y, first ? y : x[k], cs[k], sn[k], a, b);
+    x[k] = to_f(from_f<T>(first ? a : b));
+  }
+}
 
 template <class T, int D, int G>
 __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
   using C = Cfg<T, D, G>;
-  constexpr int kCT = kNCW * 32;  // consumer threads
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char *kv = smem + C::OFF_KV;
-  float *comb = reinterpret_cast<float *>(smem + C::OFF_COMB);      // [kNCW][G*D + 2G]
+  float *comb = reinterpret_cast<float *>(smem + C::OFF_COMB);      // [kNCW][REC]
   float *wlog_all = reinterpret_cast<float *>(smem + C::OFF_WLOG);  // [kNCW][G][16]
-  float *res = reinterpret_cast<float *>(smem + C::OFF_RES);        // [G*D] output, then m[G], l[G], 2G scratch
+  float *swt_all = reinterpret_cast<float *>(smem + C::OFF_SWT);    // [kMaxSeg][G * kNCW + 2G]
   Seg *segs = reinterpret_cast<Seg *>(smem + C::OFF_SEG);
-  int2 *smeta = reinterpret_cast<int2 *>(smem + C::OFF_SMETA);
+  int4 *smeta = reinterpret_cast<int4 *>(smem + C::OFF_SMETA);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
   uint64_t *empty = full + C::SLOTS;
+  int *rowoff = reinterpret_cast<int *>(smem + C::OFF_ROWS);  // [nrows + 1] when nrows <= kMaxRowsScan
   __shared__ int64_t s_total, s_rb0, s_wnext_rb;
-  __shared__ int s_row0, s_nseg, s_wnext_row, s_flag;
+  __shared__ int s_row0, s_nseg, s_wnext_row;
+  __shared__ int s_last[kMaxSeg];
+  __shared__ int scan_scratch[32];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool fused = p.k_new != nullptr;
 
   // Entry offsets of the rows (one parallel load of every row's count, a block scan in shared memory), then E,
   // this CTA's range and the row holding its first entry. Rows beyond kMaxRowsScan use a warp scan in global order.
-  int *rowoff = reinterpret_cast<int *>(smem + C::OFF_ROWS);  // [nrows + 1] when nrows <= kMaxRowsScan
-  __shared__ int scan_scratch[32];
   if (tid == 0) {
     for (int i = 0; i < C::SLOTS; ++i) {
       mbar_init(&full[i], 1);
@@ -134,10 +212,11 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
     }
     fence_barrier_init();
   }
+  if (tid < C::SLOTS) smeta[tid].w = -1;  // no entry issued yet (shared memory keeps an earlier launch's stamps)
+  grid_dependency_sync();
   const bool small_rows = p.nrows <= kMaxRowsScan;
   if (small_rows) {
-    // thread t owns rows [t*per, (t+1)*per)
-    const int per = (p.nrows + kThreads - 1) / kThreads;
+    const int per = (p.nrows + kThreads - 1) / kThreads;  // thread t owns rows [t*per, (t+1)*per)
     const int lo = min(p.nrows, tid * per), hi = min(p.nrows, lo + per);
     int cnt = 0;
     for (int rr = lo; rr < hi; ++rr) {
@@ -174,9 +253,8 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
   const int64_t cta_begin = static_cast<int64_t>(blockIdx.x) * E / nb;
   const int64_t cta_end = static_cast<int64_t>(blockIdx.x + 1) * E / nb;
 
-  // First row of the range.
   if (small_rows) {
-    if (tid == 0) {  // last row whose start is <= cta_begin (and which is not empty)
+    if (tid == 0) {  // last row whose start is <= cta_begin
       int lo = 0, hi = p.nrows - 1;
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -218,10 +296,10 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
   int w_row = s_row0;
   int64_t w_rb = s_rb0;
 
-  // The range is processed in windows of up to kMaxSeg row segments (one warp-wide scan of 32 rows each).
   for (int64_t cur = cta_begin; cur < cta_end;) {
     if (warp == kNCW) {
-      // segment table of this window: rows w_row .. w_row+31 intersected with [cur, cta_end)
+      // ---- segment table of this window: rows w_row .. w_row+31 intersected with [cur, cta_end), at most
+      // kMaxSeg non-empty segments; each gets one warp plus a share of the spare warps by its entry count.
       const int row = w_row + lane;
       const int c = row < p.nrows ? (small_rows ? rowoff[row + 1] - rowoff[row] : row_entries(p, row)) : 0;
       int incl = c;
@@ -234,28 +312,45 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
       const int64_t sb = rb > cur ? rb : cur, se = re < cta_end ? re : cta_end;
       const bool nonempty = c > 0 && sb < se;
       const unsigned mask = __ballot_sync(0xffffffffu, nonempty);
-      if (nonempty) {
-        const int idx = __popc(mask & ((1u << lane) - 1u));
+      const int idx = __popc(mask & ((1u << lane) - 1u));
+      const int nseg = min(__popc(mask), kMaxSeg);
+      const bool keep = nonempty && idx < kMaxSeg;
+      const int cnt = keep ? static_cast<int>(se - sb) : 0;
+      int cinc = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, cinc, o);
+        if (lane >= o) cinc += v;
+      }
+      const int n = __shfl_sync(0xffffffffu, cinc, 31);
+      if (keep) {
+        const int64_t cum = cinc - cnt;
+        const int64_t spare = kNCW - nseg;
         Seg sg;
         sg.b = sb;
         sg.e = se;
         sg.rb = rb;
         sg.re = re;
         sg.row = row;
-        const int r = row / p.hkv;
         sg.vr = view_row(p, row);
-        sg.L = p.ctx_len[r];
-        sg.S = p.seq_len[r];
-        sg.nsel = p.vnsel[sg.vr];
-        sg.pad = 0;
+        sg.w0 = idx + static_cast<int>(spare * cum / n);
+        sg.nw = idx + 1 + static_cast<int>(spare * (cum + cnt) / n) - sg.w0;
         segs[idx] = sg;
       }
+      const unsigned dmask = __ballot_sync(0xffffffffu, nonempty && idx == kMaxSeg);  // first row left over
       const int tot = __shfl_sync(0xffffffffu, incl, 31);
-      if (lane == 0) {
-        s_nseg = __popc(mask);
+      if (dmask) {
+        const int dl = __ffs(dmask) - 1;
+        const int64_t drb = __shfl_sync(0xffffffffu, rb, dl);
+        if (lane == 0) {
+          s_wnext_row = w_row + dl;
+          s_wnext_rb = drb;
+        }
+      } else if (lane == 0) {
         s_wnext_row = w_row + 32;
         s_wnext_rb = w_rb + tot;
       }
+      if (lane == 0) s_nseg = nseg;
     }
     __syncthreads();
     const int nseg = s_nseg;
@@ -265,7 +360,9 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
       // ============================================================================================== producer
       for (int si = 0; si < nseg; ++si) {
         const Seg sg = segs[si];
-        const int h = sg.row - (sg.row / p.hkv) * p.hkv;
+        const int r = sg.row / p.hkv, h = sg.row - r * p.hkv;
+        const int L = p.ctx_len[r], S = p.seq_len[r], nsel = p.vnsel[sg.vr];
+        const int rn = static_cast<int>(sg.re - sg.rb);
         for (int64_t e0 = sg.b; e0 < sg.e; e0 += C::BATCH) {
           const int64_t e = e0 + lane;
           if (lane < C::BATCH && e < sg.e) {
@@ -274,17 +371,23 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
             const int lp = p.vlp[o];
             const int page = p.vbt[o];
             const int base = lp * kPage;
-            int thi = min(kPage, sg.S - base);
-            int tlo = (i < sg.nsel) ? 0 : max(0, sg.L - base);
+            int thi = min(kPage, S - base);
+            int tlo = (i < nsel) ? 0 : max(0, L - base);
             if (thi > tlo && (page < 0 || page >= p.num_pages)) {
               set_error(p.err, kErrPage);
               tlo = thi = 0;
             }
             if (thi <= tlo) tlo = thi = 0;
+            int step_tok = -1;
+            if (fused) {
+              const int tk = S - 1 - base;
+              if (tk >= tlo && tk < thi) step_tok = tk;
+              if (i == rn - 1 && base + kPage <= S - 1) set_error(p.err, kErrLength);  // the view misses P
+            }
             const int64_t k = e - cta_begin;
             const int slot = static_cast<int>(k % C::SLOTS);
             if (k >= C::SLOTS) mbar_wait(&empty[slot], static_cast<uint32_t>((k / C::SLOTS) - 1) & 1u, p.err);
-            smeta[slot] = make_int2(tlo, thi);
+            smeta[slot] = make_int4(tlo | (thi << 16), step_tok, page, static_cast<int>(k));
             if (thi > tlo) {
               const size_t off = (static_cast<size_t>(page) * p.hkv + h) * kPage * D;
               mbar_arrive_expect_tx(&full[slot], 2 * C::CHUNK);
@@ -297,324 +400,352 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
           __syncwarp();
         }
       }
-    } else {
+    } else if (nseg > 0) {
       // ============================================================================================= consumers
+      int si = 0;
+      while (si + 1 < nseg && segs[si + 1].w0 <= warp) ++si;
+      const Seg sg = segs[si];
+      const int gw = warp - sg.w0, nw = sg.nw;
+      const int r = sg.row / p.hkv, h = sg.row - r * p.hkv;
       float *wlog = wlog_all + warp * G * kPage;
-      for (int si = 0; si < nseg; ++si) {
-        const Seg sg = segs[si];
-        const int r = sg.row / p.hkv, h = sg.row - r * p.hkv;
-        float qf[G][C::EPL], o[G][C::EPL], m_run[G], l_own[C::VPL];
-        {
-          const T *qrow = static_cast<const T *>(p.q) + (static_cast<size_t>(r) * p.hq + h * G) * D + base_dim;
+      float2 qf[G][C::EP2], o[G][C::EP2];
+      float m_run[G], l_own[C::VPL];
+      const int P = fused ? p.seq_len[r] - 1 : 0;  // position of the step token (fused append)
+      {
+        const T *qrow = static_cast<const T *>(p.q) + (static_cast<size_t>(r) * p.hq + h * G) * D + base_dim;
+        uint4 qraw[G];
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
-            float tmp[C::EPL];
-            Vec16<T>::unpack(*reinterpret_cast<const uint4 *>(qrow + static_cast<size_t>(g) * D), tmp);
-#pragma unroll
-            for (int k = 0; k < C::EPL; ++k) {
-              qf[g][k] = tmp[k] * qscale;
-              o[g][k] = 0.0f;
-            }
-            m_run[g] = -INFINITY;
-          }
-#pragma unroll
-          for (int k = 0; k < C::VPL; ++k) l_own[k] = 0.0f;
-        }
-        // owned (token, head) pairs after the reduce-scatter: value v = j*G + g is token j*TPI + ts of head g
-        int g_own[C::VPL], tok_own[C::VPL];
-        bool ok_own[C::VPL];
-#pragma unroll
-        for (int k = 0; k < C::VPL; ++k) {
-          const int v = (lane % C::LPT) * C::VPL + k;
-          const int j = v / G;
-          g_own[k] = v - j * G;
-          tok_own[k] = j * C::TPI + ts;
-          ok_own[k] = v < C::NI * G;
-        }
-        for (int64_t e = sg.b + warp; e < sg.e; e += kNCW) {
-          const int64_t kk = e - cta_begin;
-          const int slot = static_cast<int>(kk % C::SLOTS);
-          mbar_wait(&full[slot], static_cast<uint32_t>(kk / C::SLOTS) & 1u, p.err);
-          const int2 tt = smeta[slot];
-          const int tlo = tt.x, thi = tt.y;
-          const unsigned char *kb = kv + slot * C::SLOT;
-          // ---- logits of the page's 16 tokens for the G heads
-          float part[C::NV];
-#pragma unroll
-          for (int v = 0; v < C::NV; ++v) part[v] = 0.0f;
-          if (thi > tlo) {
-            const uint4 *kvec = reinterpret_cast<const uint4 *>(kb);
-            uint4 w4[C::NI];
-#pragma unroll
-            for (int j = 0; j < C::NI; ++j) w4[j] = kvec[j * 32 + lane];
-#pragma unroll
-            for (int j = 0; j < C::NI; ++j) {
-              float kf[C::EPL];
-              Vec16<T>::unpack(w4[j], kf);
-#pragma unroll
-              for (int g = 0; g < G; ++g) {
-                float acc = 0.0f;
-#pragma unroll
-                for (int k = 0; k < C::EPL; ++k) acc = fmaf(qf[g][k], kf[k], acc);
-                part[j * G + g] = acc;
-              }
-            }
-          }
-          // reduce-scatter over the LPT lanes of a token row: lane keeps values [(lane%LPT)*VPL, +VPL)
-#pragma unroll
-          for (int step = 0; step < C::LOG_LPT; ++step) {
-            const int msk = (C::LPT >> 1) >> step;
-            const int half = C::NV >> (step + 1);
-            const bool upper = (lane & msk) != 0;
-#pragma unroll
-            for (int k = 0; k < half; ++k) {
-              const float send = upper ? part[k] : part[k + half];
-              const float keep = upper ? part[k + half] : part[k];
-              part[k] = keep + __shfl_xor_sync(0xffffffffu, send, msk);
-            }
-          }
-          float s_own[C::VPL], mr_own[C::VPL];
-          bool over = false;
-#pragma unroll
-          for (int k = 0; k < C::VPL; ++k) {
-            const bool vis = ok_own[k] && tok_own[k] >= tlo && tok_own[k] < thi;
-            s_own[k] = vis ? part[k] : -INFINITY;
-            float mr = -INFINITY;
-#pragma unroll
-            for (int g = 0; g < G; ++g)
-              if (g == g_own[k]) mr = m_run[g];
-            mr_own[k] = mr;
-            over |= vis && (s_own[k] > mr + kRescaleThreshold);
-          }
-          if (__any_sync(0xffffffffu, over)) {
-            // raise the running max of every head to this page's max, rescaling the state accumulated so far
-#pragma unroll
-            for (int k = 0; k < C::VPL; ++k)
-              if (ok_own[k]) wlog[g_own[k] * kPage + tok_own[k]] = s_own[k];
-            __syncwarp();
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-              const float pm = warp_max(lane < kPage ? wlog[g * kPage + lane] : -INFINITY);
-              const float mn = fmaxf(m_run[g], pm);
-              const float a = (m_run[g] == -INFINITY) ? (mn == -INFINITY ? 1.0f : 0.0f) : exp2f(m_run[g] - mn);
-              m_run[g] = mn;
-#pragma unroll
-              for (int k = 0; k < C::EPL; ++k) o[g][k] *= a;
-#pragma unroll
-              for (int k = 0; k < C::VPL; ++k)
-                if (g_own[k] == g) {
-                  l_own[k] *= a;
-                  mr_own[k] = mn;
-                }
-            }
-            __syncwarp();
-          }
-          // probabilities of the owned logits, shared with the warp through wlog[g][token]
-#pragma unroll
-          for (int k = 0; k < C::VPL; ++k) {
-            if (ok_own[k]) {
-              const float pv = (s_own[k] == -INFINITY) ? 0.0f : exp2f(s_own[k] - mr_own[k]);
-              l_own[k] += pv;
-              wlog[g_own[k] * kPage + tok_own[k]] = pv;
-            }
-          }
-          __syncwarp();
-          // ---- o += p v
-          if (thi > tlo) {
-            const uint4 *vvec = reinterpret_cast<const uint4 *>(kb + C::CHUNK);
-            const bool fullpage = (tlo == 0 && thi == kPage);
-#pragma unroll
-            for (int j = 0; j < C::NI; ++j) {
-              const int tok = j * C::TPI + ts;
-              float vf[C::EPL];
-              Vec16<T>::unpack(vvec[j * 32 + lane], vf);
-              if (!fullpage && !(tok >= tlo && tok < thi)) {
-#pragma unroll
-                for (int k = 0; k < C::EPL; ++k) vf[k] = 0.0f;  // invisible slots may hold anything (even NaN)
-              }
-#pragma unroll
-              for (int g = 0; g < G; ++g) {
-                const float pw = wlog[g * kPage + tok];
-#pragma unroll
-                for (int k = 0; k < C::EPL; ++k) o[g][k] = fmaf(pw, vf[k], o[g][k]);
-              }
-            }
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&empty[slot]);
-        }
-
-        // ---- end of the segment: this warp's state into comb[warp], then combine across warps
-        float *cw = comb + warp * (G * D + 2 * G);
-#pragma unroll
-        for (int msk = C::LPT; msk < 32; msk <<= 1)
-#pragma unroll
-          for (int g = 0; g < G; ++g)
-#pragma unroll
-            for (int k = 0; k < C::EPL; ++k) o[g][k] += __shfl_xor_sync(0xffffffffu, o[g][k], msk);
-        if (lane < C::LPT) {
-#pragma unroll
-          for (int g = 0; g < G; ++g)
-#pragma unroll
-            for (int k = 0; k < C::EPL; ++k) cw[g * D + base_dim + k] = o[g][k];
-        }
+        for (int g = 0; g < G; ++g) qraw[g] = *reinterpret_cast<const uint4 *>(qrow + static_cast<size_t>(g) * D);
+        float cs[C::EPL], sn[C::EPL];  // the same angles for every head of the group
+        if (fused) rope_lane_factors<C::EPL, D>(base_dim, P, p.inv_freq, cs, sn);
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          float lsum = 0.0f;
+          float tmp[C::EPL];
+          Vec16<T>::unpack(qraw[g], tmp);
+          if (fused) rope_lane_apply<T, C::EPL, C::LPT, D>(tmp, base_dim, cs, sn);
+#pragma unroll
+          for (int k = 0; k < C::EP2; ++k) {
+            qf[g][k] = make_float2(tmp[2 * k] * qscale, tmp[2 * k + 1] * qscale);
+            o[g][k] = make_float2(0.0f, 0.0f);
+          }
+          m_run[g] = -INFINITY;
+        }
+#pragma unroll
+        for (int k = 0; k < C::VPL; ++k) l_own[k] = 0.0f;
+      }
+      // owned (token, head) pairs after the reduce-scatter: value v = j*G + g is token j*TPI + ts of head g
+      int g_own[C::VPL], tok_own[C::VPL];
+      bool ok_own[C::VPL];
+#pragma unroll
+      for (int k = 0; k < C::VPL; ++k) {
+        const int v = (lane % C::LPT) * C::VPL + k;
+        const int j = v / G;
+        g_own[k] = v - j * G;
+        tok_own[k] = j * C::TPI + ts;
+        ok_own[k] = v < C::NI * G;
+      }
+      for (int64_t e = sg.b + gw; e < sg.e; e += nw) {
+        const int64_t kk = e - cta_begin;
+        const int slot = static_cast<int>(kk % C::SLOTS);
+        wait_entry(&smeta[slot].w, &full[slot], static_cast<int>(kk), static_cast<uint32_t>(kk / C::SLOTS) & 1u,
+                   p.err);
+        const int4 mt = smeta[slot];
+        const int tlo = mt.x & 0xffff, thi = mt.x >> 16;
+        unsigned char *kb = kv + slot * C::SLOT;
+        if (mt.y >= 0) {
+          // the step token of this row lies in this page: RoPE'd key and value into the pool and into this copy
+          const int tok = mt.y;
+          const size_t src = (static_cast<size_t>(r) * p.hkv + h) * D + base_dim;
+          float kx[C::EPL];
+          Vec16<T>::unpack(*reinterpret_cast<const uint4 *>(static_cast<const T *>(p.k_new) + src), kx);
+          const uint4 vw = *reinterpret_cast<const uint4 *>(static_cast<const T *>(p.v_new) + src);
+          float kcs[C::EPL], ksn[C::EPL];
+          rope_lane_factors<C::EPL, D>(base_dim, P, p.inv_freq, kcs, ksn);
+          rope_lane_apply<T, C::EPL, C::LPT, D>(kx, base_dim, kcs, ksn);
+          if (lane < C::LPT) {
+            const uint4 kw = Vec16<T>::pack(kx);
+            const int rowb = (tok * D + base_dim) * C::ESZ;
+            *reinterpret_cast<uint4 *>(kb + rowb) = kw;
+            *reinterpret_cast<uint4 *>(kb + C::CHUNK + rowb) = vw;
+            const size_t dst = ((static_cast<size_t>(mt.z) * p.hkv + h) * kPage + tok) * D + base_dim;
+            *reinterpret_cast<uint4 *>(const_cast<T *>(Kp) + dst) = kw;
+            *reinterpret_cast<uint4 *>(const_cast<T *>(Vp) + dst) = vw;
+            fence_proxy_async_smem();  // the slot is refilled by a bulk copy later
+          }
+          __syncwarp();
+        }
+        // ---- logits of the page's 16 tokens for the G heads
+        float part[C::NV];
+#pragma unroll
+        for (int v = 0; v < C::NV; ++v) part[v] = 0.0f;
+        if (thi > tlo) {
+          const uint4 *kvec = reinterpret_cast<const uint4 *>(kb);
+          uint4 w4[C::NI];
+#pragma unroll
+          for (int j = 0; j < C::NI; ++j) w4[j] = kvec[j * 32 + lane];
+#pragma unroll
+          for (int j = 0; j < C::NI; ++j) {
+            float2 kf[C::EP2];
+            Vec16<T>::unpack2(w4[j], kf);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+              float2 acc = __fmul2_rn(qf[g][0], kf[0]);
+#pragma unroll
+              for (int k = 1; k < C::EP2; ++k) acc = __ffma2_rn(qf[g][k], kf[k], acc);
+              part[j * G + g] = acc.x + acc.y;
+            }
+          }
+        }
+        // reduce-scatter over the LPT lanes of a token row: lane keeps values [(lane%LPT)*VPL, +VPL)
+#pragma unroll
+        for (int step = 0; step < C::LOG_LPT; ++step) {
+          const int msk = (C::LPT >> 1) >> step;
+          const int half = C::NV >> (step + 1);
+          const bool upper = (lane & msk) != 0;
+#pragma unroll
+          for (int k = 0; k < half; ++k) {
+            const float send = upper ? part[k] : part[k + half];
+            const float keep = upper ? part[k + half] : part[k];
+            part[k] = keep + __shfl_xor_sync(0xffffffffu, send, msk);
+          }
+        }
+        float s_own[C::VPL], mr_own[C::VPL];
+        bool over = false;
+#pragma unroll
+        for (int k = 0; k < C::VPL; ++k) {
+          const bool vis = ok_own[k] && tok_own[k] >= tlo && tok_own[k] < thi;
+          s_own[k] = vis ? part[k] : -INFINITY;
+          float mr = -INFINITY;
+#pragma unroll
+          for (int g = 0; g < G; ++g)
+            if (g == g_own[k]) mr = m_run[g];
+          mr_own[k] = mr;
+          over |= vis && (s_own[k] > mr + kRescaleThreshold);
+        }
+        if (__any_sync(0xffffffffu, over)) {
+          // raise the running max of every head to this page's max, rescaling the state accumulated so far
 #pragma unroll
           for (int k = 0; k < C::VPL; ++k)
-            if (ok_own[k] && g_own[k] == g) lsum += l_own[k];
-          lsum = warp_sum(lsum);
-          if (lane == 0) {
-            cw[G * D + g] = m_run[g];
-            cw[G * D + G + g] = lsum;
-          }
-        }
-        consumer_sync();
-        // combine the kNCW warp states: res[0, G*D) output, res[G*D + g] max, res[G*D + G + g] sum
-        const int ctid = tid;  // 0 .. kCT-1
-        if (ctid < G) {
-          float M = -INFINITY;
-          for (int w = 0; w < kNCW; ++w) M = fmaxf(M, comb[w * (G * D + 2 * G) + G * D + ctid]);
-          float L = 0.0f;
-          for (int w = 0; w < kNCW; ++w) {
-            const float mw = comb[w * (G * D + 2 * G) + G * D + ctid];
-            L += (mw == -INFINITY) ? 0.0f : comb[w * (G * D + 2 * G) + G * D + G + ctid] * exp2f(mw - M);
-          }
-          res[G * D + ctid] = M;
-          res[G * D + G + ctid] = L;
-        }
-        consumer_sync();
-        for (int i = ctid; i < G * D; i += kCT) {
-          const int g = i / D;
-          const float M = res[G * D + g];
-          float acc = 0.0f;
-          if (M != -INFINITY) {
+            if (ok_own[k]) wlog[g_own[k] * kPage + tok_own[k]] = s_own[k];
+          __syncwarp();
 #pragma unroll
-            for (int w = 0; w < kNCW; ++w) {
-              const float mw = comb[w * (G * D + 2 * G) + G * D + g];
-              if (mw != -INFINITY) acc = fmaf(comb[w * (G * D + 2 * G) + i], exp2f(mw - M), acc);
+          for (int g = 0; g < G; ++g) {
+            const float pm = warp_max(lane < kPage ? wlog[g * kPage + lane] : -INFINITY);
+            const float mn = fmaxf(m_run[g], pm);
+            const float a = (m_run[g] == -INFINITY) ? (mn == -INFINITY ? 1.0f : 0.0f) : exp2f(m_run[g] - mn);
+            m_run[g] = mn;
+            const float2 a2 = make_float2(a, a);
+#pragma unroll
+            for (int k = 0; k < C::EP2; ++k) o[g][k] = __fmul2_rn(o[g][k], a2);
+#pragma unroll
+            for (int k = 0; k < C::VPL; ++k)
+              if (g_own[k] == g) {
+                l_own[k] *= a;
+                mr_own[k] = mn;
+              }
+          }
+          __syncwarp();
+        }
+        // probabilities of the owned logits, shared with the warp through wlog[g][token]
+#pragma unroll
+        for (int k = 0; k < C::VPL; ++k) {
+          if (ok_own[k]) {
+            const float pv = (s_own[k] == -INFINITY) ? 0.0f : exp2f(s_own[k] - mr_own[k]);
+            l_own[k] += pv;
+            wlog[g_own[k] * kPage + tok_own[k]] = pv;
+          }
+        }
+        __syncwarp();
+        // ---- o += p v
+        if (thi > tlo) {
+          const uint4 *vvec = reinterpret_cast<const uint4 *>(kb + C::CHUNK);
+          const bool fullpage = (tlo == 0 && thi == kPage);
+#pragma unroll
+          for (int j = 0; j < C::NI; ++j) {
+            const int tok = j * C::TPI + ts;
+            float2 vf[C::EP2];
+            Vec16<T>::unpack2(vvec[j * 32 + lane], vf);
+            if (!fullpage && !(tok >= tlo && tok < thi)) {
+#pragma unroll
+              for (int k = 0; k < C::EP2; ++k) vf[k] = make_float2(0.0f, 0.0f);  // invisible slots may hold NaN
+            }
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+              const float pw = wlog[g * kPage + tok];
+              const float2 pw2 = make_float2(pw, pw);
+#pragma unroll
+              for (int k = 0; k < C::EP2; ++k) o[g][k] = __ffma2_rn(pw2, vf[k], o[g][k]);
             }
           }
-          res[i] = acc;
         }
-        consumer_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+      }
 
-        // ---- finish the row, or hand over a partial record (the last CTA to finish the row merges)
-        const int b_first = owner_cta(sg.rb, E, nb), b_last = owner_cta(sg.re - 1, E, nb);
-        const int n_contrib = b_last - b_first + 1;
-        const size_t out_base = (static_cast<size_t>(r) * p.hq + h * G) * D;
-        T *outp = static_cast<T *>(p.out);
-        if (n_contrib == 1) {
-          for (int i = ctid; i < G * D; i += kCT) {
-            const float l = res[G * D + G + i / D];
-            outp[out_base + i] = from_f<T>(l > 0.0f ? res[i] / l : 0.0f);
+      // ---- end of this warp's share of the segment: its state into comb[warp]
+      float *cw = comb + warp * C::REC;
+#pragma unroll
+      for (int msk = C::LPT; msk < 32; msk <<= 1)
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+          for (int k = 0; k < C::EP2; ++k) {
+            o[g][k].x += __shfl_xor_sync(0xffffffffu, o[g][k].x, msk);
+            o[g][k].y += __shfl_xor_sync(0xffffffffu, o[g][k].y, msk);
           }
-          if (ctid < G) {
-            const float l = res[G * D + G + ctid];
-            p.lse[static_cast<size_t>(r) * p.hq + h * G + ctid] =
-                l > 0.0f ? (res[G * D + ctid] + log2f(l)) * kLn2 : -INFINITY;
-            if (!(l > 0.0f)) set_error(p.err, kErrLength);
+      if (lane < C::LPT) {
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+          for (int k = 0; k < C::EP2; ++k) *reinterpret_cast<float2 *>(cw + g * D + base_dim + 2 * k) = o[g][k];
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float lsum = 0.0f;
+#pragma unroll
+        for (int k = 0; k < C::VPL; ++k)
+          if (ok_own[k] && g_own[k] == g) lsum += l_own[k];
+        lsum = warp_sum(lsum);
+        if (lane == 0) {
+          cw[G * D + g] = m_run[g];
+          cw[G * D + G + g] = lsum;
+        }
+      }
+      const int bar_id = kBarSeg0 + si, bar_n = nw * 32;
+      group_sync(bar_id, bar_n);
+
+      // ---- the group combines its warps' states. The group's first warp derives, per head, the max M over the
+      // warps, each warp's weight 2^(m_w - M) and the weighted sum L (lane j = warp j of the group); then every
+      // thread forms its elements' weighted sums with all the group's loads in flight.
+      const int gt = gw * 32 + lane, GT = nw * 32;
+      float *wts = swt_all + si * (G * kNCW + 2 * G);  // [G][kNCW] weights, then M[G], L[G]
+      if (gw == 0) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float *rec = comb + (sg.w0 + lane) * C::REC + G * D;
+          const float mw = lane < nw ? rec[g] : -INFINITY;
+          const float lw = lane < nw ? rec[G + g] : 0.0f;
+          const float M = warp_max(mw);
+          const float wgt = (mw == -INFINITY) ? 0.0f : exp2f(mw - M);
+          const float Ls = warp_sum(lw * wgt);
+          if (lane < kNCW) wts[g * kNCW + lane] = wgt;
+          if (lane == 0) {
+            wts[G * kNCW + g] = M;
+            wts[G * kNCW + G + g] = Ls;
           }
-        } else {
-          const int pslot = static_cast<int>(blockIdx.x) + sg.row;
-          float *pp = p.part + static_cast<size_t>(pslot) * G * D;
-          for (int i = ctid; i < G * D; i += kCT) __stcg(pp + i, res[i]);
-          if (ctid < G) {
-            __stcg(p.ml + (static_cast<size_t>(pslot) * G + ctid) * 2, res[G * D + ctid]);
-            __stcg(p.ml + (static_cast<size_t>(pslot) * G + ctid) * 2 + 1, res[G * D + G + ctid]);
+        }
+      }
+      group_sync(bar_id, bar_n);
+      auto combined = [&](int i, int g) {
+        const float *ci = comb + sg.w0 * C::REC + i;
+        const float *wg = wts + g * kNCW;
+        float acc = 0.0f;
+#pragma unroll
+        for (int j = 0; j < kNCW; ++j)
+          if (j < nw) acc = fmaf(ci[j * C::REC], wg[j], acc);
+        return acc;
+      };
+
+      // ---- finish the row, or hand over a partial record (the last CTA to finish the row merges)
+      const int b_first = owner_cta(sg.rb, E, nb), b_last = owner_cta(sg.re - 1, E, nb);
+      const size_t out_base = (static_cast<size_t>(r) * p.hq + h * G) * D;
+      T *outp = static_cast<T *>(p.out);
+      float *lse_row = p.lse + static_cast<size_t>(r) * p.hq + h * G;
+      if (b_first == b_last) {
+        for (int i = gt; i < G * D; i += GT) {
+          const int g = i / D;
+          const float M = wts[G * kNCW + g], Ls = wts[G * kNCW + G + g];
+          const float acc = combined(i, g);
+          outp[out_base + i] = from_f<T>(Ls > 0.0f ? acc / Ls : 0.0f);
+          if (i - g * D == 0) {
+            lse_row[g] = Ls > 0.0f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+            if (!(Ls > 0.0f)) set_error(p.err, kErrLength);
           }
-          __threadfence();
-          consumer_sync();
-          if (ctid == 0) {
-            const int old = atomicAdd(&p.counters[sg.row], 1);
-            s_flag = (old == n_contrib - 1) ? 1 : 0;
-            if (s_flag) p.counters[sg.row] = 0;  // every contributor has arrived: leave the counter at zero
+        }
+      } else {
+        const size_t pslot = static_cast<size_t>(blockIdx.x) + sg.row;
+        for (int i = gt; i < G * D; i += GT) {
+          const int g = i / D;
+          const float M = wts[G * kNCW + g], Ls = wts[G * kNCW + G + g];
+          __stcg(p.part + pslot * G * D + i, combined(i, g));
+          if (i - g * D == 0) {
+            __stcg(p.ml + (pslot * G + g) * 2, M);
+            __stcg(p.ml + (pslot * G + g) * 2 + 1, Ls);
           }
-          consumer_sync();
-          if (s_flag) {
-            // Last arriver: merge the row's partial records from CTAs b_first..b_last. The (m, l) pairs of up to
-            // 32 contributors are staged in shared memory by one parallel load pass; the partial outputs are loaded
-            // with up to 16 loads in flight per element before any is used.
-            __threadfence();
-            constexpr int kElems = (G * D + kCT - 1) / kCT;
-            float *sm_m = wlog_all;           // [32][G] (every warp is past its pages)
-            float *sm_w = wlog_all + 32 * G;  // [32][G]
-            float *Mg = res + G * D + 2 * G, *Rg = res + G * D + 3 * G, *Lg = res + G * D + G;
-            if (ctid < G) {
-              Mg[ctid] = -INFINITY;
-              Lg[ctid] = 0.0f;
+        }
+        // One thread publishes the group's record and counts it in: the group barrier orders every thread's stores
+        // before its acquire-release atomic, which also makes the other contributors' records visible to the last
+        // arriver (and, through the second barrier, to its whole group).
+        group_sync(bar_id, bar_n);
+        if (gt == 0) {
+          const int old = atom_add_acq_rel_gpu(&p.counters[sg.row], 1);
+          const int last = (old == b_last - b_first) ? 1 : 0;
+          if (last) p.counters[sg.row] = 0;  // every contributor has arrived: leave the counter at zero
+          s_last[si] = last;
+        }
+        group_sync(bar_id, bar_n);
+        if (s_last[si]) {
+          // Last arriver: merge the partial records of CTAs b_first..b_last. A thread takes two of its elements at a
+          // time and loads their records of kMergeChunk contributors at once: one round trip per chunk.
+          for (int i0 = gt; i0 < G * D; i0 += 2 * GT) {
+            int ie[2], ge[2];
+            bool has[2];
+            float M[2], Ls[2], acc[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              ie[e] = i0 + e * GT;
+              has[e] = ie[e] < G * D;
+              ge[e] = has[e] ? ie[e] / D : 0;
+              M[e] = -INFINITY;
+              Ls[e] = 0.0f;
+              acc[e] = 0.0f;
             }
-            float acc[kElems];
+            for (int b0 = b_first; b0 <= b_last; b0 += kMergeChunk) {
+              float mv[2][kMergeChunk], lv[2][kMergeChunk], pv[2][kMergeChunk];
 #pragma unroll
-            for (int k = 0; k < kElems; ++k) acc[k] = 0.0f;
-            const int nc = b_last - b_first + 1;
-            for (int g0 = 0; g0 < nc; g0 += 32) {
-              const int ng = min(32, nc - g0);
-              consumer_sync();
-              for (int q = ctid; q < ng * G; q += kCT) {
-                const int bb = q / G, g = q - (q / G) * G;
-                const size_t o2 = (static_cast<size_t>(b_first + g0 + bb + sg.row) * G + g) * 2;
-                sm_m[bb * G + g] = __ldcg(p.ml + o2);
-                sm_w[bb * G + g] = __ldcg(p.ml + o2 + 1);
-              }
-              consumer_sync();
-              if (ctid < G) {
-                const float Mo = Mg[ctid];
-                float M = Mo;
-                for (int bb = 0; bb < ng; ++bb) M = fmaxf(M, sm_m[bb * G + ctid]);
-                const float resc = (Mo == -INFINITY || M == -INFINITY) ? 0.0f : exp2f(Mo - M);
-                float Ls = Lg[ctid] * resc;
-                for (int bb = 0; bb < ng; ++bb) {
-                  const float mb = sm_m[bb * G + ctid];
-                  const float w = (mb == -INFINITY || M == -INFINITY) ? 0.0f : exp2f(mb - M);
-                  Ls += sm_w[bb * G + ctid] * w;
-                  sm_w[bb * G + ctid] = w;
-                }
-                Mg[ctid] = M;
-                Lg[ctid] = Ls;
-                Rg[ctid] = resc;
-              }
-              consumer_sync();
+              for (int e = 0; e < 2; ++e)
 #pragma unroll
-              for (int k = 0; k < kElems; ++k) {
-                const int i = ctid + k * kCT;
-                if (i < G * D) {
-                  const int g = i / D;
-                  float a = (g0 > 0) ? acc[k] * Rg[g] : 0.0f;
-                  for (int b0 = 0; b0 < ng; b0 += 16) {
-                    float v[16];
-#pragma unroll
-                    for (int bb = 0; bb < 16; ++bb)
-                      v[bb] = (b0 + bb < ng)
-                                  ? __ldcg(p.part + static_cast<size_t>(b_first + g0 + b0 + bb + sg.row) * G * D + i)
-                                  : 0.0f;
-#pragma unroll
-                    for (int bb = 0; bb < 16; ++bb)
-                      if (b0 + bb < ng) a = fmaf(v[bb], sm_w[(b0 + bb) * G + g], a);
+                for (int c = 0; c < kMergeChunk; ++c) {
+                  mv[e][c] = -INFINITY;
+                  lv[e][c] = 0.0f;
+                  pv[e][c] = 0.0f;
+                  if (has[e] && b0 + c <= b_last) {
+                    const size_t ps = static_cast<size_t>(b0 + c) + sg.row;
+                    mv[e][c] = __ldcg(p.ml + (ps * G + ge[e]) * 2);
+                    lv[e][c] = __ldcg(p.ml + (ps * G + ge[e]) * 2 + 1);
+                    pv[e][c] = __ldcg(p.part + ps * G * D + ie[e]);
                   }
-                  acc[k] = a;
+                }
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                float Mc = M[e];
+#pragma unroll
+                for (int c = 0; c < kMergeChunk; ++c) Mc = fmaxf(Mc, mv[e][c]);
+                if (Mc != -INFINITY) {
+                  const float rs = (M[e] == -INFINITY) ? 0.0f : exp2f(M[e] - Mc);
+                  acc[e] *= rs;
+                  Ls[e] *= rs;
+#pragma unroll
+                  for (int c = 0; c < kMergeChunk; ++c) {
+                    const float w = (mv[e][c] == -INFINITY) ? 0.0f : exp2f(mv[e][c] - Mc);
+                    acc[e] = fmaf(pv[e][c], w, acc[e]);
+                    Ls[e] = fmaf(lv[e][c], w, Ls[e]);
+                  }
+                  M[e] = Mc;
                 }
               }
             }
-            consumer_sync();
 #pragma unroll
-            for (int k = 0; k < kElems; ++k) {
-              const int i = ctid + k * kCT;
-              if (i < G * D) {
-                const int g = i / D;
-                const float Ls = Lg[g];
-                outp[out_base + i] = from_f<T>(Ls > 0.0f ? acc[k] / Ls : 0.0f);
-                if ((i % D) == 0) {
-                  p.lse[static_cast<size_t>(r) * p.hq + h * G + g] =
-                      Ls > 0.0f ? (Mg[g] + log2f(Ls)) * kLn2 : -INFINITY;
-                  if (!(Ls > 0.0f)) set_error(p.err, kErrLength);
-                }
+            for (int e = 0; e < 2; ++e) {
+              if (!has[e]) continue;
+              outp[out_base + ie[e]] = from_f<T>(Ls[e] > 0.0f ? acc[e] / Ls[e] : 0.0f);
+              if (ie[e] - ge[e] * D == 0) {
+                lse_row[ge[e]] = Ls[e] > 0.0f ? (M[e] + log2f(Ls[e])) * kLn2 : -INFINITY;
+                if (!(Ls[e] > 0.0f)) set_error(p.err, kErrLength);
               }
             }
           }
         }
-        consumer_sync();
       }
     }
     __syncthreads();
@@ -640,7 +771,7 @@ cudaError_t launch_tdg(const Params &prm, cudaStream_t s) {
   }
   int nb = device_sm_count();
   if (nb > kMaxSlotsExtraCtas) nb = kMaxSlotsExtraCtas;
-  kern<<<nb, kThreads, C::SMEM, s>>>(prm);
+  launch_pdl(kern, dim3(nb), dim3(kThreads), C::SMEM, s, prm);
   return cudaGetLastError();
 }
 
@@ -669,7 +800,8 @@ size_t propose_workspace_bytes(int R, int hkv, int hq, int d) {
 }
 
 cudaError_t launch_propose(const PoolArgs &pa, const MapArgs &ma, const ViewArgs &va, const void *q, void *out,
-                           float *lse, void *ws, size_t ws_bytes, int *err, cudaStream_t s) {
+                           float *lse, void *ws, size_t ws_bytes, const void *k_new, const void *v_new,
+                           const float *inv_freq, int *err, cudaStream_t s) {
   (void)ws_bytes;
   const int G = pa.hq / pa.hkv;
   Params prm;
@@ -699,6 +831,9 @@ cudaError_t launch_propose(const PoolArgs &pa, const MapArgs &ma, const ViewArgs
   w += ((slots * G * 2 * 4 + 255) / 256) * 256;
   prm.part = reinterpret_cast<float *>(w);
   prm.err = err;
+  prm.k_new = k_new;
+  prm.v_new = v_new;
+  prm.inv_freq = inv_freq;
   if (pa.dtype == 0 && pa.d == 128) return launch_td<__nv_bfloat16, 128>(prm, G, s);
   if (pa.dtype == 0 && pa.d == 64) return launch_td<__nv_bfloat16, 64>(prm, G, s);
   if (pa.dtype == 1 && pa.d == 128) return launch_td<float, 128>(prm, G, s);

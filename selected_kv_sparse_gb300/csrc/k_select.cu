@@ -17,6 +17,7 @@ __global__ void __launch_bounds__(128) summaries_kernel(const T *__restrict__ K,
                                                         int num_pages, int hkv, int d,
                                                         const int32_t *__restrict__ bt, int max_pages,
                                                         const int32_t *__restrict__ ctx_len, int *err) {
+  grid_dependency_sync();
   const int r = blockIdx.y, j = blockIdx.x;
   const int L = ctx_len[r];
   const int N = min((L + kPage - 1) / kPage, max_pages);
@@ -50,6 +51,7 @@ __global__ void __launch_bounds__(256) score_kernel(const T *__restrict__ q, con
                                                     int max_pages, const int32_t *__restrict__ ctx_len,
                                                     int per_head, float *__restrict__ scores, int *err) {
   __shared__ float qbar[kMaxPooledHeads][D];
+  grid_dependency_sync();
   const int rows = per_head ? hkv : 1;
   const int row = blockIdx.y;
   const int r = row / rows, v = row - r * rows;
@@ -159,6 +161,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float *__restr
   __shared__ int hist[256];
   __shared__ int scan_scratch[32];
   __shared__ int s_bin, s_remaining;
+  grid_dependency_sync();
   const int row = blockIdx.x;
   const int r = row / rows;
   int a = a_def, rr = r_def, k = k_def;
@@ -274,6 +277,7 @@ __global__ void __launch_bounds__(512) spans_kernel(const int32_t *__restrict__ 
                                                     int *err) {
   extern __shared__ unsigned char keep[];
   __shared__ int scan_scratch[32];
+  grid_dependency_sync();
   const int r = blockIdx.x;
   int a = a_def, rr = r_def, k = 0;
   read_ark(per_seq_ark, r, a, rr, k);
@@ -312,6 +316,7 @@ __global__ void __launch_bounds__(128) view_kernel(const int32_t *__restrict__ b
                                                    int32_t *__restrict__ fallback, float s_max,
                                                    int64_t *__restrict__ slot_out, int32_t *__restrict__ pos_out,
                                                    int *err) {
+  grid_dependency_sync();
   const int row = blockIdx.x;
   const int r = row / rows;
   const int L = ctx_len[r];
@@ -382,6 +387,7 @@ __global__ void __launch_bounds__(128) view_kernel(const int32_t *__restrict__ b
 __global__ void slot_kernel(const int32_t *__restrict__ bt, int max_pages, int R,
                             const int32_t *__restrict__ tok_offsets, const int32_t *__restrict__ start_pos, int T,
                             int64_t *__restrict__ slot_out, int32_t *__restrict__ pos_out) {
+  grid_dependency_sync();
   const int j = blockIdx.x * blockDim.x + threadIdx.x;
   if (j >= T) return;
   int lo = 0, hi = R - 1;  // request r with tok_offsets[r] <= j < tok_offsets[r+1]
@@ -406,11 +412,11 @@ __global__ void slot_kernel(const int32_t *__restrict__ bt, int max_pages, int R
 cudaError_t launch_build_summaries(const PoolArgs &p, const MapArgs &m, int *err, cudaStream_t s) {
   dim3 grid(m.max_pages, m.R);
   if (p.dtype == 0)
-    summaries_kernel<__nv_bfloat16><<<grid, 128, 0, s>>>(static_cast<const __nv_bfloat16 *>(p.k), p.ksum,
-                                                         p.num_pages, p.hkv, p.d, m.bt, m.max_pages, m.ctx_len, err);
+    launch_pdl(summaries_kernel<__nv_bfloat16>, grid, dim3(128), 0, s, static_cast<const __nv_bfloat16 *>(p.k),
+               p.ksum, p.num_pages, p.hkv, p.d, m.bt, m.max_pages, m.ctx_len, err);
   else
-    summaries_kernel<float><<<grid, 128, 0, s>>>(static_cast<const float *>(p.k), p.ksum, p.num_pages, p.hkv, p.d,
-                                                 m.bt, m.max_pages, m.ctx_len, err);
+    launch_pdl(summaries_kernel<float>, grid, dim3(128), 0, s, static_cast<const float *>(p.k), p.ksum, p.num_pages,
+               p.hkv, p.d, m.bt, m.max_pages, m.ctx_len, err);
   return cudaGetLastError();
 }
 
@@ -419,8 +425,8 @@ cudaError_t launch_score(const PoolArgs &p, const MapArgs &m, const void *q, int
   const int rows = per_head ? p.hkv : 1;
   dim3 grid((m.max_pages + kScorePagesPerCta - 1) / kScorePagesPerCta, m.R * rows);
 #define KAP_SCORE(T, D)                                                                                    \
-  score_kernel<T, D><<<grid, 256, 0, s>>>(static_cast<const T *>(q), p.ksum, p.hkv, p.hq, p.num_pages, m.bt, \
-                                          m.max_pages, m.ctx_len, per_head, scores, err)
+  launch_pdl(score_kernel<T, D>, grid, dim3(256), 0, s, static_cast<const T *>(q), p.ksum, p.hkv, p.hq,     \
+             p.num_pages, m.bt, m.max_pages, m.ctx_len, per_head, scores, err)
   if (p.dtype == 0 && p.d == 128) KAP_SCORE(__nv_bfloat16, 128);
   else if (p.dtype == 0 && p.d == 64) KAP_SCORE(__nv_bfloat16, 64);
   else if (p.dtype == 1 && p.d == 128) KAP_SCORE(float, 128);
@@ -437,8 +443,8 @@ cudaError_t launch_topk(const MapArgs &m, const float *scores, int rows, int a, 
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  topk_kernel<<<m.R * rows, kTopkThreads, smem, s>>>(scores, rows, m.ctx_len, m.max_pages, a, r, k, per_seq_ark,
-                                                       cap, sel, n_sel, err);
+  launch_pdl(topk_kernel, dim3(m.R * rows), dim3(kTopkThreads), smem, s, scores, rows, m.ctx_len, m.max_pages, a, r,
+             k, per_seq_ark, cap, sel, n_sel, err);
   return cudaGetLastError();
 }
 
@@ -451,7 +457,8 @@ cudaError_t launch_select_spans(const MapArgs &m, const int32_t *spans, const in
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  spans_kernel<<<m.R, 512, smem, s>>>(m.ctx_len, m.max_pages, spans, span_offsets, a, r, per_seq_ark, cap, sel, n_sel, err);
+  launch_pdl(spans_kernel, dim3(m.R), dim3(512), smem, s, m.ctx_len, m.max_pages, spans, span_offsets, a, r,
+             per_seq_ark, cap, sel, n_sel, err);
   return cudaGetLastError();
 }
 
@@ -459,15 +466,16 @@ cudaError_t launch_compile_view(const MapArgs &m, const int32_t *sel, const int3
                                 int horizon, int32_t *vbt, int32_t *vlp, int32_t *vn, int32_t *vnsel, int vcap,
                                 int32_t *fallback, float s_max, int64_t *slot_out, int32_t *pos_out, int *err,
                                 cudaStream_t s) {
-  view_kernel<<<m.R * rows, 128, 0, s>>>(m.bt, m.max_pages, m.ctx_len, m.seq_len, sel, n_sel, rows, sel_cap,
-                                         horizon, vbt, vlp, vn, vnsel, vcap, fallback, s_max, slot_out, pos_out, err);
+  launch_pdl(view_kernel, dim3(m.R * rows), dim3(128), 0, s, m.bt, m.max_pages, m.ctx_len, m.seq_len, sel, n_sel,
+             rows, sel_cap, horizon, vbt, vlp, vn, vnsel, vcap, fallback, s_max, slot_out, pos_out, err);
   return cudaGetLastError();
 }
 
 cudaError_t launch_slot_mapping(const MapArgs &m, const int32_t *tok_offsets, const int32_t *start_pos, int T,
                                 int64_t *slot_out, int32_t *pos_out, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
-  slot_kernel<<<(T + 255) / 256, 256, 0, s>>>(m.bt, m.max_pages, m.R, tok_offsets, start_pos, T, slot_out, pos_out);
+  launch_pdl(slot_kernel, dim3((T + 255) / 256), dim3(256), 0, s, m.bt, m.max_pages, m.R, tok_offsets, start_pos, T,
+             slot_out, pos_out);
   return cudaGetLastError();
 }
 

@@ -154,6 +154,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = p.hq / p.hkv;
+  grid_dependency_sync();
 
   if (warp == 0) {
     int64_t tot = 0;
@@ -734,6 +735,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 template <class T, int D>
 __global__ void __launch_bounds__(256) verify_ffma_kernel(const T *__restrict__ K, const T *__restrict__ V,
                                                           const VParams p, int total_q) {
+  grid_dependency_sync();
   const int64_t wid = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (wid >= static_cast<int64_t>(total_q) * p.hq) return;
@@ -831,7 +833,7 @@ cudaError_t launch_tc(const PoolArgs &pa, const VParams &prm, cudaStream_t s) {
     attr_set[dev & 63] = true;
   }
   const int nb = device_sm_count();
-  verify_tc_kernel<NPMAX><<<nb, kTcThreads, L::ALLOC, s>>>(tmK, tmV, prm);
+  launch_pdl(verify_tc_kernel<NPMAX>, dim3(nb), dim3(kTcThreads), L::ALLOC, s, tmK, tmV, prm);
   return cudaGetLastError();
 }
 
@@ -890,14 +892,14 @@ cudaError_t launch_verify(const PoolArgs &pa, const MapArgs &ma, int max_q, int 
   const int64_t warps = static_cast<int64_t>(total_q) * pa.hq;
   const int blocks = static_cast<int>((warps + 7) / 8);
   if (pa.dtype == 0)
-    verify_ffma_kernel<__nv_bfloat16, 64><<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(pa.k),
-                                                                  static_cast<const __nv_bfloat16 *>(pa.v), prm, total_q);
+    launch_pdl(verify_ffma_kernel<__nv_bfloat16, 64>, dim3(blocks), dim3(256), 0, s,
+               static_cast<const __nv_bfloat16 *>(pa.k), static_cast<const __nv_bfloat16 *>(pa.v), prm, total_q);
   else if (pa.d == 128)
-    verify_ffma_kernel<float, 128><<<blocks, 256, 0, s>>>(static_cast<const float *>(pa.k),
-                                                          static_cast<const float *>(pa.v), prm, total_q);
+    launch_pdl(verify_ffma_kernel<float, 128>, dim3(blocks), dim3(256), 0, s, static_cast<const float *>(pa.k),
+               static_cast<const float *>(pa.v), prm, total_q);
   else
-    verify_ffma_kernel<float, 64><<<blocks, 256, 0, s>>>(static_cast<const float *>(pa.k),
-                                                         static_cast<const float *>(pa.v), prm, total_q);
+    launch_pdl(verify_ffma_kernel<float, 64>, dim3(blocks), dim3(256), 0, s, static_cast<const float *>(pa.k),
+               static_cast<const float *>(pa.v), prm, total_q);
   return cudaGetLastError();
 }
 

@@ -208,8 +208,10 @@ size_t kap_propose_workspace_size(int32_t num_seqs, int32_t num_kv_heads, int32_
   return propose_workspace_bytes(num_seqs, num_kv_heads, num_q_heads, head_dim);
 }
 
-kap_status kap_attn_propose(const kap_kv_pool *pool, const kap_page_map *map, const kap_view *view, const void *q_dev,
-                            void *out, float *lse, void *workspace, size_t workspace_bytes, kap_stream stream) {
+namespace {
+kap_status propose_common(const kap_kv_pool *pool, const kap_page_map *map, const kap_view *view, const void *q_dev,
+                          void *out, float *lse, void *workspace, size_t workspace_bytes, const void *k_new,
+                          const void *v_new, const float *inv_freq_dev, kap_stream stream) {
   kap_status st = check_pool(pool, false);
   if (st != KAP_OK) return st;
   if ((st = check_map(map, true)) != KAP_OK) return st;
@@ -218,6 +220,7 @@ kap_status kap_attn_propose(const kap_kv_pool *pool, const kap_page_map *map, co
   if (view->cap <= 0) return KAP_EINVAL;
   if (view->rows_per_seq != 1 && view->rows_per_seq != pool->num_kv_heads) return KAP_ESHAPE;
   if (!aligned16(q_dev) || !aligned16(out)) return KAP_EINVAL;
+  if (k_new && (!aligned16(k_new) || !aligned16(v_new) || !aligned16(inv_freq_dev))) return KAP_EINVAL;
   const int G = pool->num_q_heads / pool->num_kv_heads;
   if (!(G == 1 || G == 2 || G == 4 || G == 5 || G == 8)) return KAP_EUNSUPPORTED;
   if (workspace_bytes <
@@ -231,7 +234,22 @@ kap_status kap_attn_propose(const kap_kv_pool *pool, const kap_page_map *map, co
   va.n_entries = view->n_entries;
   va.n_selected = view->n_selected;
   return cuda_status(launch_propose(pool_args(pool), map_args(map), va, q_dev, out, lse, workspace, workspace_bytes,
-                                    error_word(), cs(stream)));
+                                    k_new, v_new, inv_freq_dev, error_word(), cs(stream)));
+}
+}  // namespace
+
+kap_status kap_attn_propose(const kap_kv_pool *pool, const kap_page_map *map, const kap_view *view, const void *q_dev,
+                            void *out, float *lse, void *workspace, size_t workspace_bytes, kap_stream stream) {
+  return propose_common(pool, map, view, q_dev, out, lse, workspace, workspace_bytes, nullptr, nullptr, nullptr,
+                        stream);
+}
+
+kap_status kap_append_propose(const kap_kv_pool *pool, const kap_page_map *map, const kap_view *view,
+                              const void *q_dev, const void *k_new, const void *v_new, const float *inv_freq_dev,
+                              void *out, float *lse, void *workspace, size_t workspace_bytes, kap_stream stream) {
+  if (!k_new || !v_new || !inv_freq_dev) return KAP_EINVAL;
+  return propose_common(pool, map, view, q_dev, out, lse, workspace, workspace_bytes, k_new, v_new, inv_freq_dev,
+                        stream);
 }
 
 size_t kap_verify_workspace_size(int32_t num_seqs, int32_t num_kv_heads, int32_t num_q_heads, int32_t head_dim,

@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace kap {
 
 constexpr int kPage = 16;
@@ -19,6 +21,31 @@ constexpr int kErrTimeout = 8;   // a bounded wait ran out; the kernel skipped t
 
 __device__ __forceinline__ void set_error(int *err, int bit) {
   if (err) atomicOr(err, bit);
+}
+
+// ------------------------------------------------------------------------------- dependent launches
+// Every kernel of the library is launched with programmatic stream serialization: its CTAs may start while the
+// previous kernel in the stream drains. Each kernel therefore lets its own dependent start early and then waits,
+// before its first global memory access, until the previous kernel has completed and its writes are visible.
+__device__ __forceinline__ void grid_dependency_sync() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+template <class... KArgs, class... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // ------------------------------------------------------------------------------------------ conversions
@@ -40,6 +67,22 @@ template <> struct Vec16<__nv_bfloat16> {
       o[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
     }
   }
+  // fp32 pairs (element 2i, 2i+1) of one 16-byte vector
+  __device__ __forceinline__ static void unpack2(const uint4 &w, float2 *o) {
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[i] = make_float2(__uint_as_float(u[i] << 16), __uint_as_float(u[i] & 0xffff0000u));
+  }
+  // 8 values rounded to nearest into one 16-byte vector
+  __device__ __forceinline__ static uint4 pack(const float *v) {
+    uint32_t u[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+      u[i] = *reinterpret_cast<const uint32_t *>(&b);
+    }
+    return make_uint4(u[0], u[1], u[2], u[3]);
+  }
 };
 template <> struct Vec16<float> {
   static constexpr int N = 4;
@@ -49,7 +92,29 @@ template <> struct Vec16<float> {
     o[2] = __uint_as_float(w.z);
     o[3] = __uint_as_float(w.w);
   }
+  __device__ __forceinline__ static void unpack2(const uint4 &w, float2 *o) {
+    o[0] = make_float2(__uint_as_float(w.x), __uint_as_float(w.y));
+    o[1] = make_float2(__uint_as_float(w.z), __uint_as_float(w.w));
+  }
+  __device__ __forceinline__ static uint4 pack(const float *v) {
+    return make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]), __float_as_uint(v[3]));
+  }
 };
+
+// Rotary embedding of one (i, i + d/2) pair at logical position pos: angle = (float)pos * inv_freq_i in fp32,
+// x' = x cos - y sin, y' = x sin + y cos, with the multiply-adds written out so that every kernel rounds alike.
+__device__ __forceinline__ void rope_factors(int pos, float inv_freq_i, float &cs, float &sn) {
+  sincosf(static_cast<float>(pos) * inv_freq_i, &sn, &cs);
+}
+__device__ __forceinline__ void rope_rotate(float x, float y, float cs, float sn, float &xr, float &yr) {
+  xr = fmaf(x, cs, -(y * sn));
+  yr = fmaf(x, sn, y * cs);
+}
+__device__ __forceinline__ void rope_pair(float x, float y, int pos, float inv_freq_i, float &xr, float &yr) {
+  float cs, sn;
+  rope_factors(pos, inv_freq_i, cs, sn);
+  rope_rotate(x, y, cs, sn, xr, yr);
+}
 
 // Monotone key of a float score: larger score -> larger key; -0 == +0; NaN below every number.
 __device__ __forceinline__ uint32_t order_key(float f) {

@@ -46,8 +46,10 @@ cudaError_t launch_append(const PoolArgs &p, const void *k_new, const void *v_ne
 
 // proposal attention (k_propose.cu)
 size_t propose_workspace_bytes(int R, int hkv, int hq, int d);
+// k_new/v_new/inv_freq non-null: fused append of the step token at seq_len-1 (q is then taken before RoPE)
 cudaError_t launch_propose(const PoolArgs &p, const MapArgs &m, const ViewArgs &v, const void *q, void *out,
-                           float *lse, void *ws, size_t ws_bytes, int *err, cudaStream_t s);
+                           float *lse, void *ws, size_t ws_bytes, const void *k_new, const void *v_new,
+                           const float *inv_freq, int *err, cudaStream_t s);
 
 // verification attention (k_verify.cu)
 size_t verify_workspace_bytes(int R, int hkv, int hq, int d, int max_q);

@@ -2,9 +2,10 @@
 
 KAP paper, executor and verifier: the plan (selection, compact view, slot mapping) is compiled once per cycle;
 each of the k proposal steps appends the step's token KV (RoPE at its logical position) and runs q = 1 attention
-over the compact view; the verifier appends the window's KV into the full-context slots and runs causal q = n
-attention over the full block table. Every buffer is allocated here, once; the calls themselves allocate nothing,
-so a cycle can be captured in a CUDA graph.
+over the compact view, in one fused call (kap_append_propose) or as kap_append_kv + kap_attn_propose; the verifier
+appends the window's KV into the full-context slots and runs causal q = n attention over the full block table.
+Every buffer is allocated here, once; the calls themselves allocate nothing, so a cycle can be captured in a CUDA
+graph.
 """
 from __future__ import annotations
 
@@ -21,8 +22,9 @@ class DecodeCycle:
     def __init__(self, pool: kb.KVPool, block_table: torch.Tensor, ctx_len: torch.Tensor, seq_len0: torch.Tensor,
                  k_prop: int, n_q: torch.Tensor, inv_freq: torch.Tensor, policy: Optional[kb.AccessPolicy] = None,
                  spans: Optional[torch.Tensor] = None, span_offsets: Optional[torch.Tensor] = None,
-                 sel_cap: Optional[int] = None, s_max: float = 1.0):
+                 sel_cap: Optional[int] = None, s_max: float = 1.0, fused: bool = True):
         dev = block_table.device
+        self.fused = bool(fused)
         self.pool = pool
         self.R = int(block_table.shape[0])
         self.Hq = pool.num_q_heads
@@ -105,8 +107,14 @@ class DecodeCycle:
                             stream)
 
     def propose_step(self, i: int, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
-        self.append_step(i, q, k_new, v_new, stream)
-        self.propose(i, q, stream)
+        """Proposal step i: append the step token's KV and attend. Fused, q is read before RoPE and left as it is;
+        unfused, kap_append_kv rotates q in place first."""
+        if self.fused:
+            kb.kap_append_propose(self.pool, self.map_steps[i], self.view, q, k_new, v_new, self.inv_freq,
+                                  self.o_prop[i], self.lse_prop[i], self.ws_prop, stream)
+        else:
+            self.append_step(i, q, k_new, v_new, stream)
+            self.propose(i, q, stream)
 
     def append_window(self, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
         """The verify window's KV into the full-context slots (q rotated in place)."""
@@ -126,8 +134,9 @@ class DecodeCycle:
 
     def launches_per_cycle(self) -> int:
         """Kernel launches of one run(): selection (score + top-K, or spans), the view (with the horizon's slot
-        mapping), a separate window slot mapping when the windows differ from the horizon, an append and a
-        proposal kernel per step, then the window append and verification."""
+        mapping), a separate window slot mapping when the windows differ from the horizon, per step one fused
+        kernel (or an append and a proposal kernel), then the window append and verification."""
         sel = 1 if self.spans is not None else 2
         slots = 0 if self.window_is_horizon else 1
-        return sel + 1 + slots + 2 * self.k_prop + 2
+        per_step = 1 if self.fused else 2
+        return sel + 1 + slots + per_step * self.k_prop + 2

@@ -32,12 +32,12 @@ def policy_of(w, cap=None):
     return kap.AccessPolicy(a, r, k, w.per_kv_head, cap, None if same else w.ark.contiguous())
 
 
-def make_cycle(w, cap=None):
+def make_cycle(w, cap=None, fused=True):
     pool = kap.KVPool(w.K, w.V, w.Hq, torch.zeros(w.num_pages, w.Hkv, w.d, dtype=torch.float32, device=w.K.device))
     inv = kap.rope_inv_freq(w.d, w.theta, w.K.device)
     pol = policy_of(w, cap)
     cyc = kap.DecodeCycle(pool, w.block_table, w.ctx_len, w.seq_len0, w.k_prop, w.n_q, inv, policy=pol,
-                          spans=w.spans, span_offsets=w.span_offsets, sel_cap=pol.cap)
+                          spans=w.spans, span_offsets=w.span_offsets, sel_cap=pol.cap, fused=fused)
     return pool, cyc
 
 
@@ -72,15 +72,16 @@ def oracle_selection(w, S_np, q_route_np):
     return sel, nsel
 
 
-def run_cycle_and_oracle(w, check_rows=None, nthreads=8):
-    """Runs one full cycle on the GPU and the oracle on identical inputs.
+def run_cycle_and_oracle(w, check_rows=None, nthreads=8, fused=True):
+    """Runs one full cycle on the GPU and the oracle on identical inputs (proposal steps fused with their KV append,
+    or as separate append and proposal calls).
 
     Returns a dict with GPU and oracle results for selection, view, proposal (every step) and verify.
     The oracle sees the pool exactly as the GPU kernels saw it at each point: proposal step i sees the proposal
     tokens 0..i appended (RoPE'd by the oracle itself), verify sees the window tokens appended.
     """
     dev = w.K.device
-    pool, cyc = make_cycle(w)
+    pool, cyc = make_cycle(w, fused=fused)
     kap.kap_build_summaries(pool, kap.PageMap(w.block_table, w.ctx_len, w.seq_len0))
     # snapshot inputs before the cycle mutates them (q is rotated in place, the pool receives new tokens)
     K0, V0 = f32(w.K), f32(w.V)
@@ -116,7 +117,7 @@ def run_cycle_and_oracle(w, check_rows=None, nthreads=8):
             torch.from_numpy(qrot).to(torch.bfloat16).float().numpy()
         out, lse = oracle.attn_propose(qin, K, V, bt, ctx, seq0 + i + 1, sel, nsel, nthreads=nthreads)
         res["prop"].append(dict(o_orc=out, lse_orc=lse, o_gpu=f32(cyc.o_prop[i]), lse_gpu=f32(cyc.lse_prop[i]),
-                                q_gpu=f32(q_prop[i]), q_orc=qrot))
+                                q_gpu=None if fused else f32(q_prop[i]), q_orc=qrot))
     # verify: window tokens appended at seq0 .. seq0 + n_q - 1 (overwriting proposal slots)
     qo = i32(w.q_offsets)
     kv_, vv_ = f32(w.k_new_ver), f32(w.v_new_ver)
