@@ -4,9 +4,10 @@
 One step = one proposal/verification cycle of the whole hot path over `--layers` independent attention layers
 (replicas with their own KV pools), on the Llama-3-8B-shaped workload: 4 requests x 32768-token prompts, Hq=32,
 Hkv=8, d=128, bf16 KV, per-KV-head K-summary scoring with A1R2K125 selection (s = 6.25%), 4 proposal steps (q=1)
-and a verify window of 4 (causal). Per layer and cycle: score + top-K, view compilation (which also writes the slot
-mapping of the cycle's new tokens), then 4 proposal steps, each one kernel that appends the step token's KV and
-attends over the view (--unfused: a KV-append kernel and a proposal kernel), then window append + verification.
+and a verify window of 4 (causal). Per layer and cycle: scoring, then top-K with the view compilation (and the slot
+mapping of the cycle's new tokens) in the same kernel, then 4 proposal steps, each one kernel that appends the step
+token's KV and attends over the view, then window append + verification. --unfused runs the separate calls: score,
+top-K, view; a KV-append kernel and a proposal kernel per step.
 
 Output: one JSON line (rank 0). `value` is the algorithmic HBM bytes of every hot-path kernel in a step divided by
 the device time of the step (GB/s, whole job); the phase times come from CUDA events recorded between CUDA-graph

@@ -124,6 +124,17 @@ kap_status kap_score_topk(const kap_kv_pool *pool, const kap_page_map *map, cons
                           void *workspace, size_t workspace_bytes, kap_stream stream);
 size_t kap_score_workspace_size(int32_t num_seqs, int32_t rows_per_seq, int32_t max_pages);
 
+/* Page scoring, A/R/K top-K and view compilation in one call: the same outputs as kap_score_topk followed by
+ * kap_compile_view(map, sel_ids, n_sel, rows, policy->cap, horizon_tokens, view, fallback_dev, s_max, slot_out,
+ * pos_out), where rows = Hkv (per_kv_head) or 1. The top-K kernel compiles each row's view right after selecting
+ * it, which saves the view kernel's launch and its reload of the selection. Needs map->seq_len; view->rows_per_seq
+ * must equal rows and view->cap >= policy->cap + ceil(horizon_tokens/16) + 1. */
+kap_status kap_score_topk_view(const kap_kv_pool *pool, const kap_page_map *map, const void *q_dev,
+                               const kap_access_policy *policy, int32_t *sel_ids, int32_t *n_sel, void *workspace,
+                               size_t workspace_bytes, int32_t horizon_tokens, const kap_view *view,
+                               int32_t *fallback_dev, float s_max, int64_t *slot_out, int32_t *pos_out,
+                               kap_stream stream);
+
 /* Span selection. KAP paper, compiler stage 3 (selected spans resolved to KV pages): a prompt page is kept when
  * any token of a selected span falls in it; pinned anchor/recent pages (policy a, r) are added. One row per
  * request (shared by all heads).

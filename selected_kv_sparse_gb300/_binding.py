@@ -67,6 +67,7 @@ def _declare(lib):
         "kap_build_summaries": ([P, P, P], I),
         "kap_score_topk": ([P, P, P, P, P, P, P, Z, P], I),
         "kap_score_workspace_size": ([I, I, I], Z),
+        "kap_score_topk_view": ([P, P, P, P, P, P, P, Z, I, P, P, F, P, P, P], I),
         "kap_select_spans": ([P, P, P, P, P, P, P], I),
         "kap_compile_view": ([P, P, P, I, I, I, P, P, F, P, P, P], I),
         "kap_slot_mapping": ([P, P, P, I, P, P, P], I),
@@ -254,6 +255,26 @@ def kap_score_topk(pool: KVPool, pmap: PageMap, q: torch.Tensor, policy: AccessP
     _check("kap_score_topk", lib.kap_score_topk(ctypes.byref(p), ctypes.byref(m), _ptr(q), ctypes.byref(pol),
                                                 _i32(sel_ids, "sel_ids"), _i32(n_sel, "n_sel"), _ptr(workspace),
                                                 workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def kap_score_topk_view(pool: KVPool, pmap: PageMap, q: torch.Tensor, policy: AccessPolicy, sel_ids: torch.Tensor,
+                        n_sel: torch.Tensor, workspace: torch.Tensor, horizon_tokens: int, view: View,
+                        fallback: Optional[torch.Tensor] = None, s_max: float = 1.0,
+                        slot_out: Optional[torch.Tensor] = None, pos_out: Optional[torch.Tensor] = None,
+                        stream=None):
+    """kap_score_topk and kap_compile_view in one call (the top-K kernel compiles each row's view)."""
+    lib = load()
+    if q.dtype != pool.dtype:
+        raise TypeError("q must have the pool dtype")
+    if slot_out is not None and (slot_out.dtype != torch.int64 or slot_out.numel() < pmap.block_table.shape[0] *
+                                 horizon_tokens):
+        raise ValueError("slot_out must be int64 with R * horizon_tokens elements")
+    p, m, pol, v = pool._c(), pmap._c(), policy._c(), view._c()
+    _check("kap_score_topk_view", lib.kap_score_topk_view(
+        ctypes.byref(p), ctypes.byref(m), _ptr(q), ctypes.byref(pol), _i32(sel_ids, "sel_ids"), _i32(n_sel, "n_sel"),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), horizon_tokens, ctypes.byref(v),
+        _i32(fallback, "fallback") if fallback is not None else None, float(s_max), _ptr(slot_out),
+        _i32(pos_out, "pos_out") if pos_out is not None else None, _stream(stream)))
 
 
 def kap_select_spans(pmap: PageMap, spans: torch.Tensor, span_offsets: torch.Tensor, policy: AccessPolicy,

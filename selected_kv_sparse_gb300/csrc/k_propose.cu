@@ -56,9 +56,14 @@ struct Cfg {
   static constexpr int VPL = NV / LPT;           // finished logits owned by each lane
   static constexpr int LOG_LPT = LPT == 8 ? 3 : (LPT == 16 ? 4 : 5);
   static constexpr int REC = G * D + 2 * G;      // floats of one warp's state record (o, m, l)
+  // Select-free reduce-scatter: when the NI*G partial values are a power of two (G a power of two) and at least LPT,
+  // a lane keeps logical value v in register v ^ PERM(lane), so every butterfly level sends the upper half of the
+  // registers and keeps the lower half. The lane loads token row j ^ PJ(lane) and query head g ^ PG(lane) for it.
+  static constexpr bool XPERM = (G & (G - 1)) == 0 && NI * G >= LPT;
+  static constexpr int LOG_G = G == 1 ? 0 : (G == 2 ? 1 : (G == 4 ? 2 : 3));
   // shared memory carve-up (bytes)
   static constexpr int COMB = kNCW * REC * 4;             // per-warp state records
-  static constexpr int WLOG = kNCW * G * kPage * 4;       // per-warp logits / probabilities of one page
+  static constexpr int WLOG = kNCW * G * kPage * 8;       // per-warp logits, or probability pairs, of one page
   static constexpr int SWT = kMaxSeg * G * (kNCW + 2) * 4;  // per segment: warp weights, max and sum per head
   static constexpr int SEGB = kMaxSeg * 48;               // segment table
   static constexpr int ROWB = (kMaxRowsScan + 1) * 4;     // per-row entry offsets (row scan)
@@ -188,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char *kv = smem + C::OFF_KV;
   float *comb = reinterpret_cast<float *>(smem + C::OFF_COMB);      // [kNCW][REC]
-  float *wlog_all = reinterpret_cast<float *>(smem + C::OFF_WLOG);  // [kNCW][G][16]
+  float *wlog_all = reinterpret_cast<float *>(smem + C::OFF_WLOG);  // [kNCW][16][G] float2 (or [G][16] float)
   float *swt_all = reinterpret_cast<float *>(smem + C::OFF_SWT);    // [kMaxSeg][G * kNCW + 2G]
   Seg *segs = reinterpret_cast<Seg *>(smem + C::OFF_SEG);
   int4 *smeta = reinterpret_cast<int4 *>(smem + C::OFF_SMETA);
@@ -407,15 +412,18 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
       const Seg sg = segs[si];
       const int gw = warp - sg.w0, nw = sg.nw;
       const int r = sg.row / p.hkv, h = sg.row - r * p.hkv;
-      float *wlog = wlog_all + warp * G * kPage;
+      float *wlog = wlog_all + warp * G * kPage * 2;  // logits [g][token] for a rescale, then (p, p) [token][g]
+      float2 *wpair = reinterpret_cast<float2 *>(wlog);
       float2 qf[G][C::EP2], o[G][C::EP2];
       float m_run[G], l_own[C::VPL];
       const int P = fused ? p.seq_len[r] - 1 : 0;  // position of the step token (fused append)
       {
         const T *qrow = static_cast<const T *>(p.q) + (static_cast<size_t>(r) * p.hq + h * G) * D + base_dim;
         uint4 qraw[G];
+        const int pg = C::XPERM ? (((lane % C::LPT) * C::VPL) & (G - 1)) : 0;  // register g holds head g ^ pg
 #pragma unroll
-        for (int g = 0; g < G; ++g) qraw[g] = *reinterpret_cast<const uint4 *>(qrow + static_cast<size_t>(g) * D);
+        for (int g = 0; g < G; ++g)
+          qraw[g] = *reinterpret_cast<const uint4 *>(qrow + static_cast<size_t>(g ^ pg) * D);
         float cs[C::EPL], sn[C::EPL];  // the same angles for every head of the group
         if (fused) rope_lane_factors<C::EPL, D>(base_dim, P, p.inv_freq, cs, sn);
 #pragma unroll
@@ -481,8 +489,9 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
         if (thi > tlo) {
           const uint4 *kvec = reinterpret_cast<const uint4 *>(kb);
           uint4 w4[C::NI];
+          const int pj = C::XPERM ? (((lane % C::LPT) * C::VPL) >> C::LOG_G) : 0;  // register j: row j ^ pj
 #pragma unroll
-          for (int j = 0; j < C::NI; ++j) w4[j] = kvec[j * 32 + lane];
+          for (int j = 0; j < C::NI; ++j) w4[j] = kvec[(j ^ pj) * 32 + lane];
 #pragma unroll
           for (int j = 0; j < C::NI; ++j) {
             float2 kf[C::EP2];
@@ -504,9 +513,13 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
           const bool upper = (lane & msk) != 0;
 #pragma unroll
           for (int k = 0; k < half; ++k) {
-            const float send = upper ? part[k] : part[k + half];
-            const float keep = upper ? part[k + half] : part[k];
-            part[k] = keep + __shfl_xor_sync(0xffffffffu, send, msk);
+            if (C::XPERM) {
+              part[k] += __shfl_xor_sync(0xffffffffu, part[k + half], msk);
+            } else {
+              const float send = upper ? part[k] : part[k + half];
+              const float keep = upper ? part[k + half] : part[k];
+              part[k] = keep + __shfl_xor_sync(0xffffffffu, send, msk);
+            }
           }
         }
         float s_own[C::VPL], mr_own[C::VPL];
@@ -546,13 +559,13 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
           }
           __syncwarp();
         }
-        // probabilities of the owned logits, shared with the warp through wlog[g][token]
+        // probabilities of the owned logits, shared with the warp as (p, p) pairs in wpair[token][g]
 #pragma unroll
         for (int k = 0; k < C::VPL; ++k) {
           if (ok_own[k]) {
             const float pv = (s_own[k] == -INFINITY) ? 0.0f : exp2f(s_own[k] - mr_own[k]);
             l_own[k] += pv;
-            wlog[g_own[k] * kPage + tok_own[k]] = pv;
+            wpair[tok_own[k] * G + g_own[k]] = make_float2(pv, pv);
           }
         }
         __syncwarp();
@@ -569,13 +582,23 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
 #pragma unroll
               for (int k = 0; k < C::EP2; ++k) vf[k] = make_float2(0.0f, 0.0f);  // invisible slots may hold NaN
             }
+            float2 pw2[G];
+            if (G % 2 == 0) {
+              const float4 *p4 = reinterpret_cast<const float4 *>(wpair + tok * G);
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-              const float pw = wlog[g * kPage + tok];
-              const float2 pw2 = make_float2(pw, pw);
+              for (int g = 0; g < G; g += 2) {
+                const float4 t = p4[g / 2];
+                pw2[g] = make_float2(t.x, t.y);
+                pw2[g + 1 < G ? g + 1 : g] = make_float2(t.z, t.w);
+              }
+            } else {
 #pragma unroll
-              for (int k = 0; k < C::EP2; ++k) o[g][k] = __ffma2_rn(pw2, vf[k], o[g][k]);
+              for (int g = 0; g < G; ++g) pw2[g] = wpair[tok * G + g];
             }
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+#pragma unroll
+              for (int k = 0; k < C::EP2; ++k) o[g][k] = __ffma2_rn(pw2[g], vf[k], o[g][k]);
           }
         }
         __syncwarp();
@@ -669,8 +692,7 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
           const float M = wts[G * kNCW + g], Ls = wts[G * kNCW + G + g];
           __stcg(p.part + pslot * G * D + i, combined(i, g));
           if (i - g * D == 0) {
-            __stcg(p.ml + (pslot * G + g) * 2, M);
-            __stcg(p.ml + (pslot * G + g) * 2 + 1, Ls);
+            __stcg(reinterpret_cast<float2 *>(p.ml) + pslot * G + g, make_float2(M, Ls));
           }
         }
         // One thread publishes the group's record and counts it in: the group barrier orders every thread's stores
@@ -695,7 +717,8 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
             for (int e = 0; e < 2; ++e) {
               ie[e] = i0 + e * GT;
               has[e] = ie[e] < G * D;
-              ge[e] = has[e] ? ie[e] / D : 0;
+              if (!has[e]) ie[e] = i0;  // a valid address: every load below is issued unconditionally
+              ge[e] = ie[e] / D;
               M[e] = -INFINITY;
               Ls[e] = 0.0f;
               acc[e] = 0.0f;
@@ -706,16 +729,21 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
               for (int e = 0; e < 2; ++e)
 #pragma unroll
                 for (int c = 0; c < kMergeChunk; ++c) {
-                  mv[e][c] = -INFINITY;
-                  lv[e][c] = 0.0f;
-                  pv[e][c] = 0.0f;
-                  if (has[e] && b0 + c <= b_last) {
-                    const size_t ps = static_cast<size_t>(b0 + c) + sg.row;
-                    mv[e][c] = __ldcg(p.ml + (ps * G + ge[e]) * 2);
-                    lv[e][c] = __ldcg(p.ml + (ps * G + ge[e]) * 2 + 1);
-                    pv[e][c] = __ldcg(p.part + ps * G * D + ie[e]);
-                  }
+                  const size_t ps = static_cast<size_t>(min(b0 + c, b_last)) + sg.row;  // clamped: always valid
+                  const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.ml) + ps * G + ge[e]);
+                  mv[e][c] = ml.x;
+                  lv[e][c] = ml.y;
+                  pv[e][c] = __ldcg(p.part + ps * G * D + ie[e]);
                 }
+#pragma unroll
+              for (int e = 0; e < 2; ++e)
+#pragma unroll
+                for (int c = 0; c < kMergeChunk; ++c)
+                  if (b0 + c > b_last) {  // beyond the last contributor: no weight
+                    mv[e][c] = -INFINITY;
+                    lv[e][c] = 0.0f;
+                    pv[e][c] = 0.0f;
+                  }
 #pragma unroll
               for (int e = 0; e < 2; ++e) {
                 float Mc = M[e];

@@ -38,9 +38,11 @@ __global__ void __launch_bounds__(128) summaries_kernel(const T *__restrict__ K,
 }
 
 // ---------------------------------------------------------------------------------------------- scores
-// grid.x: chunks of 64 logical pages; grid.y: (request, selection row). 8 warps; each warp scores 8 pages with all
-// of their summary loads in flight at once. Dot products follow the fixed order: lane l accumulates fmaf over
-// i = l, l+32, ...; then an xor-butterfly 16, 8, 4, 2, 1.
+// grid.x: chunks of 64 logical pages; grid.y: (request, selection row). 8 warps; each warp scores 8 pages. The
+// prompt length, the warp's block-table entries and the query rows are loaded together, and the first head's
+// summary loads are in flight (unconditionally, from clamped page ids) while the group-summed query is formed.
+// Dot products follow the fixed order: lane l accumulates fmaf over i = l, l+32, ...; then an xor-butterfly
+// 16, 8, 4, 2, 1.
 constexpr int kScorePagesPerWarp = 8;
 constexpr int kScorePagesPerCta = 8 * kScorePagesPerWarp;
 constexpr int kMaxPooledHeads = 16;
@@ -50,64 +52,93 @@ __global__ void __launch_bounds__(256) score_kernel(const T *__restrict__ q, con
                                                     int hq, int num_pages, const int32_t *__restrict__ bt,
                                                     int max_pages, const int32_t *__restrict__ ctx_len,
                                                     int per_head, float *__restrict__ scores, int *err) {
+  constexpr int C = D / 32;
   __shared__ float qbar[kMaxPooledHeads][D];
   grid_dependency_sync();
   const int rows = per_head ? hkv : 1;
   const int row = blockIdx.y;
   const int r = row / rows, v = row - r * rows;
   const int G = hq / hkv;
-  const int N = min((ctx_len[r] + kPage - 1) / kPage, max_pages);
-  const int j0 = blockIdx.x * kScorePagesPerCta;
-  if (j0 >= N) return;
   const int h_lo = per_head ? v : 0, h_hi = per_head ? v + 1 : hkv;
-  for (int idx = threadIdx.x; idx < (h_hi - h_lo) * D; idx += blockDim.x) {
-    const int hh = h_lo + idx / D, i = idx % D;
-    float acc = 0.0f;
-    for (int g = 0; g < G; ++g) acc = __fadd_rn(acc, to_f(q[(static_cast<size_t>(r) * hq + hh * G + g) * D + i]));
-    qbar[hh - h_lo][i] = acc;
-  }
-  __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int j0 = blockIdx.x * kScorePagesPerCta;
   const int jb = j0 + warp * kScorePagesPerWarp;
-  if (jb >= N) return;
+  // independent loads: prompt length, block-table entries of this warp's pages, this thread's query elements
+  const int Lr = ctx_len[r];
   const int32_t *btr = bt + static_cast<size_t>(r) * max_pages;
   int pg[kScorePagesPerWarp];
+#pragma unroll
+  for (int u = 0; u < kScorePagesPerWarp; ++u) pg[u] = (jb + u < max_pages) ? btr[jb + u] : -1;
+  const int nq = (h_hi - h_lo) * D;
+  float qsum0 = 0.0f, qsum1 = 0.0f;  // this thread's (at most two) elements of the group-summed query
+  {
+    const int i0 = threadIdx.x, i1 = threadIdx.x + blockDim.x;
+    for (int g = 0; g < G; ++g) {
+      if (i0 < nq)
+        qsum0 = __fadd_rn(qsum0, to_f(q[(static_cast<size_t>(r) * hq + (h_lo + i0 / D) * G + g) * D + i0 % D]));
+      if (i1 < nq)
+        qsum1 = __fadd_rn(qsum1, to_f(q[(static_cast<size_t>(r) * hq + (h_lo + i1 / D) * G + g) * D + i1 % D]));
+    }
+  }
+  const int N = min((Lr + kPage - 1) / kPage, max_pages);
+  if (j0 >= N) return;  // uniform over the CTA
   bool ok[kScorePagesPerWarp];
+  int pc[kScorePagesPerWarp];
 #pragma unroll
   for (int u = 0; u < kScorePagesPerWarp; ++u) {
-    const int j = jb + u;
-    ok[u] = j < N;
-    pg[u] = ok[u] ? btr[j] : 0;
+    ok[u] = jb + u < N;
     if (ok[u] && (pg[u] < 0 || pg[u] >= num_pages)) {
       ok[u] = false;
       if (lane == 0) set_error(err, kErrPage);
     }
+    pc[u] = ok[u] ? pg[u] : 0;  // a valid page: the loads below are unconditional
   }
+  float sv[kScorePagesPerWarp][C];
+#pragma unroll
+  for (int u = 0; u < kScorePagesPerWarp; ++u)
+#pragma unroll
+    for (int c = 0; c < C; ++c) sv[u][c] = __ldg(S + (static_cast<size_t>(pc[u]) * hkv + h_lo) * D + lane + 32 * c);
+  // group-summed query rows into shared memory (g ascending, fp32)
+  {
+    const int i0 = threadIdx.x, i1 = threadIdx.x + blockDim.x;
+    if (i0 < nq) qbar[i0 / D][i0 % D] = qsum0;
+    if (i1 < nq) qbar[i1 / D][i1 % D] = qsum1;
+    for (int i = threadIdx.x + 2 * blockDim.x; i < nq; i += blockDim.x) {  // more than 2*blockDim elements
+      float acc = 0.0f;
+      for (int g = 0; g < G; ++g)
+        acc = __fadd_rn(acc, to_f(q[(static_cast<size_t>(r) * hq + (h_lo + i / D) * G + g) * D + i % D]));
+      qbar[i / D][i % D] = acc;
+    }
+  }
+  __syncthreads();
+  if (jb >= N) return;
   float tot[kScorePagesPerWarp];
   for (int hh = h_lo; hh < h_hi; ++hh) {
-    float sv[kScorePagesPerWarp][D / 32];
+    if (hh > h_lo) {
 #pragma unroll
-    for (int u = 0; u < kScorePagesPerWarp; ++u)
+      for (int u = 0; u < kScorePagesPerWarp; ++u)
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c)
-        sv[u][c] = ok[u] ? __ldg(S + (static_cast<size_t>(pg[u]) * hkv + hh) * D + lane + 32 * c) : 0.0f;
+        for (int c = 0; c < C; ++c) sv[u][c] = __ldg(S + (static_cast<size_t>(pc[u]) * hkv + hh) * D + lane + 32 * c);
+    }
 #pragma unroll
     for (int u = 0; u < kScorePagesPerWarp; ++u) {
       float a = 0.0f;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) a = __fmaf_rn(qbar[hh - h_lo][lane + 32 * c], sv[u][c], a);
+      for (int c = 0; c < C; ++c) a = __fmaf_rn(qbar[hh - h_lo][lane + 32 * c], sv[u][c], a);
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, o));
       tot[u] = (hh == h_lo) ? a : __fadd_rn(tot[u], a);
     }
   }
-  if (lane < kScorePagesPerWarp && ok[lane]) {
-    float val = tot[0];
+  float val = tot[0];
+  bool okl = ok[0];
 #pragma unroll
-    for (int u = 1; u < kScorePagesPerWarp; ++u)
-      if (lane == u) val = tot[u];
-    scores[static_cast<size_t>(row) * max_pages + jb + lane] = val;
-  }
+  for (int u = 1; u < kScorePagesPerWarp; ++u)
+    if (lane == u) {
+      val = tot[u];
+      okl = ok[u];
+    }
+  if (lane < kScorePagesPerWarp && okl) scores[static_cast<size_t>(row) * max_pages + jb + lane] = val;
 }
 
 // ------------------------------------------------------------------------------------ compaction helper
@@ -146,27 +177,116 @@ __device__ __forceinline__ void read_ark(const int32_t *per_seq_ark, int r, int 
   k = max(k, 0);
 }
 
+// --------------------------------------------------------------------------------------- compile view
+// One view row: the n selected pages (ascending, sel_at(i)) then the tail pages, physical ids from the full block
+// table; the horizon's slot mapping and the request's fallback flag come with the request's first row.
+struct ViewOut {
+  int32_t *vbt, *vlp, *vn, *vnsel;
+  int vcap, sel_cap, horizon;
+  int32_t *fallback;
+  float s_max;
+  int64_t *slot_out;
+  int32_t *pos_out;
+};
+
+template <class SelAt, class NselOf>
+__device__ void compile_view_row(int row, int rows, const int32_t *__restrict__ bt, int max_pages, int L, int S,
+                                 int n, SelAt sel_at, NselOf nsel_of, const ViewOut &vo, int *err) {
+  const int r = row / rows;
+  const int N = min((L + kPage - 1) / kPage, max_pages);
+  if (n > vo.sel_cap || n < 0) {
+    if (threadIdx.x == 0) set_error(err, kErrCapacity);
+    n = min(max(n, 0), vo.sel_cap);
+  }
+  const int32_t *btr = bt + static_cast<size_t>(r) * max_pages;
+  const int first_tail = min(L / kPage, max_pages);
+  int end_page = static_cast<int>((static_cast<int64_t>(S) + vo.horizon + kPage - 1) / kPage);
+  if (end_page > max_pages) {
+    if (threadIdx.x == 0) set_error(err, kErrCapacity);
+    end_page = max_pages;
+  }
+  const int last_sel = n > 0 ? sel_at(n - 1) : -1;
+  const int skip = (last_sel == first_tail) ? 1 : 0;
+  int n_tail = max(0, end_page - first_tail - skip);
+  int n_keep = n;
+  if (n_keep > vo.vcap) n_keep = vo.vcap;
+  if (n_keep + n_tail > vo.vcap) {
+    if (threadIdx.x == 0) set_error(err, kErrCapacity);
+    n_tail = vo.vcap - n_keep;
+  }
+  int32_t *obt = vo.vbt + static_cast<size_t>(row) * vo.vcap;
+  int32_t *olp = vo.vlp + static_cast<size_t>(row) * vo.vcap;
+  for (int i = threadIdx.x; i < n_keep; i += blockDim.x) {
+    const int j = sel_at(i);
+    const bool ok = j >= 0 && j < max_pages;
+    if (!ok) set_error(err, kErrPage);
+    olp[i] = ok ? j : 0;
+    obt[i] = ok ? btr[j] : -1;
+  }
+  for (int t = threadIdx.x; t < n_tail; t += blockDim.x) {
+    const int j = first_tail + skip + t;
+    olp[n_keep + t] = j;
+    obt[n_keep + t] = btr[j];
+  }
+  if (vo.slot_out && row % rows == 0) {  // slot mapping of the horizon tokens, once per request
+    for (int t = threadIdx.x; t < vo.horizon; t += blockDim.x) {
+      const int pos = S + t;
+      int64_t slot = -1;
+      if (pos >= 0 && pos / kPage < max_pages) {
+        const int page = btr[pos / kPage];
+        if (page >= 0) slot = static_cast<int64_t>(page) * kPage + pos % kPage;
+      }
+      vo.slot_out[static_cast<size_t>(r) * vo.horizon + t] = slot;
+      if (vo.pos_out) vo.pos_out[static_cast<size_t>(r) * vo.horizon + t] = pos;
+    }
+  }
+  if (threadIdx.x == 0) {
+    vo.vn[row] = n_keep + n_tail;
+    vo.vnsel[row] = n_keep;
+    if (vo.fallback && row % rows == 0) {
+      int fb = 0;
+      for (int v = 0; v < rows; ++v) {
+        const float ratio = static_cast<float>(nsel_of(r * rows + v)) / static_cast<float>(max(N, 1));
+        fb |= (ratio > vo.s_max) ? 1 : 0;
+      }
+      vo.fallback[r] = fb;
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------------------------- top-K
 // One CTA per selection row. Pinned pages [0, a) and [N-r, N); from the middle the k largest scores by a 4-pass
-// 8-bit radix select on order keys, ties resolved toward the lower page id; output ascending.
+// 8-bit radix select on order keys, ties resolved toward the lower page id; output ascending. With VIEW the CTA also
+// compiles its view row from the selection it just made (every row of a request selects the same number of pages,
+// so the request's fallback flag needs no other row).
 constexpr int kTopkThreads = 512;
+constexpr int kCandMax = 64;  // once at most this many keys share the selected prefix, they are ranked directly
 
+template <bool VIEW>
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float *__restrict__ scores, int rows,
                                                              const int32_t *__restrict__ ctx_len, int max_pages,
                                                              int a_def, int r_def, int k_def,
                                                              const int32_t *__restrict__ per_seq_ark, int cap,
                                                              int32_t *__restrict__ sel, int32_t *__restrict__ n_sel,
+                                                             const int32_t *__restrict__ bt,
+                                                             const int32_t *__restrict__ seq_len, const ViewOut vo,
                                                              int *err) {
-  extern __shared__ uint32_t keys[];  // [max_pages]
-  __shared__ int hist[256];
-  __shared__ int scan_scratch[32];
-  __shared__ int s_bin, s_remaining;
+  extern __shared__ uint32_t keys[];  // [max_pages], then (VIEW) the selection [cap]
+  int32_t *sel_s = reinterpret_cast<int32_t *>(keys + max_pages);
+  __shared__ int s_nsel;
+  __shared__ int hist2[2][256];  // pass p counts into hist2[p & 1] while hist2[(p + 1) & 1] is cleared
+  __shared__ unsigned long long scan_scratch[32];
+  __shared__ int s_bin, s_remaining, s_cnt, s_ncand, s_need;
+  __shared__ uint32_t s_cand[kCandMax], s_T;
+  if (threadIdx.x == 0) s_ncand = 0;
   grid_dependency_sync();
   const int row = blockIdx.x;
   const int r = row / rows;
   int a = a_def, rr = r_def, k = k_def;
   read_ark(per_seq_ark, r, a, rr, k);
-  int N = (ctx_len[r] + kPage - 1) / kPage;
+  const int Lr = ctx_len[r];
+  const int Sr = VIEW ? seq_len[r] : 0;
+  int N = (Lr + kPage - 1) / kPage;
   if (N > max_pages) {
     if (threadIdx.x == 0) set_error(err, kErrLength);
     N = max_pages;
@@ -175,7 +295,19 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float *__restr
   const int M = max(0, r_begin - a_end);
   const int kk = min(k, M);
   const float *sc = scores + static_cast<size_t>(row) * max_pages;
-  for (int j = a_end + threadIdx.x; j < r_begin; j += blockDim.x) keys[j] = order_key(sc[j]);
+  // middle-page keys, four loads in flight per thread (clamped indices: every load is issued)
+  for (int base = a_end; base < r_begin; base += 4 * static_cast<int>(blockDim.x)) {
+    float vals[4];
+    int js[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      js[u] = base + u * static_cast<int>(blockDim.x) + static_cast<int>(threadIdx.x);
+      vals[u] = sc[min(js[u], r_begin - 1)];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (js[u] < r_begin) keys[js[u]] = order_key(vals[u]);
+  }
   __syncthreads();
 
   // Radix select of the kk-th largest key among the middle pages.
@@ -183,13 +315,25 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float *__restr
   int remaining = kk;
   const bool all_middle = (kk == M);
   if (kk > 0 && !all_middle) {
+    for (int b = threadIdx.x; b < 256; b += blockDim.x) hist2[0][b] = 0;
+    __syncthreads();
+    const int lane_id = threadIdx.x & 31;
     for (int pass = 0; pass < 4; ++pass) {
       const int shift = 24 - 8 * pass;
-      for (int b = threadIdx.x; b < 256; b += blockDim.x) hist[b] = 0;
-      __syncthreads();
-      for (int j = a_end + threadIdx.x; j < r_begin; j += blockDim.x) {
-        const uint32_t key = keys[j];
-        if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1);
+      int *hist = hist2[pass & 1];
+      for (int b = threadIdx.x; b < 256; b += blockDim.x) hist2[(pass + 1) & 1][b] = 0;
+      // Scores of similar magnitude share few leading key bytes: lanes of a warp with equal bins are merged into
+      // one shared-memory atomic (the loop trip count is uniform over the block, so the warp stays converged).
+      for (int jj = a_end; jj < r_begin; jj += blockDim.x) {
+        const int j = jj + static_cast<int>(threadIdx.x);
+        const uint32_t key = j < r_begin ? keys[j] : 0u;
+        const bool take = j < r_begin && (key & mask) == prefix;
+        const unsigned tm = __ballot_sync(0xffffffffu, take);
+        if (take) {
+          const int bin = static_cast<int>((key >> shift) & 255u);
+          const unsigned grp = __match_any_sync(tm, bin);
+          if (lane_id == __ffs(grp) - 1) atomicAdd(&hist[bin], __popc(grp));
+        }
       }
       __syncthreads();
       if (threadIdx.x < 32) {
@@ -211,6 +355,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float *__restr
             if (cum + hist[b] >= remaining) {
               s_bin = b;
               s_remaining = remaining - cum;
+              s_cnt = hist[b];
               break;
             }
             cum += hist[b];
@@ -218,52 +363,100 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float *__restr
         }
       }
       __syncthreads();
+      // s_bin / s_remaining are rewritten only after the next pass's first barrier
       prefix |= static_cast<uint32_t>(s_bin) << shift;
       mask |= 0xFFu << shift;
       remaining = s_remaining;
-      __syncthreads();
+      if (pass < 3 && s_cnt <= kCandMax) {
+        // Few keys left with this prefix: gather them and take the remaining-th largest exactly. T is the key with
+        // fewer than `remaining` candidates above it and at least `remaining` at or above it.
+        for (int jj = a_end; jj < r_begin; jj += blockDim.x) {
+          const int j = jj + static_cast<int>(threadIdx.x);
+          if (j < r_begin) {
+            const uint32_t key = keys[j];
+            if ((key & mask) == prefix) s_cand[atomicAdd(&s_ncand, 1)] = key;
+          }
+        }
+        __syncthreads();
+        if (threadIdx.x < 32) {
+          const int nc = s_ncand;
+          for (int c0 = lane_id; c0 < nc; c0 += 32) {
+            const uint32_t x = s_cand[c0];
+            int gt = 0, ge = 0;
+            for (int i = 0; i < nc; ++i) {
+              const uint32_t y = s_cand[i];
+              gt += y > x ? 1 : 0;
+              ge += y >= x ? 1 : 0;
+            }
+            if (gt < remaining && remaining <= ge) {  // equal candidates write equal values
+              s_T = x;
+              s_need = remaining - gt;
+            }
+          }
+        }
+        __syncthreads();
+        prefix = s_T;
+        mask = 0xFFFFFFFFu;
+        remaining = s_need;
+        break;
+      }
     }
   }
   const uint32_t T = prefix;
   const int need = remaining;  // how many keys equal to T are taken (lowest ids first)
 
-  // Rank of each middle page among the pages whose key equals T, in id order.
+  // One block scan of packed counts per thread's id range: low half the pages taken for certain (pinned, or key
+  // above T), high half the middle pages whose key equals T. In id order, the first `need` of the latter are taken.
   const int per = (N + blockDim.x - 1) / blockDim.x;
   const int lo = min(N, static_cast<int>(threadIdx.x) * per), hi = min(N, lo + per);
-  int eq = 0;
-  if (kk > 0 && !all_middle)
-    for (int j = max(lo, a_end); j < min(hi, r_begin); ++j) eq += (keys[j] == T) ? 1 : 0;
-  const int eq_incl = block_inclusive_scan(eq, scan_scratch);
-  const int eq_base = eq_incl - eq;
-  // Selection flags, then ascending compaction.
-  auto chosen = [&](int j, int &eq_seen) -> bool {
-    if (j < a_end || j >= r_begin) return true;
-    if (kk == 0) return false;
-    if (all_middle) return true;
-    const uint32_t key = keys[j];
-    if (key > T) return true;
-    if (key == T) return (eq_seen++) < need;
-    return false;
-  };
-  int cnt = 0;
-  {
-    int eq_seen = eq_base;
-    for (int j = lo; j < hi; ++j) cnt += chosen(j, eq_seen) ? 1 : 0;
+  const bool radix = kk > 0 && !all_middle;
+  int c_sure = 0, c_eq = 0;
+  for (int j = lo; j < hi; ++j) {
+    if (j < a_end || j >= r_begin || (kk > 0 && all_middle)) {
+      ++c_sure;
+    } else if (radix) {
+      const uint32_t key = keys[j];
+      c_sure += key > T ? 1 : 0;
+      c_eq += key == T ? 1 : 0;
+    }
   }
-  const int incl = block_inclusive_scan(cnt, scan_scratch);
-  int pos = incl - cnt;
+  const unsigned long long mine = static_cast<unsigned long long>(c_sure) |
+                                  (static_cast<unsigned long long>(c_eq) << 32);
+  const unsigned long long incl = block_inclusive_scan(mine, scan_scratch);
+  const unsigned long long excl = incl - mine;
+  const int sure_before = static_cast<int>(excl & 0xffffffffull), eq_before = static_cast<int>(excl >> 32);
+  int pos = sure_before + min(eq_before, need);
+  int eq_seen = eq_before;
   int32_t *out = sel + static_cast<size_t>(row) * cap;
-  {
-    int eq_seen = eq_base;
-    for (int j = lo; j < hi; ++j)
-      if (chosen(j, eq_seen)) {
-        if (pos < cap) out[pos] = j;
-        ++pos;
+  for (int j = lo; j < hi; ++j) {
+    bool take;
+    if (j < a_end || j >= r_begin || (kk > 0 && all_middle)) {
+      take = true;
+    } else if (radix) {
+      const uint32_t key = keys[j];
+      take = key > T || (key == T && (eq_seen++) < need);
+    } else {
+      take = false;
+    }
+    if (take) {
+      if (pos < cap) {
+        out[pos] = j;
+        if (VIEW) sel_s[pos] = j;
       }
+      ++pos;
+    }
   }
   if (threadIdx.x == blockDim.x - 1) {
-    if (incl > cap) set_error(err, kErrCapacity);
-    n_sel[row] = min(incl, cap);
+    const int total = static_cast<int>(incl & 0xffffffffull) + min(static_cast<int>(incl >> 32), need);
+    if (total > cap) set_error(err, kErrCapacity);
+    n_sel[row] = min(total, cap);
+    s_nsel = min(total, cap);
+  }
+  if (VIEW) {
+    __syncthreads();
+    const int n = s_nsel;
+    compile_view_row(
+        row, rows, bt, max_pages, Lr, Sr, n, [&](int i) { return sel_s[i]; }, [&](int) { return n; }, vo, err);
   }
 }
 
@@ -304,83 +497,19 @@ __global__ void __launch_bounds__(512) spans_kernel(const int32_t *__restrict__ 
   if (threadIdx.x == 0) n_sel[r] = min(total, cap);
 }
 
-// --------------------------------------------------------------------------------------- compile view
-// One CTA per view row: selected pages (ascending) then tail pages, physical ids from the full block table.
+// One CTA per view row, reading a selection made by an earlier kernel.
 __global__ void __launch_bounds__(128) view_kernel(const int32_t *__restrict__ bt, int max_pages,
                                                    const int32_t *__restrict__ ctx_len,
                                                    const int32_t *__restrict__ seq_len,
                                                    const int32_t *__restrict__ sel, const int32_t *__restrict__ n_sel,
-                                                   int rows, int sel_cap, int horizon, int32_t *__restrict__ vbt,
-                                                   int32_t *__restrict__ vlp, int32_t *__restrict__ vn,
-                                                   int32_t *__restrict__ vnsel, int vcap,
-                                                   int32_t *__restrict__ fallback, float s_max,
-                                                   int64_t *__restrict__ slot_out, int32_t *__restrict__ pos_out,
-                                                   int *err) {
+                                                   int rows, const ViewOut vo, int *err) {
   grid_dependency_sync();
   const int row = blockIdx.x;
   const int r = row / rows;
-  const int L = ctx_len[r];
-  const int N = min((L + kPage - 1) / kPage, max_pages);
-  int n = n_sel[row];
-  if (n > sel_cap || n < 0) {
-    if (threadIdx.x == 0) set_error(err, kErrCapacity);
-    n = min(max(n, 0), sel_cap);
-  }
-  const int32_t *srow = sel + static_cast<size_t>(row) * sel_cap;
-  const int32_t *btr = bt + static_cast<size_t>(r) * max_pages;
-  const int first_tail = min(L / kPage, max_pages);
-  int end_page = static_cast<int>((static_cast<int64_t>(seq_len[r]) + horizon + kPage - 1) / kPage);
-  if (end_page > max_pages) {
-    if (threadIdx.x == 0) set_error(err, kErrCapacity);
-    end_page = max_pages;
-  }
-  const int last_sel = n > 0 ? srow[n - 1] : -1;
-  const int skip = (last_sel == first_tail) ? 1 : 0;
-  int n_tail = max(0, end_page - first_tail - skip);
-  int n_keep = n;
-  if (n_keep > vcap) n_keep = vcap;
-  if (n_keep + n_tail > vcap) {
-    if (threadIdx.x == 0) set_error(err, kErrCapacity);
-    n_tail = vcap - n_keep;
-  }
-  int32_t *obt = vbt + static_cast<size_t>(row) * vcap;
-  int32_t *olp = vlp + static_cast<size_t>(row) * vcap;
-  for (int i = threadIdx.x; i < n_keep; i += blockDim.x) {
-    const int j = srow[i];
-    const bool ok = j >= 0 && j < max_pages;
-    if (!ok) set_error(err, kErrPage);
-    olp[i] = ok ? j : 0;
-    obt[i] = ok ? btr[j] : -1;
-  }
-  for (int t = threadIdx.x; t < n_tail; t += blockDim.x) {
-    const int j = first_tail + skip + t;
-    olp[n_keep + t] = j;
-    obt[n_keep + t] = btr[j];
-  }
-  if (slot_out && row % rows == 0) {  // slot mapping of the horizon tokens, once per request
-    for (int t = threadIdx.x; t < horizon; t += blockDim.x) {
-      const int pos = seq_len[r] + t;
-      int64_t slot = -1;
-      if (pos >= 0 && pos / kPage < max_pages) {
-        const int page = btr[pos / kPage];
-        if (page >= 0) slot = static_cast<int64_t>(page) * kPage + pos % kPage;
-      }
-      slot_out[static_cast<size_t>(r) * horizon + t] = slot;
-      if (pos_out) pos_out[static_cast<size_t>(r) * horizon + t] = pos;
-    }
-  }
-  if (threadIdx.x == 0) {
-    vn[row] = n_keep + n_tail;
-    vnsel[row] = n_keep;
-    if (fallback && row % rows == 0) {
-      int fb = 0;
-      for (int v = 0; v < rows; ++v) {
-        const float ratio = static_cast<float>(n_sel[r * rows + v]) / static_cast<float>(max(N, 1));
-        fb |= (ratio > s_max) ? 1 : 0;
-      }
-      fallback[r] = fb;
-    }
-  }
+  const int32_t *srow = sel + static_cast<size_t>(row) * vo.sel_cap;
+  compile_view_row(
+      row, rows, bt, max_pages, ctx_len[r], seq_len[r], n_sel[row], [&](int i) { return srow[i]; },
+      [&](int rr) { return n_sel[rr]; }, vo, err);
 }
 
 // --------------------------------------------------------------------------------------- slot mapping
@@ -436,15 +565,21 @@ cudaError_t launch_score(const PoolArgs &p, const MapArgs &m, const void *q, int
 }
 
 cudaError_t launch_topk(const MapArgs &m, const float *scores, int rows, int a, int r, int k,
-                        const int32_t *per_seq_ark, int cap, int32_t *sel, int32_t *n_sel, int *err, cudaStream_t s) {
-  const size_t smem = static_cast<size_t>(m.max_pages) * sizeof(uint32_t);
+                        const int32_t *per_seq_ark, int cap, int32_t *sel, int32_t *n_sel, const ViewArgsOut *view,
+                        int *err, cudaStream_t s) {
+  const bool with_view = view != nullptr;
+  const size_t smem = static_cast<size_t>(m.max_pages) * sizeof(uint32_t) + (with_view ? cap * sizeof(int32_t) : 0);
+  auto kern = with_view ? topk_kernel<true> : topk_kernel<false>;
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  launch_pdl(topk_kernel, dim3(m.R * rows), dim3(kTopkThreads), smem, s, scores, rows, m.ctx_len, m.max_pages, a, r,
-             k, per_seq_ark, cap, sel, n_sel, err);
+  ViewOut vo{};
+  if (with_view)
+    vo = ViewOut{view->vbt, view->vlp, view->vn, view->vnsel, view->vcap, cap, view->horizon, view->fallback,
+                 view->s_max, view->slot_out, view->pos_out};
+  launch_pdl(kern, dim3(m.R * rows), dim3(kTopkThreads), smem, s, scores, rows, m.ctx_len, m.max_pages, a, r, k,
+             per_seq_ark, cap, sel, n_sel, m.bt, m.seq_len, vo, err);
   return cudaGetLastError();
 }
 
@@ -466,8 +601,9 @@ cudaError_t launch_compile_view(const MapArgs &m, const int32_t *sel, const int3
                                 int horizon, int32_t *vbt, int32_t *vlp, int32_t *vn, int32_t *vnsel, int vcap,
                                 int32_t *fallback, float s_max, int64_t *slot_out, int32_t *pos_out, int *err,
                                 cudaStream_t s) {
+  const ViewOut vo{vbt, vlp, vn, vnsel, vcap, sel_cap, horizon, fallback, s_max, slot_out, pos_out};
   launch_pdl(view_kernel, dim3(m.R * rows), dim3(128), 0, s, m.bt, m.max_pages, m.ctx_len, m.seq_len, sel, n_sel,
-             rows, sel_cap, horizon, vbt, vlp, vn, vnsel, vcap, fallback, s_max, slot_out, pos_out, err);
+             rows, vo, err);
   return cudaGetLastError();
 }
 

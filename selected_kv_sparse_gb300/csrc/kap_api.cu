@@ -122,12 +122,13 @@ size_t kap_score_workspace_size(int32_t num_seqs, int32_t rows_per_seq, int32_t 
   return static_cast<size_t>(num_seqs) * rows_per_seq * max_pages * sizeof(float);
 }
 
-kap_status kap_score_topk(const kap_kv_pool *pool, const kap_page_map *map, const void *q_dev,
-                          const kap_access_policy *policy, int32_t *sel_ids, int32_t *n_sel, void *workspace,
-                          size_t workspace_bytes, kap_stream stream) {
+namespace {
+kap_status score_topk_common(const kap_kv_pool *pool, const kap_page_map *map, const void *q_dev,
+                             const kap_access_policy *policy, int32_t *sel_ids, int32_t *n_sel, void *workspace,
+                             size_t workspace_bytes, const ViewArgsOut *vw, kap_stream stream) {
   kap_status st = check_pool(pool, true);
   if (st != KAP_OK) return st;
-  if ((st = check_map(map, false)) != KAP_OK) return st;
+  if ((st = check_map(map, vw != nullptr)) != KAP_OK) return st;
   if (!q_dev || !policy || !sel_ids || !n_sel || !workspace) return KAP_EINVAL;
   if (!aligned16(q_dev)) return KAP_EINVAL;
   if (policy->anchor < 0 || policy->recent < 0 || policy->topk < 0 || policy->cap <= 0) return KAP_EINVAL;
@@ -137,7 +138,8 @@ kap_status kap_score_topk(const kap_kv_pool *pool, const kap_page_map *map, cons
       policy->cap < map->max_pages)
     return KAP_ECAPACITY;
   if (!policy->per_kv_head && pool->num_kv_heads > 16) return KAP_EUNSUPPORTED;
-  if (static_cast<size_t>(map->max_pages) * 4 > 200 * 1024) return KAP_EUNSUPPORTED;
+  const size_t topk_smem = static_cast<size_t>(map->max_pages) * 4 + (vw ? static_cast<size_t>(policy->cap) * 4 : 0);
+  if (topk_smem > 200 * 1024) return KAP_EUNSUPPORTED;
   const int rows = policy->per_kv_head ? pool->num_kv_heads : 1;
   if (workspace_bytes < kap_score_workspace_size(map->num_seqs, rows, map->max_pages)) return KAP_ECAPACITY;
   const PoolArgs pa = pool_args(pool);
@@ -147,7 +149,30 @@ kap_status kap_score_topk(const kap_kv_pool *pool, const kap_page_map *map, cons
   cudaError_t e = launch_score(pa, ma, q_dev, policy->per_kv_head, scores, err, cs(stream));
   if (e != cudaSuccess) return cuda_status(e);
   return cuda_status(launch_topk(ma, scores, rows, policy->anchor, policy->recent, policy->topk, policy->per_seq_ark,
-                                 policy->cap, sel_ids, n_sel, err, cs(stream)));
+                                 policy->cap, sel_ids, n_sel, vw, err, cs(stream)));
+}
+}  // namespace
+
+kap_status kap_score_topk(const kap_kv_pool *pool, const kap_page_map *map, const void *q_dev,
+                          const kap_access_policy *policy, int32_t *sel_ids, int32_t *n_sel, void *workspace,
+                          size_t workspace_bytes, kap_stream stream) {
+  return score_topk_common(pool, map, q_dev, policy, sel_ids, n_sel, workspace, workspace_bytes, nullptr, stream);
+}
+
+kap_status kap_score_topk_view(const kap_kv_pool *pool, const kap_page_map *map, const void *q_dev,
+                               const kap_access_policy *policy, int32_t *sel_ids, int32_t *n_sel, void *workspace,
+                               size_t workspace_bytes, int32_t horizon_tokens, const kap_view *view,
+                               int32_t *fallback_dev, float s_max, int64_t *slot_out, int32_t *pos_out,
+                               kap_stream stream) {
+  if (!policy || !view || horizon_tokens < 0) return KAP_EINVAL;
+  if (!view->block_table || !view->logical_page || !view->n_entries || !view->n_selected) return KAP_EINVAL;
+  const int rows = policy->per_kv_head ? (pool ? pool->num_kv_heads : 0) : 1;
+  if (view->rows_per_seq != rows) return KAP_ESHAPE;
+  if (static_cast<int64_t>(view->cap) < static_cast<int64_t>(policy->cap) + (horizon_tokens + 15) / 16 + 1)
+    return KAP_ECAPACITY;
+  const ViewArgsOut vw{view->block_table, view->logical_page, view->n_entries, view->n_selected, view->cap,
+                       horizon_tokens, fallback_dev, s_max, slot_out, pos_out};
+  return score_topk_common(pool, map, q_dev, policy, sel_ids, n_sel, workspace, workspace_bytes, &vw, stream);
 }
 
 kap_status kap_select_spans(const kap_page_map *map, const int32_t *spans_dev, const int32_t *span_offsets_dev,

@@ -227,27 +227,20 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// Inclusive prefix sum over a block; `scratch` holds one int per warp (<= 32 warps). Ends with a barrier.
-__device__ __forceinline__ int block_inclusive_scan(int v, int *scratch) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+// Inclusive prefix sum over a block; `scratch` holds one value per warp (<= 32 warps). Each thread adds the totals
+// of the warps before its own (shared-memory broadcasts). Ends with a barrier, so the scratch can be reused.
+template <class V>
+__device__ __forceinline__ V block_inclusive_scan(V v, V *scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int n = __shfl_up_sync(0xffffffffu, v, o);
+    const V n = __shfl_up_sync(0xffffffffu, v, o);
     if (lane >= o) v += n;
   }
   if (lane == 31) scratch[warp] = v;
   __syncthreads();
-  if (warp == 0) {
-    int s = lane < nw ? scratch[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += n;
-    }
-    if (lane < nw) scratch[lane] = s;
-  }
-  __syncthreads();
-  const int add = warp > 0 ? scratch[warp - 1] : 0;
+  V add = 0;
+  for (int w = 0; w < warp; ++w) add += scratch[w];
   __syncthreads();
   return v + add;
 }

@@ -27,8 +27,19 @@ struct ViewArgs {
 cudaError_t launch_build_summaries(const PoolArgs &p, const MapArgs &m, int *err, cudaStream_t s);
 cudaError_t launch_score(const PoolArgs &p, const MapArgs &m, const void *q, int per_head, float *scores,
                          int *err, cudaStream_t s);
+// Outputs of view compilation fused into top-K (see kap_score_topk_view).
+struct ViewArgsOut {
+  int32_t *vbt, *vlp, *vn, *vnsel;
+  int vcap, horizon;
+  int32_t *fallback;
+  float s_max;
+  int64_t *slot_out;
+  int32_t *pos_out;
+};
+// view non-null: the top-K CTA of each row also compiles that row's view
 cudaError_t launch_topk(const MapArgs &m, const float *scores, int rows, int a, int r, int k,
-                        const int32_t *per_seq_ark, int cap, int32_t *sel, int32_t *n_sel, int *err, cudaStream_t s);
+                        const int32_t *per_seq_ark, int cap, int32_t *sel, int32_t *n_sel, const ViewArgsOut *view,
+                        int *err, cudaStream_t s);
 cudaError_t launch_select_spans(const MapArgs &m, const int32_t *spans, const int32_t *span_offsets, int a, int r,
                                 const int32_t *per_seq_ark, int cap, int32_t *sel, int32_t *n_sel, int *err,
                                 cudaStream_t s);

@@ -84,15 +84,21 @@ class DecodeCycle:
 
     # -------------------------------------------------------------------------------------------------- phases
     def plan(self, q_route: torch.Tensor, stream=None):
-        """Selection (scores + A/R/K top-K, or spans), compact view and both slot mappings."""
+        """Selection (scores + A/R/K top-K, or spans), compact view and both slot mappings. Fused, score selection
+        and view compilation are one call (kap_score_topk_view)."""
         if self.spans is not None:
             kb.kap_select_spans(self.map_plan, self.spans, self.span_offsets, self.policy, self.sel_ids, self.n_sel,
                                 stream)
+        elif self.fused:
+            kb.kap_score_topk_view(self.pool, self.map_plan, q_route, self.policy, self.sel_ids, self.n_sel,
+                                   self.ws_score, self.horizon, self.view, self.fallback, self.s_max, self.slots_prop,
+                                   self.pos_prop, stream)
         else:
             kb.kap_score_topk(self.pool, self.map_plan, q_route, self.policy, self.sel_ids, self.n_sel, self.ws_score,
                               stream)
-        kb.kap_compile_view(self.map_plan, self.sel_ids, self.n_sel, self.horizon, self.view, self.fallback,
-                            self.s_max, self.slots_prop, self.pos_prop, stream)
+        if self.spans is not None or not self.fused:
+            kb.kap_compile_view(self.map_plan, self.sel_ids, self.n_sel, self.horizon, self.view, self.fallback,
+                                self.s_max, self.slots_prop, self.pos_prop, stream)
         if not self.window_is_horizon:
             kb.kap_slot_mapping(self.map_plan, self.q_offsets, self.q_start, self.slots_ver, self.pos_ver, stream)
 
@@ -133,10 +139,11 @@ class DecodeCycle:
         self.verify(q_ver, k_new_ver, v_new_ver, stream)
 
     def launches_per_cycle(self) -> int:
-        """Kernel launches of one run(): selection (score + top-K, or spans), the view (with the horizon's slot
-        mapping), a separate window slot mapping when the windows differ from the horizon, per step one fused
-        kernel (or an append and a proposal kernel), then the window append and verification."""
-        sel = 1 if self.spans is not None else 2
+        """Kernel launches of one run(): selection and view (score + top-K with the view fused in; unfused score,
+        top-K and view; or spans and view), a separate window slot mapping when the windows differ from the
+        horizon, per step one fused kernel (or an append and a proposal kernel), then the window append and
+        verification."""
+        sel_view = 2 if self.spans is not None else (2 if self.fused else 3)
         slots = 0 if self.window_is_horizon else 1
         per_step = 1 if self.fused else 2
-        return sel + 1 + slots + per_step * self.k_prop + 2
+        return sel_view + slots + per_step * self.k_prop + 2
