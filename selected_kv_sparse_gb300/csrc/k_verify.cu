@@ -27,6 +27,7 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kMaxCtas = 4096;
+constexpr int kMaxDeferred = 16;  // row segments whose hand-off a CTA postpones to the end of its tiles
 
 struct VParams {
   int num_pages, hkv, hq;
@@ -52,6 +53,11 @@ __device__ __forceinline__ int row_tiles(const VParams &p, int row) {
   if (nq <= 0) return 0;
   const int pages = (p.q_start[r] + nq + kPage - 1) / kPage;
   return (pages + 7) / 8;
+}
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int *p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
 }
 __device__ __forceinline__ int owner_cta(int64_t x, int64_t E, int nb) {
   return static_cast<int>(((x + 1) * nb - 1) / E);
@@ -148,7 +154,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   TileMeta *meta = reinterpret_cast<TileMeta *>(sm + L::OFF_META);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::OFF_TMEM);
   __shared__ int64_t s_total;
-  __shared__ int s_flag, s_abort, s_row0;
+  __shared__ int s_abort, s_row0;
+  __shared__ int4 s_def[kMaxDeferred];  // row segments whose partial record awaits counting in: row, b_first,
+  __shared__ int s_defn[kMaxDeferred];  // b_last, first window row; and the row's query columns
+  __shared__ int s_deflast[kMaxDeferred];
+  __shared__ int s_ndef;
   volatile int *abort_flag = &s_abort;
   __shared__ int64_t s_rb0, s_re0;
 
@@ -168,6 +178,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   if (tid == 0) {
     s_abort = 0;
+    s_ndef = 0;
     for (int i = 0; i < L::NBAR; ++i) mbar_init(&bars[i], 1);
     for (int b = 0; b < 2; ++b) {  // barriers the 4 softmax warps arrive on (one elected lane per warp)
       mbar_init(&sfree[b], 4);
@@ -294,17 +305,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int qoff = row_qoff;
         const __nv_bfloat16 *qg = static_cast<const __nv_bfloat16 *>(p.q);
         unsigned char *qd = Qs + qb * 2 * L::KATOM;
-        for (int idx = lane; idx < NPMAX * 16; idx += 32) {
-          const int n = idx >> 4, c = idx & 15;
-          uint4 val = make_uint4(0, 0, 0, 0);
-          if (n < nreal) {
-            const int i = n / G, g = n - (n / G) * G;
-            val = *reinterpret_cast<const uint4 *>(qg + (static_cast<size_t>(qoff + i) * p.hq + pl_h * G + g) * 128 +
-                                                   c * 8);
+        // 16-byte pieces idx = lane + 32 u of the [NPMAX x 128] operand, loaded 8 at a time (one round trip)
+        // before any is stored
+        constexpr int kQPieces = NPMAX * 16 / 32;  // per lane
+        for (int u0 = 0; u0 < kQPieces; u0 += 8) {
+          uint4 val[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int idx = lane + 32 * (u0 + u);
+            const int n = idx >> 4, c = idx & 15;
+            const int nc_ = n < nreal ? n : 0;  // clamped row: the load is always issued
+            const int i = nc_ / G, g = nc_ - (nc_ / G) * G;
+            val[u] = *reinterpret_cast<const uint4 *>(qg + (static_cast<size_t>(qoff + i) * p.hq + pl_h * G + g) * 128 +
+                                                      c * 8);
+            if (n >= nreal) val[u] = make_uint4(0, 0, 0, 0);
           }
-          const int katom = c >> 3, cc = c & 7;
-          *reinterpret_cast<uint4 *>(qd + katom * L::KATOM + (n >> 3) * 1024 + (n & 7) * 128 + ((cc ^ (n & 7)) << 4)) =
-              val;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int idx = lane + 32 * (u0 + u);
+            const int n = idx >> 4, c = idx & 15;
+            const int katom = c >> 3, cc = c & 7;
+            *reinterpret_cast<uint4 *>(qd + katom * L::KATOM + (n >> 3) * 1024 + (n & 7) * 128 +
+                                       ((cc ^ (n & 7)) << 4)) = val[u];
+          }
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -465,6 +488,97 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       return true;
     };
+    // Last arriver of a row: merges the partial records of CTAs b_first..b_last and writes the row's output.
+    // Thread t owns 16 consecutive head dims of one query column (8 threads per column, 16 columns at a time); for
+    // every chunk of 8 contributors it issues all its loads (the (m, l) pair and four 16-byte pieces of the
+    // partial output per contributor) before using any, so a chunk costs one round trip and no barrier.
+    auto merge_row = [&](int row, int b_first, int b_last, int qoff, int nreal) {
+      const int h = row - (row / p.hkv) * p.hkv;
+      __nv_bfloat16 *outp = static_cast<__nv_bfloat16 *>(p.out);
+      const int nc = b_last - b_first + 1;
+      const int d0 = (tid & 7) * 16;
+      for (int n0 = 0; n0 < nreal; n0 += 16) {
+        const int n = n0 + (tid >> 3);
+        const int nn = n < nreal ? n : n0;  // clamped column: every load below is issued
+        float acc[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) acc[e] = 0.0f;
+        float M = -INFINITY, Ls = 0.0f;
+        for (int b0 = 0; b0 < nc; b0 += 8) {
+          float2 ml[8];
+          float4 pv[8][4];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const size_t sl = static_cast<size_t>(b_first + min(b0 + c, nc - 1) + row);
+            ml[c] = __ldcg(reinterpret_cast<const float2 *>(p.ml) + sl * p.npad_ws + nn);
+            const float4 *pp = reinterpret_cast<const float4 *>(p.part + (sl * p.npad_ws + nn) * 128 + d0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) pv[c][q] = __ldcg(pp + q);
+          }
+          float Mc = M;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            if (b0 + c < nc) Mc = fmaxf(Mc, ml[c].x);
+          if (Mc == -INFINITY) continue;
+          const float rs = (M == -INFINITY) ? 0.0f : exp2f(M - Mc);
+          Ls *= rs;
+#pragma unroll
+          for (int e = 0; e < 16; ++e) acc[e] *= rs;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            if (b0 + c >= nc || ml[c].x == -INFINITY) continue;
+            const float w = exp2f(ml[c].x - Mc);
+            Ls = fmaf(ml[c].y, w, Ls);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              acc[4 * q] = fmaf(pv[c][q].x, w, acc[4 * q]);
+              acc[4 * q + 1] = fmaf(pv[c][q].y, w, acc[4 * q + 1]);
+              acc[4 * q + 2] = fmaf(pv[c][q].z, w, acc[4 * q + 2]);
+              acc[4 * q + 3] = fmaf(pv[c][q].w, w, acc[4 * q + 3]);
+            }
+          }
+          M = Mc;
+        }
+        if (n < nreal) {
+          const int i = n / G, g = n - (n / G) * G;
+          const float inv = Ls > 0.0f ? 1.0f / Ls : 0.0f;
+          uint32_t wd[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * e] * inv, acc[2 * e + 1] * inv);
+            wd[e] = *reinterpret_cast<const uint32_t *>(&b2);
+          }
+          uint4 *dst = reinterpret_cast<uint4 *>(outp + (static_cast<size_t>(qoff + i) * p.hq + h * G + g) * 128 + d0);
+          dst[0] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+          dst[1] = make_uint4(wd[4], wd[5], wd[6], wd[7]);
+          if ((tid & 7) == 0)
+            p.lse[static_cast<size_t>(qoff + i) * p.hq + h * G + g] = Ls > 0.0f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+        }
+      }
+    };
+    // Counts the noted row segments in: one thread's acquire-release atomic per row publishes this CTA's records
+    // (ordered before it by the group barrier) and, for the row's last arriver, makes the others' records visible.
+    auto flush_deferred = [&]() {
+      named_sync_128();
+      const int nd = s_ndef;
+      if (tid == 0)
+        for (int d = 0; d < nd; ++d) {
+          const int4 e = s_def[d];
+          const int old = atom_add_acq_rel_gpu(&p.counters[e.x], 1);
+          const int last = (old == e.z - e.y) ? 1 : 0;
+          if (last) p.counters[e.x] = 0;  // every contributor has arrived: leave the counter at zero
+          s_deflast[d] = last;
+        }
+      named_sync_128();
+      for (int d = 0; d < nd; ++d)
+        if (s_deflast[d]) {
+          const int4 e = s_def[d];
+          merge_row(e.x, e.y, e.z, e.w, s_defn[d]);
+        }
+      named_sync_128();
+      if (tid == 0) s_ndef = 0;
+      named_sync_128();
+    };
     int pending = -1, pending_npad = 16;  // tile whose O is not merged yet
     bool pending_resc = false;
     bool okrun = true;
@@ -617,111 +731,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               l > 0.0f ? (m_run[tid] + log2f(l)) * kLn2 : -INFINITY;
         }
       } else {
+        // Partial record of this row segment. The row is counted in (and merged, by its last arriver) only once
+        // this CTA's tiles are done, so the pipeline never waits here on other CTAs' progress.
         const int slot = static_cast<int>(blockIdx.x) + m.row;
         float *pp = p.part + static_cast<size_t>(slot) * p.npad_ws * 128;
 #pragma unroll
         for (int n = 0; n < NPMAX; ++n)
           if (n < npad) __stcg(pp + n * 128 + tid, oreg[n]);
-        if (tid < npad) {
-          __stcg(p.ml + (static_cast<size_t>(slot) * p.npad_ws + tid) * 2, m_run[tid]);
-          __stcg(p.ml + (static_cast<size_t>(slot) * p.npad_ws + tid) * 2 + 1, lsum[tid]);
-        }
-        __threadfence();
-        named_sync_128();
+        if (tid < npad)
+          __stcg(reinterpret_cast<float2 *>(p.ml) + static_cast<size_t>(slot) * p.npad_ws + tid,
+                 make_float2(m_run[tid], lsum[tid]));
         if (tid == 0) {
-          const int old = atomicAdd(&p.counters[m.row], 1);
-          s_flag = (old == ncontrib - 1) ? 1 : 0;
-          if (s_flag) p.counters[m.row] = 0;  // every contributor has arrived: leave the counter at zero
+          s_def[s_ndef] = make_int4(m.row, b_first, b_last, qoff);
+          s_defn[s_ndef] = nreal;
+          ++s_ndef;
         }
         named_sync_128();
-        if (s_flag) {
-          // Last arriver: merge the row's partial records from CTAs b_first..b_last. The (m, l) pairs of up to 8
-          // contributors are staged in the idle P buffers by one parallel load pass; the partial outputs of the
-          // group are then loaded with every load in flight before any is used.
-          __threadfence();
-          float *sm_m = reinterpret_cast<float *>(Ps);  // [8][NPMAX]: both P buffers are idle at a segment end
-          float *sm_w = sm_m + 8 * NPMAX;               // [8][NPMAX]
-          float Mrun = -INFINITY, Lrun = 0.0f;          // column tid (tid < nreal)
-#pragma unroll
-          for (int n = 0; n < NPMAX; ++n) oreg[n] = 0.0f;
-          const int nc = b_last - b_first + 1;
-          for (int g0 = 0; g0 < nc; g0 += 8) {
-            const int ng = min(8, nc - g0);
-            named_sync_128();
-            for (int q = tid; q < ng * nreal; q += 128) {
-              const int bb = q / nreal, n = q - (q / nreal) * nreal;
-              const size_t o = (static_cast<size_t>(b_first + g0 + bb + m.row) * p.npad_ws + n) * 2;
-              sm_m[bb * NPMAX + n] = __ldcg(p.ml + o);
-              sm_w[bb * NPMAX + n] = __ldcg(p.ml + o + 1);
-            }
-            named_sync_128();
-            if (tid < nreal) {
-              float M = Mrun;
-              for (int bb = 0; bb < ng; ++bb) M = fmaxf(M, sm_m[bb * NPMAX + tid]);
-              const float resc = (Mrun == -INFINITY || M == -INFINITY) ? 0.0f : exp2f(Mrun - M);
-              float Lsum = Lrun * resc;
-              for (int bb = 0; bb < ng; ++bb) {
-                const float mb = sm_m[bb * NPMAX + tid];
-                const float w = (mb == -INFINITY || M == -INFINITY) ? 0.0f : exp2f(mb - M);
-                Lsum += sm_w[bb * NPMAX + tid] * w;
-                sm_w[bb * NPMAX + tid] = w;
-              }
-              colmax[tid] = resc;
-              Mrun = M;
-              Lrun = Lsum;
-            }
-            named_sync_128();
-            if (g0 > 0) {
-#pragma unroll
-              for (int n = 0; n < NPMAX; ++n) oreg[n] *= colmax[n];
-            }
-#pragma unroll
-            for (int n0 = 0; n0 < NPMAX; n0 += 16) {
-              if (n0 < nreal) {
-                float v[8][16];
-#pragma unroll
-                for (int bb = 0; bb < 8; ++bb)
-#pragma unroll
-                  for (int n = 0; n < 16; ++n)
-                    v[bb][n] = (bb < ng && n0 + n < nreal)
-                                   ? __ldcg(p.part +
-                                            (static_cast<size_t>(b_first + g0 + bb + m.row) * p.npad_ws + n0 + n) * 128 +
-                                            tid)
-                                   : 0.0f;
-#pragma unroll
-                for (int bb = 0; bb < 8; ++bb)
-#pragma unroll
-                  for (int n = 0; n < 16; ++n)
-                    if (bb < ng) oreg[n0 + n] = fmaf(v[bb][n], sm_w[bb * NPMAX + n0 + n], oreg[n0 + n]);
-              }
-            }
-          }
-          named_sync_128();
-          float *Ms = colmax;          // [NPMAX]
-          float *Ls = colmax + NPMAX;  // [NPMAX]
-          if (tid < nreal) {
-            Ms[tid] = Mrun;
-            Ls[tid] = Lrun;
-          }
-          named_sync_128();
-#pragma unroll
-          for (int n = 0; n < NPMAX; ++n) {
-            if (n < nreal) {
-              const int i = n / G, g = n - (n / G) * G;
-              const float l = Ls[n];
-              outp[(static_cast<size_t>(qoff + i) * p.hq + h * G + g) * 128 + tid] =
-                  __float2bfloat16_rn(l > 0.0f ? oreg[n] / l : 0.0f);
-            }
-          }
-          if (tid < nreal) {
-            const int i = tid / G, g = tid - (tid / G) * G;
-            const float l = Ls[tid];
-            p.lse[static_cast<size_t>(qoff + i) * p.hq + h * G + g] = l > 0.0f ? (Ms[tid] + log2f(l)) * kLn2 : -INFINITY;
-          }
-        }
+        if (s_ndef == kMaxDeferred) flush_deferred();
       }
       named_sync_128();
     }
+    // every softmax thread gets here; the hand-offs run only when none of them gave up on a wait
+    if (!named_or_128(!okrun)) flush_deferred();
     if (!okrun) *abort_flag = 1;
   }
 
