@@ -164,6 +164,20 @@ __device__ __forceinline__ void load_inv_freq(const float *inv_freq, int i0, flo
   }
 }
 
+// Four consecutive output elements, rounded to the output type, in one store (8 bytes bf16, 16 bytes fp32).
+template <class T>
+__device__ __forceinline__ void store4(T *dst, float a, float b, float c, float d);
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16 *dst, float a, float b, float c, float d) {
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
+  *reinterpret_cast<uint2 *>(dst) =
+      make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
+}
+template <>
+__device__ __forceinline__ void store4<float>(float *dst, float a, float b, float c, float d) {
+  *reinterpret_cast<float4 *>(dst) = make_float4(a, b, c, d);
+}
+
 // Rotary factors (cos, sin) at position pos of the EPL pairs whose elements this lane holds (dims base_dim ..).
 template <int EPL, int D>
 __device__ __forceinline__ void rope_lane_factors(int base_dim, int pos, const float *inv_freq, float *cs, float *sn) {
@@ -707,70 +721,48 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
         }
         group_sync(bar_id, bar_n);
         if (s_last[si]) {
-          // Last arriver: merge the partial records of CTAs b_first..b_last. A thread takes two of its elements at a
-          // time and loads their records of kMergeChunk contributors at once: one round trip per chunk.
-          for (int i0 = gt; i0 < G * D; i0 += 2 * GT) {
-            int ie[2], ge[2];
-            bool has[2];
-            float M[2], Ls[2], acc[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              ie[e] = i0 + e * GT;
-              has[e] = ie[e] < G * D;
-              if (!has[e]) ie[e] = i0;  // a valid address: every load below is issued unconditionally
-              ge[e] = ie[e] / D;
-              M[e] = -INFINITY;
-              Ls[e] = 0.0f;
-              acc[e] = 0.0f;
-            }
+          // Last arriver: merge the partial records of CTAs b_first..b_last. A thread owns 4 consecutive elements of
+          // one head; per chunk of kMergeChunk contributors it issues all its loads (an (m, l) pair and a 16-byte piece
+          // of the partial output per contributor) before using any: one round trip per chunk.
+          for (int i4 = gt; i4 < G * D / 4; i4 += GT) {
+            const int i0 = i4 * 4, g = i0 / D;
+            float M = -INFINITY, Ls = 0.0f;
+            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
             for (int b0 = b_first; b0 <= b_last; b0 += kMergeChunk) {
-              float mv[2][kMergeChunk], lv[2][kMergeChunk], pv[2][kMergeChunk];
+              float2 ml[kMergeChunk];
+              float4 pv[kMergeChunk];
 #pragma unroll
-              for (int e = 0; e < 2; ++e)
-#pragma unroll
-                for (int c = 0; c < kMergeChunk; ++c) {
-                  const size_t ps = static_cast<size_t>(min(b0 + c, b_last)) + sg.row;  // clamped: always valid
-                  const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.ml) + ps * G + ge[e]);
-                  mv[e][c] = ml.x;
-                  lv[e][c] = ml.y;
-                  pv[e][c] = __ldcg(p.part + ps * G * D + ie[e]);
-                }
-#pragma unroll
-              for (int e = 0; e < 2; ++e)
-#pragma unroll
-                for (int c = 0; c < kMergeChunk; ++c)
-                  if (b0 + c > b_last) {  // beyond the last contributor: no weight
-                    mv[e][c] = -INFINITY;
-                    lv[e][c] = 0.0f;
-                    pv[e][c] = 0.0f;
-                  }
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                float Mc = M[e];
-#pragma unroll
-                for (int c = 0; c < kMergeChunk; ++c) Mc = fmaxf(Mc, mv[e][c]);
-                if (Mc != -INFINITY) {
-                  const float rs = (M[e] == -INFINITY) ? 0.0f : exp2f(M[e] - Mc);
-                  acc[e] *= rs;
-                  Ls[e] *= rs;
-#pragma unroll
-                  for (int c = 0; c < kMergeChunk; ++c) {
-                    const float w = (mv[e][c] == -INFINITY) ? 0.0f : exp2f(mv[e][c] - Mc);
-                    acc[e] = fmaf(pv[e][c], w, acc[e]);
-                    Ls[e] = fmaf(lv[e][c], w, Ls[e]);
-                  }
-                  M[e] = Mc;
-                }
+              for (int c = 0; c < kMergeChunk; ++c) {
+                const size_t ps = static_cast<size_t>(min(b0 + c, b_last)) + sg.row;  // clamped: always valid
+                ml[c] = __ldcg(reinterpret_cast<const float2 *>(p.ml) + ps * G + g);
+                pv[c] = __ldcg(reinterpret_cast<const float4 *>(p.part + ps * G * D + i0));
               }
+              float Mc = M;
+#pragma unroll
+              for (int c = 0; c < kMergeChunk; ++c)
+                if (b0 + c <= b_last) Mc = fmaxf(Mc, ml[c].x);
+              if (Mc == -INFINITY) continue;
+              const float rs = (M == -INFINITY) ? 0.0f : exp2f(M - Mc);
+              Ls *= rs;
+#pragma unroll
+              for (int e = 0; e < 4; ++e) acc[e] *= rs;
+#pragma unroll
+              for (int c = 0; c < kMergeChunk; ++c) {
+                if (b0 + c > b_last || ml[c].x == -INFINITY) continue;
+                const float w = exp2f(ml[c].x - Mc);
+                Ls = fmaf(ml[c].y, w, Ls);
+                acc[0] = fmaf(pv[c].x, w, acc[0]);
+                acc[1] = fmaf(pv[c].y, w, acc[1]);
+                acc[2] = fmaf(pv[c].z, w, acc[2]);
+                acc[3] = fmaf(pv[c].w, w, acc[3]);
+              }
+              M = Mc;
             }
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              if (!has[e]) continue;
-              outp[out_base + ie[e]] = from_f<T>(Ls[e] > 0.0f ? acc[e] / Ls[e] : 0.0f);
-              if (ie[e] - ge[e] * D == 0) {
-                lse_row[ge[e]] = Ls[e] > 0.0f ? (M[e] + log2f(Ls[e])) * kLn2 : -INFINITY;
-                if (!(Ls[e] > 0.0f)) set_error(p.err, kErrLength);
-              }
+            const float inv = Ls > 0.0f ? 1.0f / Ls : 0.0f;
+            store4<T>(outp + out_base + i0, acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+            if (i0 - g * D == 0) {
+              lse_row[g] = Ls > 0.0f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+              if (!(Ls > 0.0f)) set_error(p.err, kErrLength);
             }
           }
         }
