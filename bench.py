@@ -165,6 +165,36 @@ def step_bytes(w, cyc, sel_ids, n_sel):
     return dict(score=score, propose=prop, verify=ver, append=app)
 
 
+# ------------------------------------------------------------------------------------------------ arenas
+class Arena:
+    """One contiguous device buffer holding, for each of `copies` layers, tensors of the given (name, shape, dtype);
+    each tensor starts on a 256-byte boundary."""
+
+    def __init__(self, specs, copies, device):
+        import torch
+        self.specs = specs
+        self.offsets = []
+        off = 0
+        for _ in range(copies):
+            lay = {}
+            for name, shape, dtype in specs:
+                n = 1
+                for x in shape:
+                    n *= int(x)
+                nbytes = n * torch.tensor([], dtype=dtype).element_size()
+                lay[name] = (off, nbytes)
+                off += (nbytes + 255) // 256 * 256
+            self.offsets.append(lay)
+        self.buf = torch.zeros(off, dtype=torch.uint8, device=device)
+
+    def views(self, copy):
+        out = {}
+        for name, shape, dtype in self.specs:
+            off, nbytes = self.offsets[copy][name]
+            out[name] = self.buf[off:off + nbytes].view(dtype).view(shape)
+        return out
+
+
 # ------------------------------------------------------------------------------------------ recorded counters
 KERNEL_SOURCES = {"verify_tc_kernel": ["k_verify.cu", "kap_device.cuh"],
                   "propose_kernel": ["k_propose.cu", "kap_device.cuh"]}
@@ -287,7 +317,10 @@ def run_kap(args, world, rank, local):
     kap.load()
 
     L = args.layers
+    # All layers' inputs live in one device buffer and all outputs in another (views per layer), so the
+    # end-to-end step moves each direction with a single copy.
     layers = []
+    out_arena = None
     for l in range(L):
         w = make_workload(CONFIG, device=dev, seed_offset=rank * 1000 + l, poison=False)
         ksum = torch.zeros(w.num_pages, w.Hkv, w.d, dtype=torch.float32, device=dev)
@@ -295,12 +328,23 @@ def run_kap(args, world, rank, local):
         kap.kap_build_summaries(pool, kap.PageMap(w.block_table, w.ctx_len, w.seq_len0))
         a, r, k = (int(x) for x in w.ark[0].tolist())
         pol = kap.AccessPolicy(a, r, k, True, w.sel_cap())
+        if out_arena is None:
+            probe = kap.DecodeCycle(pool, w.block_table, w.ctx_len, w.seq_len0, w.k_prop, w.n_q,
+                                    kap.rope_inv_freq(w.d, w.theta, dev), policy=pol, fused=not args.unfused)
+            out_arena = Arena([(n, sh, dt) for n, (sh, dt) in probe.output_shapes().items()], L, dev)
+            del probe
         cyc = kap.DecodeCycle(pool, w.block_table, w.ctx_len, w.seq_len0, w.k_prop, w.n_q,
-                              kap.rope_inv_freq(w.d, w.theta, dev), policy=pol, fused=not args.unfused)
-        ins = dict(q_route=w.q_route.clone(), q_prop=w.q_prop.clone(), k_prop=w.k_new_prop.clone(),
-                   v_prop=w.v_new_prop.clone(), q_ver=w.q_ver.clone(), k_ver=w.k_new_ver.clone(),
-                   v_ver=w.v_new_ver.clone())
+                              kap.rope_inv_freq(w.d, w.theta, dev), policy=pol, fused=not args.unfused,
+                              outputs=out_arena.views(l))
+        ins = dict(q_route=w.q_route, q_prop=w.q_prop, k_prop=w.k_new_prop, v_prop=w.v_new_prop, q_ver=w.q_ver,
+                   k_ver=w.k_new_ver, v_ver=w.v_new_ver)
         layers.append((w, cyc, ins))
+    in_arena = Arena([(n, tuple(t.shape), t.dtype) for n, t in layers[0][2].items()], L, dev)
+    for l, (_, _, x) in enumerate(layers):
+        views = in_arena.views(l)
+        for n in list(x):
+            views[n].copy_(x[n])
+            x[n] = views[n]
     k_prop = layers[0][0].k_prop
 
     phases = [("plan", lambda: [c.plan(x["q_route"]) for _, c, x in layers])]
@@ -389,23 +433,17 @@ def run_kap(args, world, rank, local):
     # end to end: inputs from pinned host memory, results back, through the same calls
     e2e = None
     if not args.no_e2e:
-        host_in = []
-        for _, _, x in layers:
-            host_in.append({k2: v.detach().cpu().pin_memory() for k2, v in x.items()})
-        outs = [(c.o_prop, c.lse_prop, c.o_ver, c.lse_ver) for _, c, _ in layers]
-        host_out = [tuple(torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in o) for o in outs]
-        h2d = sum(v.numel() * v.element_size() for d_ in host_in for v in d_.values())
-        d2h = sum(t.numel() * t.element_size() for o in outs for t in o)
+        # every layer's inputs from one pinned host buffer, every output back into another: one copy each way
+        host_in = in_arena.buf.cpu().pin_memory()
+        host_out = torch.empty(out_arena.buf.shape, dtype=torch.uint8, pin_memory=True)
+        h2d = host_in.numel()
+        d2h = host_out.numel()
         n_e2e = max(3, min(K, 50))
 
         def e2e_step():
-            for (_, _, x), hx in zip(layers, host_in):
-                for k2, v in x.items():
-                    v.copy_(hx[k2], non_blocking=True)
+            in_arena.buf.copy_(host_in, non_blocking=True)
             replay_step()
-            for o, ho in zip(outs, host_out):
-                for t, ht in zip(o, ho):
-                    ht.copy_(t, non_blocking=True)
+            host_out.copy_(out_arena.buf, non_blocking=True)
             torch.cuda.current_stream().synchronize()
         for _ in range(2):
             e2e_step()

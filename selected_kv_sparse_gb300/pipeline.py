@@ -22,7 +22,8 @@ class DecodeCycle:
     def __init__(self, pool: kb.KVPool, block_table: torch.Tensor, ctx_len: torch.Tensor, seq_len0: torch.Tensor,
                  k_prop: int, n_q: torch.Tensor, inv_freq: torch.Tensor, policy: Optional[kb.AccessPolicy] = None,
                  spans: Optional[torch.Tensor] = None, span_offsets: Optional[torch.Tensor] = None,
-                 sel_cap: Optional[int] = None, s_max: float = 1.0, fused: bool = True):
+                 sel_cap: Optional[int] = None, s_max: float = 1.0, fused: bool = True,
+                 outputs: Optional[dict] = None):
         dev = block_table.device
         self.fused = bool(fused)
         self.pool = pool
@@ -75,12 +76,24 @@ class DecodeCycle:
         self.ws_score = kb.workspace(kb.kap_score_workspace_size(self.R, self.rows, mp), dev)
         self.ws_prop = kb.workspace(kb.kap_propose_workspace_size(self.R, self.Hkv, self.Hq, self.d), dev)
         self.ws_ver = kb.workspace(kb.kap_verify_workspace_size(self.R, self.Hkv, self.Hq, self.d, self.max_q), dev)
-        # outputs
-        dt = pool.dtype
-        self.o_prop = torch.empty(self.k_prop, self.R, self.Hq, self.d, dtype=dt, device=dev)
-        self.lse_prop = torch.empty(self.k_prop, self.R, self.Hq, dtype=torch.float32, device=dev)
-        self.o_ver = torch.empty(self.total_q, self.Hq, self.d, dtype=dt, device=dev)
-        self.lse_ver = torch.empty(self.total_q, self.Hq, dtype=torch.float32, device=dev)
+        # outputs (caller-provided tensors of these shapes may be passed in `outputs`, e.g. views of one buffer)
+        shapes = self.output_shapes()
+        outputs = outputs or {}
+        for name, (shape, odt) in shapes.items():
+            t = outputs.get(name)
+            if t is None:
+                t = torch.empty(shape, dtype=odt, device=dev)
+            elif tuple(t.shape) != tuple(shape) or t.dtype != odt or not t.is_contiguous():
+                raise ValueError(f"output {name} must be a contiguous {odt} tensor of shape {tuple(shape)}")
+            setattr(self, name, t)
+
+    def output_shapes(self) -> dict:
+        """Shapes and dtypes of the cycle's outputs: proposal outputs and LSEs per step, verify outputs and LSEs."""
+        dt = self.pool.dtype
+        return {"o_prop": ((self.k_prop, self.R, self.Hq, self.d), dt),
+                "lse_prop": ((self.k_prop, self.R, self.Hq), torch.float32),
+                "o_ver": ((self.total_q, self.Hq, self.d), dt),
+                "lse_ver": ((self.total_q, self.Hq), torch.float32)}
 
     # -------------------------------------------------------------------------------------------------- phases
     def plan(self, q_route: torch.Tensor, stream=None):
