@@ -137,18 +137,18 @@ __device__ __forceinline__ int ld_acquire_shared(const int *p) {
 }
 
 // Waits until ring entry kk (this CTA's entry index) has landed in its slot. Warp groups consume the ring out of
-// order, so the slot's previous occupant (entry kk - SLOTS) may not have landed yet, and the full barrier's phase
-// parity alone cannot tell the two apart: first wait for the producer to stamp the slot with kk (it does so only
-// after the previous occupant was consumed), then for the barrier phase. Both waits are bounded.
+// order, so the slot's barrier may still be a phase (or more) behind: a parity wait can then return for an earlier
+// phase. The producer stamps the slot with kk before the phase of kk can complete, so after each completed wait the
+// stamp tells whether the phase was ours; if not, wait for the other parity (the pending earlier phase) and retry.
+// All waits suspend in hardware and are bounded.
 __device__ __forceinline__ bool wait_entry(const int *stamp, uint64_t *full, int kk, uint32_t parity, int *err) {
-  for (uint32_t i = 0; ld_acquire_shared(stamp) != kk; ++i) {
-    if (i == kWaitPolls) {
-      set_error(err, kErrTimeout);
-      return false;
-    }
-    __nanosleep(32);
+  for (int attempt = 0; attempt < 8; ++attempt) {
+    if (!mbar_wait(full, parity, err)) return false;
+    if (ld_acquire_shared(stamp) == kk) return true;
+    if (!mbar_wait(full, parity ^ 1u, err)) return false;
   }
-  return mbar_wait(full, parity, err);
+  set_error(err, kErrTimeout);
+  return false;
 }
 
 // Inverse frequencies of the EPL consecutive rotary pairs starting at pair index i0 (a multiple of EPL).
