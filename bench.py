@@ -45,6 +45,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--unfused", action="store_true", help="separate KV-append and proposal launches per step")
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="proposal kernels wait for the previous kernel before reading their view")
     ap.add_argument("--clock-log", default=None, help="CSV file for the nvidia-smi samples of the timed region")
     return ap.parse_args(argv)
 
@@ -335,7 +337,7 @@ def run_kap(args, world, rank, local):
             del probe
         cyc = kap.DecodeCycle(pool, w.block_table, w.ctx_len, w.seq_len0, w.k_prop, w.n_q,
                               kap.rope_inv_freq(w.d, w.theta, dev), policy=pol, fused=not args.unfused,
-                              outputs=out_arena.views(l))
+                              outputs=out_arena.views(l), overlap=not args.no_overlap)
         ins = dict(q_route=w.q_route, q_prop=w.q_prop, k_prop=w.k_new_prop, v_prop=w.v_new_prop, q_ver=w.q_ver,
                    k_ver=w.k_new_ver, v_ver=w.v_new_ver)
         layers.append((w, cyc, ins))
@@ -347,15 +349,19 @@ def run_kap(args, world, rank, local):
             x[n] = views[n]
     k_prop = layers[0][0].k_prop
 
+    # Each phase runs every layer's call and is replayed as its own CUDA graph, so the plan graph that wrote the
+    # views has completed before any proposal launch, and within a proposal graph the kernel ahead of a layer's
+    # launch belongs to another layer: every proposal call may treat its view as settled.
+    st = None if args.no_overlap else True
     phases = [("plan", lambda: [c.plan(x["q_route"]) for _, c, x in layers])]
     for i in range(k_prop):
         if args.unfused:
             phases.append((f"app{i}", lambda i=i: [c.append_step(i, x["q_prop"][i], x["k_prop"][i], x["v_prop"][i])
                                                     for _, c, x in layers]))
-            phases.append((f"prop{i}", lambda i=i: [c.propose(i, x["q_prop"][i]) for _, c, x in layers]))
+            phases.append((f"prop{i}", lambda i=i: [c.propose(i, x["q_prop"][i], settled=st) for _, c, x in layers]))
         else:   # the step's KV append runs inside the proposal kernel
-            phases.append((f"prop{i}", lambda i=i: [c.propose_step(i, x["q_prop"][i], x["k_prop"][i], x["v_prop"][i])
-                                                    for _, c, x in layers]))
+            phases.append((f"prop{i}", lambda i=i: [c.propose_step(i, x["q_prop"][i], x["k_prop"][i], x["v_prop"][i],
+                                                                   settled=st) for _, c, x in layers]))
     phases.append(("vapp", lambda: [c.append_window(x["q_ver"], x["k_ver"], x["v_ver"]) for _, c, x in layers]))
     phases.append(("ver", lambda: [c.verify(x["q_ver"]) for _, c, x in layers]))
 
@@ -484,6 +490,8 @@ def run_kap(args, world, rank, local):
             "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
             "config": {"workload": WORKLOAD, "layers_per_step": L, "parallelism": "replicas" if world > 1 else "1 GPU",
+                       "calls": "separate" if args.unfused else "fused",
+                       "proposal_overlap": not args.no_overlap,
                        "l2": f"inputs larger than L2: {ws_bytes / 2**30:.1f} GiB of KV per rank, "
                              f"{b_step / 2**30:.2f} GiB read per step"},
             "pct_of_hbm_roofline": 100.0 * value / (hbm_peak * world),

@@ -52,7 +52,8 @@ class _Policy(ctypes.Structure):
 
 class _View(ctypes.Structure):
     _fields_ = [("rows_per_seq", ctypes.c_int32), ("cap", ctypes.c_int32), ("block_table", ctypes.c_void_p),
-                ("logical_page", ctypes.c_void_p), ("n_entries", ctypes.c_void_p), ("n_selected", ctypes.c_void_p)]
+                ("logical_page", ctypes.c_void_p), ("n_entries", ctypes.c_void_p), ("n_selected", ctypes.c_void_p),
+                ("settled", ctypes.c_int32)]
 
 
 class _Verify(ctypes.Structure):
@@ -217,10 +218,10 @@ class View:
         return View(rows_per_seq, cap, z(R, rows_per_seq, cap), z(R, rows_per_seq, cap), z(R, rows_per_seq),
                     z(R, rows_per_seq))
 
-    def _c(self) -> _View:
+    def _c(self, settled: bool = False) -> _View:
         return _View(self.rows_per_seq, self.cap, _i32(self.block_table, "view.block_table"),
                      _i32(self.logical_page, "view.logical_page"), _i32(self.n_entries, "view.n_entries"),
-                     _i32(self.n_selected, "view.n_selected"))
+                     _i32(self.n_selected, "view.n_selected"), int(bool(settled)))
 
 
 @dataclass
@@ -338,11 +339,13 @@ def kap_propose_workspace_size(R: int, hkv: int, hq: int, d: int) -> int:
 
 
 def kap_attn_propose(pool: KVPool, pmap: PageMap, view: View, q: torch.Tensor, out: torch.Tensor, lse: torch.Tensor,
-                     workspace: torch.Tensor, stream=None):
+                     workspace: torch.Tensor, stream=None, settled: bool = False):
+    """settled: the caller's promise that the view, the page map and the prompt tokens were written before the
+    kernel launched just ahead of this call on the stream (kap_view.settled)."""
     lib = load()
     if q.dtype != pool.dtype or out.dtype != pool.dtype or lse.dtype != torch.float32:
         raise TypeError("q/out must have the pool dtype and lse fp32")
-    p, m, v = pool._c(), pmap._c(), view._c()
+    p, m, v = pool._c(), pmap._c(), view._c(settled)
     _check("kap_attn_propose", lib.kap_attn_propose(ctypes.byref(p), ctypes.byref(m), ctypes.byref(v), _ptr(q),
                                                     _ptr(out), _ptr(lse), _ptr(workspace),
                                                     workspace.numel() * workspace.element_size(), _stream(stream)))
@@ -350,15 +353,15 @@ def kap_attn_propose(pool: KVPool, pmap: PageMap, view: View, q: torch.Tensor, o
 
 def kap_append_propose(pool: KVPool, pmap: PageMap, view: View, q: torch.Tensor, k_new: torch.Tensor,
                        v_new: torch.Tensor, inv_freq: torch.Tensor, out: torch.Tensor, lse: torch.Tensor,
-                       workspace: torch.Tensor, stream=None):
+                       workspace: torch.Tensor, stream=None, settled: bool = False):
     """One proposal step with the step token's KV append fused in: the token of request r sits at seq_len[r]-1;
-    q holds the step's queries before RoPE (read only)."""
+    q holds the step's queries before RoPE (read only). settled: as for kap_attn_propose."""
     lib = load()
     if any(t.dtype != pool.dtype for t in (q, k_new, v_new, out)) or lse.dtype != torch.float32:
         raise TypeError("q, k_new, v_new and out must have the pool dtype and lse fp32")
     if inv_freq.dtype != torch.float32:
         raise TypeError("inv_freq must be fp32")
-    p, m, v = pool._c(), pmap._c(), view._c()
+    p, m, v = pool._c(), pmap._c(), view._c(settled)
     _check("kap_append_propose", lib.kap_append_propose(ctypes.byref(p), ctypes.byref(m), ctypes.byref(v), _ptr(q),
                                                         _ptr(k_new), _ptr(v_new), _ptr(inv_freq), _ptr(out),
                                                         _ptr(lse), _ptr(workspace),

@@ -101,6 +101,7 @@ struct Params {
   int *err;
   const void *k_new, *v_new;  // fused append: [R][Hkv][D] step-token keys (before RoPE) and values, or null
   const float *inv_freq;      // [D/2]
+  int settled;                // view, lengths and prompt tokens predate the previous kernel on the stream
 };
 
 // One row segment of a window: global entries [b, e) of attention row `row` (whose own range is [rb, re)),
@@ -232,7 +233,9 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
     fence_barrier_init();
   }
   if (tid < C::SLOTS) smeta[tid].w = -1;  // no entry issued yet (shared memory keeps an earlier launch's stamps)
-  grid_dependency_sync();
+  // A settled view lets the row scan, the segment tables and the copies of pure prompt pages run while the previous
+  // kernel finishes; everything else waits for it (consumers below, the producer at its first other entry).
+  if (!p.settled) grid_dependency_sync();
   const bool small_rows = p.nrows <= kMaxRowsScan;
   if (small_rows) {
     const int per = (p.nrows + kThreads - 1) / kThreads;  // thread t owns rows [t*per, (t+1)*per)
@@ -268,7 +271,10 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
   const int64_t E = s_total;
   // Split over nb <= E CTAs so that every participating CTA owns at least one entry (the merge counts them).
   const int nb = static_cast<int>(E < static_cast<int64_t>(gridDim.x) ? E : static_cast<int64_t>(gridDim.x));
-  if (E == 0 || static_cast<int>(blockIdx.x) >= nb) return;
+  if (E == 0 || static_cast<int>(blockIdx.x) >= nb) {
+    if (p.settled) grid_dependency_sync();  // an idle CTA still orders its dependents after the previous kernel
+    return;
+  }
   const int64_t cta_begin = static_cast<int64_t>(blockIdx.x) * E / nb;
   const int64_t cta_end = static_cast<int64_t>(blockIdx.x + 1) * E / nb;
 
@@ -314,6 +320,10 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
   const float qscale = rsqrtf(static_cast<float>(D)) * kLog2e;
   int w_row = s_row0;
   int64_t w_rb = s_rb0;
+  // With a settled view the dependency wait comes later: consumers take it before their first read of q (after the
+  // first window's segment table, so that the producer's copies are not held at that barrier), the producer before
+  // its first entry that is not pure prompt.
+  bool waited = !p.settled;
 
   for (int64_t cur = cta_begin; cur < cta_end;) {
     if (warp == kNCW) {
@@ -377,6 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
 
     if (warp == kNCW) {
       // ============================================================================================== producer
+      const uint64_t pol = l2_evict_first_policy();  // the selected pages are streamed once per launch
       for (int si = 0; si < nseg; ++si) {
         const Seg sg = segs[si];
         const int r = sg.row / p.hkv, h = sg.row - r * p.hkv;
@@ -384,19 +395,29 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
         const int rn = static_cast<int>(sg.re - sg.rb);
         for (int64_t e0 = sg.b; e0 < sg.e; e0 += C::BATCH) {
           const int64_t e = e0 + lane;
-          if (lane < C::BATCH && e < sg.e) {
-            const int i = static_cast<int>(e - sg.rb);  // entry index within the row's view
+          const bool act = lane < C::BATCH && e < sg.e;
+          int i = 0, page = 0, base = 0, tlo = 0, thi = 0;
+          if (act) {
+            i = static_cast<int>(e - sg.rb);  // entry index within the row's view
             const size_t o = static_cast<size_t>(sg.vr) * p.vcap + i;
             const int lp = p.vlp[o];
-            const int page = p.vbt[o];
-            const int base = lp * kPage;
-            int thi = min(kPage, S - base);
-            int tlo = (i < nsel) ? 0 : max(0, L - base);
+            page = p.vbt[o];
+            base = lp * kPage;
+            thi = min(kPage, S - base);
+            tlo = (i < nsel) ? 0 : max(0, L - base);
             if (thi > tlo && (page < 0 || page >= p.num_pages)) {
               set_error(p.err, kErrPage);
               tlo = thi = 0;
             }
             if (thi <= tlo) tlo = thi = 0;
+          }
+          // Before the dependency wait only pages whose visible tokens are all prompt tokens are copied: a later
+          // position of a page (a generated token) may have been written by the previous kernel.
+          if (!waited && __any_sync(0xffffffffu, act && thi > tlo && base + thi > L)) {
+            grid_dependency_wait();
+            waited = true;
+          }
+          if (act) {
             int step_tok = -1;
             if (fused) {
               const int tk = S - 1 - base;
@@ -410,8 +431,8 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
             if (thi > tlo) {
               const size_t off = (static_cast<size_t>(page) * p.hkv + h) * kPage * D;
               mbar_arrive_expect_tx(&full[slot], 2 * C::CHUNK);
-              bulk_g2s(kv + slot * C::SLOT, Kp + off, C::CHUNK, &full[slot]);
-              bulk_g2s(kv + slot * C::SLOT + C::CHUNK, Vp + off, C::CHUNK, &full[slot]);
+              bulk_g2s_stream(kv + slot * C::SLOT, Kp + off, C::CHUNK, &full[slot], pol);
+              bulk_g2s_stream(kv + slot * C::SLOT + C::CHUNK, Vp + off, C::CHUNK, &full[slot], pol);
             } else {
               mbar_arrive(&full[slot]);
             }
@@ -432,14 +453,20 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
       float m_run[G], l_own[C::VPL];
       const int P = fused ? p.seq_len[r] - 1 : 0;  // position of the step token (fused append)
       {
+        // The rotary factors depend only on the page map and the frequencies, which a settled view covers, so they
+        // are formed before the dependency wait; q is read after it.
+        float cs[C::EPL], sn[C::EPL];  // the same angles for every head of the group
+        if (fused) rope_lane_factors<C::EPL, D>(base_dim, P, p.inv_freq, cs, sn);
+        if (!waited) {
+          grid_dependency_sync();  // before q, the step token, outputs and the workspace
+          waited = true;
+        }
         const T *qrow = static_cast<const T *>(p.q) + (static_cast<size_t>(r) * p.hq + h * G) * D + base_dim;
         uint4 qraw[G];
         const int pg = C::XPERM ? (((lane % C::LPT) * C::VPL) & (G - 1)) : 0;  // register g holds head g ^ pg
 #pragma unroll
         for (int g = 0; g < G; ++g)
           qraw[g] = *reinterpret_cast<const uint4 *>(qrow + static_cast<size_t>(g ^ pg) * D);
-        float cs[C::EPL], sn[C::EPL];  // the same angles for every head of the group
-        if (fused) rope_lane_factors<C::EPL, D>(base_dim, P, p.inv_freq, cs, sn);
 #pragma unroll
         for (int g = 0; g < G; ++g) {
           float tmp[C::EPL];
@@ -466,11 +493,11 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
         tok_own[k] = j * C::TPI + ts;
         ok_own[k] = v < C::NI * G;
       }
-      for (int64_t e = sg.b + gw; e < sg.e; e += nw) {
-        const int64_t kk = e - cta_begin;
-        const int slot = static_cast<int>(kk % C::SLOTS);
-        wait_entry(&smeta[slot].w, &full[slot], static_cast<int>(kk), static_cast<uint32_t>(kk / C::SLOTS) & 1u,
-                   p.err);
+      // this warp's entries: kk = kk0, kk0 + nw, ... (CTA-local indices, fewer than 2^31), slot kk % SLOTS
+      const int kk0 = static_cast<int>(sg.b - cta_begin) + gw, kk_end = static_cast<int>(sg.e - cta_begin);
+      for (int kk = kk0; kk < kk_end; kk += nw) {
+        const int slot = kk % C::SLOTS;
+        wait_entry(&smeta[slot].w, &full[slot], kk, static_cast<uint32_t>(kk / C::SLOTS) & 1u, p.err);
         const int4 mt = smeta[slot];
         const int tlo = mt.x & 0xffff, thi = mt.x >> 16;
         unsigned char *kb = kv + slot * C::SLOT;
@@ -854,6 +881,7 @@ cudaError_t launch_propose(const PoolArgs &pa, const MapArgs &ma, const ViewArgs
   prm.k_new = k_new;
   prm.v_new = v_new;
   prm.inv_freq = inv_freq;
+  prm.settled = va.settled;
   if (pa.dtype == 0 && pa.d == 128) return launch_td<__nv_bfloat16, 128>(prm, G, s);
   if (pa.dtype == 0 && pa.d == 64) return launch_td<__nv_bfloat16, 64>(prm, G, s);
   if (pa.dtype == 1 && pa.d == 128) return launch_td<float, 128>(prm, G, s);

@@ -233,6 +233,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // Warp 4 issues the K boxes of each tile (and writes the tile metadata and the Q operand), warp 6 the V
     // boxes: both walk the same tile sequence, so their 16 TMA requests per tile are issued in parallel.
     const bool kprod = (warp == 4);
+    const uint64_t pol = l2_evict_first_policy();  // the full KV is streamed once per launch
     int pr_row = s_row0, seg = -1;
     int64_t pr_rb = s_rb0, pr_re = s_re0, pr_cur = cta_begin;
     int row_r = -1, row_kvp = 0, row_nq_ = 0, row_qpos0 = 0, row_qoff = 0;
@@ -343,8 +344,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (ok) {
           unsigned char *vd = Vs + st * kStageBytes;
           const int row0 = (pl_page * p.hkv + pl_h) * kPage;
-          tma_load_2d(vd + lane * 2048, &tmV, 0, row0, &vfull[st]);
-          tma_load_2d(vd + kHalfBytes + lane * 2048, &tmV, 64, row0, &vfull[st]);
+          tma_load_2d_stream(vd + lane * 2048, &tmV, 0, row0, &vfull[st], pol);
+          tma_load_2d_stream(vd + kHalfBytes + lane * 2048, &tmV, 64, row0, &vfull[st], pol);
         }
         plan();
         continue;
@@ -369,8 +370,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (ok) {
         unsigned char *kd = Ks + st * kStageBytes;
         const int row0 = (pl_page * p.hkv + pl_h) * kPage;
-        tma_load_2d(kd + lane * 2048, &tmK, 0, row0, &kfull[st]);
-        tma_load_2d(kd + kHalfBytes + lane * 2048, &tmK, 64, row0, &kfull[st]);
+        tma_load_2d_stream(kd + lane * 2048, &tmK, 0, row0, &kfull[st], pol);
+        tma_load_2d_stream(kd + kHalfBytes + lane * 2048, &tmK, 64, row0, &kfull[st], pol);
       }
       plan();
     }

@@ -258,6 +258,7 @@ kap_status propose_common(const kap_kv_pool *pool, const kap_page_map *map, cons
   va.lp = view->logical_page;
   va.n_entries = view->n_entries;
   va.n_selected = view->n_selected;
+  va.settled = view->settled != 0;
   return cuda_status(launch_propose(pool_args(pool), map_args(map), va, q_dev, out, lse, workspace, workspace_bytes,
                                     k_new, v_new, inv_freq_dev, error_word(), cs(stream)));
 }

@@ -25,11 +25,17 @@ __device__ __forceinline__ void set_error(int *err, int bit) {
 
 // ------------------------------------------------------------------------------- dependent launches
 // Every kernel of the library is launched with programmatic stream serialization: its CTAs may start while the
-// previous kernel in the stream drains. Each kernel therefore lets its own dependent start early and then waits,
-// before its first global memory access, until the previous kernel has completed and its writes are visible.
-__device__ __forceinline__ void grid_dependency_sync() {
+// previous kernel in the stream drains. A kernel waits, before it touches memory that the previous kernel may
+// write, until that kernel has completed and its writes are visible, and only then lets its own dependent start.
+// Triggering after the wait keeps a chain transitive: when a kernel starts, the kernel two places ahead of it has
+// completed, so a prologue may read data that is known to be older than its immediate predecessor.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_sync() {
+  grid_dependency_wait();
+  grid_launch_dependents();
 }
 
 template <class... KArgs, class... Args>
@@ -203,6 +209,30 @@ __device__ __forceinline__ void tma_load_2d(void *dst_smem, const void *tmap, in
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
           "r"(smem_u32(dst_smem)),
       "l"(tmap), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// L2 policy for data that is streamed once: its lines are the first evicted, so the small metadata, queries and
+// outputs that the next kernels read stay resident in L2 while gigabytes of KV pass through it.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void bulk_g2s_stream(void *dst_smem, const void *src_gmem, uint32_t bytes, uint64_t *bar,
+                                                uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+          "r"(smem_u32(dst_smem)),
+      "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_2d_stream(void *dst_smem, const void *tmap, int c0, int c1, uint64_t *bar,
+                                                   uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst_smem)),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(pol)
       : "memory");
 }
 

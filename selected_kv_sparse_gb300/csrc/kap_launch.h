@@ -21,6 +21,7 @@ struct MapArgs {
 struct ViewArgs {
   int rows_per_seq, cap;
   const int32_t *bt, *lp, *n_entries, *n_selected;
+  int settled;  // the view, lengths and prompt tokens predate the previous kernel on the stream
 };
 
 // selection kernels (k_select.cu)

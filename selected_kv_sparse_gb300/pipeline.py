@@ -6,6 +6,11 @@ over the compact view, in one fused call (kap_append_propose) or as kap_append_k
 appends the window's KV into the full-context slots and runs causal q = n attention over the full block table.
 Every buffer is allocated here, once; the calls themselves allocate nothing, so a cycle can be captured in a CUDA
 graph.
+
+With overlap (the default), a proposal call that does not directly follow the plan marks the view as settled: its
+kernel then scans the view and starts streaming the selected prompt pages while the previous kernel finishes. The
+cycle tracks its own launches for this; a caller that launches kernels writing the view, the page map or prompt
+tokens on the same stream between the cycle's calls must pass overlap=False.
 """
 from __future__ import annotations
 
@@ -23,9 +28,11 @@ class DecodeCycle:
                  k_prop: int, n_q: torch.Tensor, inv_freq: torch.Tensor, policy: Optional[kb.AccessPolicy] = None,
                  spans: Optional[torch.Tensor] = None, span_offsets: Optional[torch.Tensor] = None,
                  sel_cap: Optional[int] = None, s_max: float = 1.0, fused: bool = True,
-                 outputs: Optional[dict] = None):
+                 outputs: Optional[dict] = None, overlap: bool = True):
         dev = block_table.device
         self.fused = bool(fused)
+        self.overlap = bool(overlap)
+        self._view_fresh = True  # the last launch of this cycle wrote the view (or none has run yet)
         self.pool = pool
         self.R = int(block_table.shape[0])
         self.Hq = pool.num_q_heads
@@ -114,36 +121,50 @@ class DecodeCycle:
                                 self.s_max, self.slots_prop, self.pos_prop, stream)
         if not self.window_is_horizon:
             kb.kap_slot_mapping(self.map_plan, self.q_offsets, self.q_start, self.slots_ver, self.pos_ver, stream)
+        self._view_fresh = True
+
+    def _settled(self, override: Optional[bool]) -> bool:
+        """Whether the next launch may treat the view as settled (override: the caller knows its launch order); the
+        launch itself makes the view settled for the one after."""
+        s = (self.overlap and not self._view_fresh) if override is None else bool(override)
+        self._view_fresh = False
+        return s
 
     def append_step(self, i: int, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
         """Proposal step i, first half: the step token's KV at its logical position (q rotated in place)."""
         kb.kap_append_kv(self.pool, k_new, v_new, q, self.pos_prop[i:], self.slots_prop[i:], self.inv_freq,
                          num_tokens=self.R, tok_stride=self.horizon, stream=stream)
+        self._view_fresh = False
 
-    def propose(self, i: int, q: torch.Tensor, stream=None):
+    def propose(self, i: int, q: torch.Tensor, stream=None, settled: Optional[bool] = None):
         """Proposal step i, second half: q = 1 attention over the compact view."""
         kb.kap_attn_propose(self.pool, self.map_steps[i], self.view, q, self.o_prop[i], self.lse_prop[i], self.ws_prop,
-                            stream)
+                            stream, settled=self._settled(settled))
 
-    def propose_step(self, i: int, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
+    def propose_step(self, i: int, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, stream=None,
+                     settled: Optional[bool] = None):
         """Proposal step i: append the step token's KV and attend. Fused, q is read before RoPE and left as it is;
-        unfused, kap_append_kv rotates q in place first."""
+        unfused, kap_append_kv rotates q in place first. settled: None decides from this cycle's own launches; True
+        is the caller's promise that the kernel launched just ahead of this one did not write the view, the page
+        map or prompt tokens."""
         if self.fused:
             kb.kap_append_propose(self.pool, self.map_steps[i], self.view, q, k_new, v_new, self.inv_freq,
-                                  self.o_prop[i], self.lse_prop[i], self.ws_prop, stream)
+                                  self.o_prop[i], self.lse_prop[i], self.ws_prop, stream, settled=self._settled(settled))
         else:
             self.append_step(i, q, k_new, v_new, stream)
-            self.propose(i, q, stream)
+            self.propose(i, q, stream, settled)
 
     def append_window(self, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
         """The verify window's KV into the full-context slots (q rotated in place)."""
         kb.kap_append_kv(self.pool, k_new, v_new, q, self.pos_ver, self.slots_ver, self.inv_freq, stream=stream)
+        self._view_fresh = False
 
     def verify(self, q: torch.Tensor, k_new: torch.Tensor = None, v_new: torch.Tensor = None, stream=None):
         """Causal attention of the window over the full table (after append_window when k_new/v_new are given)."""
         if k_new is not None:
             self.append_window(q, k_new, v_new, stream)
         kb.kap_attn_verify(self.pool, self.map_full, self.vpol, q, self.o_ver, self.lse_ver, self.ws_ver, stream)
+        self._view_fresh = False
 
     def run(self, q_route, q_prop, k_new_prop, v_new_prop, q_ver, k_new_ver, v_new_ver, stream=None):
         self.plan(q_route, stream)

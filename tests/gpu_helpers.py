@@ -32,12 +32,12 @@ def policy_of(w, cap=None):
     return kap.AccessPolicy(a, r, k, w.per_kv_head, cap, None if same else w.ark.contiguous())
 
 
-def make_cycle(w, cap=None, fused=True):
+def make_cycle(w, cap=None, fused=True, overlap=True):
     pool = kap.KVPool(w.K, w.V, w.Hq, torch.zeros(w.num_pages, w.Hkv, w.d, dtype=torch.float32, device=w.K.device))
     inv = kap.rope_inv_freq(w.d, w.theta, w.K.device)
     pol = policy_of(w, cap)
     cyc = kap.DecodeCycle(pool, w.block_table, w.ctx_len, w.seq_len0, w.k_prop, w.n_q, inv, policy=pol,
-                          spans=w.spans, span_offsets=w.span_offsets, sel_cap=pol.cap, fused=fused)
+                          spans=w.spans, span_offsets=w.span_offsets, sel_cap=pol.cap, fused=fused, overlap=overlap)
     return pool, cyc
 
 

@@ -80,3 +80,32 @@ def test_long_spans_recipe():
     for (a0, n0), (a1, _) in zip(pages, pages[1:]):
         assert a0 + n0 < a1          # non-overlapping and non-adjacent
     assert pages[0][0] >= 1 and pages[-1][0] + pages[-1][1] <= 8188
+
+
+def test_binding_structs_match_the_header(tmp_path):
+    """The binding's ctypes mirrors of the header's structs: same size and the same offset for every field, as a C
+    compiler lays them out from include/kap.h."""
+    import shutil
+    import subprocess
+    from selected_kv_sparse_gb300 import _binding as kb
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    mirrors = {"kap_kv_pool": kb._Pool, "kap_page_map": kb._Map, "kap_access_policy": kb._Policy,
+               "kap_view": kb._View, "kap_verify_policy": kb._Verify}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "kap.h"', "int main(void) {"]
+    for cname, py in mirrors.items():
+        lines.append(f'  printf("{cname} size %zu\\n", sizeof({cname}));')
+        for fname, _ in py._fields_:
+            lines.append(f'  printf("{cname} {fname} %zu\\n", offsetof({cname}, {fname}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    got = {tuple(l.split()[:2]): int(l.split()[2]) for l in out if l.strip()}
+    for cname, py in mirrors.items():
+        assert got[(cname, "size")] == ctypes.sizeof(py), cname
+        for fname, _ in py._fields_:
+            assert got[(cname, fname)] == getattr(py, fname).offset, (cname, fname)

@@ -8,6 +8,9 @@ kap_attn_propose produces:
 - the pool contents after the step, bit for bit;
 - the attention outputs and LSEs, to within 1e-6 in fp32 or one bf16 rounding step. The fused kernel rotates q in
   the same arithmetic, but its warps may merge a split row in a different order.
+
+A proposal launch with a settled view (kap_view.settled: scan and prompt-page copies start before the dependency
+wait) must produce exactly what the same launch produces when it waits first: only the timing differs.
 """
 import numpy as np
 import pytest
@@ -83,4 +86,29 @@ def test_append_propose_equals_append_then_propose(kap, case):
         atol = float(np.abs(u["o"].numpy()).max()) * 2.0 ** -7 + 1e-6
     assert torch.allclose(f["o"], u["o"], atol=atol, rtol=0)
     assert torch.allclose(f["lse"], u["lse"], atol=1e-5, rtol=0)
+    assert kap.kap_device_error() == 0
+
+
+@pytest.mark.parametrize("fused", [True, False], ids=["fused", "separate"])
+@pytest.mark.parametrize("case", CASES, ids=_id)
+def test_settled_view_changes_nothing(kap, case, fused):
+    from tests.gpu_helpers import make_cycle
+    from workloads import make_workload
+    res = []
+    for overlap in (True, False):
+        w = make_workload(device="cuda", **case)
+        pool, cyc = make_cycle(w, fused=fused, overlap=overlap)
+        kap.kap_build_summaries(pool, kap.PageMap(w.block_table, w.ctx_len, w.seq_len0))
+        cyc.plan(w.q_route)
+        torch.cuda.synchronize()  # the view is complete before the first proposal launch: every step may be settled
+        q = w.q_prop.clone()
+        for i in range(w.k_prop):
+            cyc.propose_step(i, q[i], w.k_new_prop[i], w.v_new_prop[i], settled=True if overlap else None)
+        torch.cuda.synchronize()
+        res.append(dict(o=cyc.o_prop.cpu(), lse=cyc.lse_prop.cpu(), K=w.K.cpu(), V=w.V.cpu()))
+    a, b = res
+    for k in ("o", "lse", "K", "V"):
+        nan = torch.isnan(a[k])
+        assert torch.equal(nan, torch.isnan(b[k])), k
+        assert torch.equal(a[k][~nan], b[k][~nan]), k
     assert kap.kap_device_error() == 0
