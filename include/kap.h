@@ -91,9 +91,9 @@ typedef struct {
   int32_t *n_entries;     /* [R][rows_per_seq] entries in use */
   int32_t *n_selected;    /* [R][rows_per_seq] leading entries that are selected prompt pages */
   /* Read by kap_attn_propose and kap_append_propose only; ignored (and left unchanged) by the calls that write a
-   * view. Nonzero is the caller's promise that this view, the page map and the prompt tokens of the pool
-   * (positions < ctx_len) were last written before the kernel launched just ahead of the call on the same
-   * stream. The call may then read them, and start streaming the selected prompt pages, while that kernel is
+   * view. Nonzero is the caller's promise that this view, the page map, the prompt tokens of the pool
+   * (positions < ctx_len) and the rotary frequencies were last written before the kernel launched just ahead of
+   * the call on the same stream. The call may then read them, and start streaming the selected prompt pages, while that kernel is
    * still finishing; it waits for it before reading anything else or writing anything. Zero: the call waits for
    * the previous kernel before its first memory access. The promise does not hold for a call that directly
    * follows the kernel that wrote the view. */

@@ -22,9 +22,9 @@
 //    (and the state rescaled) when a page exceeds it by more than 2^8, which is exact.
 //  * A group that has finished its segment combines its warps' states behind its own named barrier and writes the
 //    row's output, or hands a partial record to the row's last CTA, while the other groups keep streaming.
-//  * Fused append: the step token of request r sits at position P = seq_len[r] - 1. Every warp rotates its copy of
-//    the query at P; the warp that consumes the page holding P rotates the token's key, writes K and V into the
-//    pool and patches its shared-memory copy of the page before using it.
+//  * Fused append: the step token of request r sits at position P = seq_len[r] - 1. Every warp loads the token's
+//    key and value with its query and rotates both key and query at P; the warp that consumes the page holding P
+//    writes K and V into the pool and patches its shared-memory copy of the page before using it.
 #include "kap_device.cuh"
 #include "kap_launch.h"
 
@@ -452,6 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
       float2 qf[G][C::EP2], o[G][C::EP2];
       float m_run[G], l_own[C::VPL];
       const int P = fused ? p.seq_len[r] - 1 : 0;  // position of the step token (fused append)
+      uint4 kw_step = make_uint4(0u, 0u, 0u, 0u), vw_step = kw_step;  // this row's step token, K rotated at P
       {
         // The rotary factors depend only on the page map and the frequencies, which a settled view covers, so they
         // are formed before the dependency wait; q is read after it.
@@ -467,6 +468,17 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
 #pragma unroll
         for (int g = 0; g < G; ++g)
           qraw[g] = *reinterpret_cast<const uint4 *>(qrow + static_cast<size_t>(g ^ pg) * D);
+        if (fused) {
+          // The step token's key and value travel with q, and its key turns by the same angles as q: the warp that
+          // meets the token's page only stores them.
+          const size_t src = (static_cast<size_t>(r) * p.hkv + h) * D + base_dim;
+          const uint4 kraw = *reinterpret_cast<const uint4 *>(static_cast<const T *>(p.k_new) + src);
+          vw_step = *reinterpret_cast<const uint4 *>(static_cast<const T *>(p.v_new) + src);
+          float kx[C::EPL];
+          Vec16<T>::unpack(kraw, kx);
+          rope_lane_apply<T, C::EPL, C::LPT, D>(kx, base_dim, cs, sn);
+          kw_step = Vec16<T>::pack(kx);
+        }
 #pragma unroll
         for (int g = 0; g < G; ++g) {
           float tmp[C::EPL];
@@ -504,15 +516,8 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
         if (mt.y >= 0) {
           // the step token of this row lies in this page: RoPE'd key and value into the pool and into this copy
           const int tok = mt.y;
-          const size_t src = (static_cast<size_t>(r) * p.hkv + h) * D + base_dim;
-          float kx[C::EPL];
-          Vec16<T>::unpack(*reinterpret_cast<const uint4 *>(static_cast<const T *>(p.k_new) + src), kx);
-          const uint4 vw = *reinterpret_cast<const uint4 *>(static_cast<const T *>(p.v_new) + src);
-          float kcs[C::EPL], ksn[C::EPL];
-          rope_lane_factors<C::EPL, D>(base_dim, P, p.inv_freq, kcs, ksn);
-          rope_lane_apply<T, C::EPL, C::LPT, D>(kx, base_dim, kcs, ksn);
           if (lane < C::LPT) {
-            const uint4 kw = Vec16<T>::pack(kx);
+            const uint4 kw = kw_step, vw = vw_step;
             const int rowb = (tok * D + base_dim) * C::ESZ;
             *reinterpret_cast<uint4 *>(kb + rowb) = kw;
             *reinterpret_cast<uint4 *>(kb + C::CHUNK + rowb) = vw;
