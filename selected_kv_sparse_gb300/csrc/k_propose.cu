@@ -35,7 +35,7 @@ constexpr int kNCW = 11;                     // consumer warps (12 warps in all:
 constexpr int kThreads = (kNCW + 1) * 32;    // + the producer warp (warp kNCW)
 constexpr int kMaxSlotsExtraCtas = 4096;     // bound on the grid, for workspace sizing
 constexpr int kMaxSeg = kNCW;                // row segments per window (each gets at least one warp)
-constexpr int kMaxRowsScan = 2048;           // rows whose entry offsets are scanned into shared memory at once
+constexpr int kMaxRowsScan = 512;            // rows whose entry offsets are scanned into shared memory at once
 constexpr int kBarSeg0 = 1;                  // named barriers kBarSeg0 .. kBarSeg0 + kMaxSeg - 1, one per segment
 constexpr int kMergeChunk = 8;               // partial records loaded at once by a merging CTA
 constexpr float kLog2e = 1.4426950408889634f;
@@ -69,7 +69,7 @@ struct Cfg {
   static constexpr int ROWB = (kMaxRowsScan + 1) * 4;     // per-row entry offsets (row scan)
   static constexpr int FIXED = COMB + WLOG + SWT + SEGB + ROWB + 1024;
   static constexpr int SLOT = 2 * CHUNK;                  // K and V of one entry
-  static constexpr int SLOTS_FIT = (200 * 1024 - FIXED) / (SLOT + 32);
+  static constexpr int SLOTS_FIT = (226 * 1024 - FIXED) / (SLOT + 32);  // 1 KiB left for static shared memory
   static constexpr int SLOTS = SLOTS_FIT > 32 ? 32 : SLOTS_FIT;
   static constexpr int BATCH = SLOTS < 16 ? SLOTS : 16;   // entries the producer handles per step
   static constexpr int OFF_KV = 0;
@@ -82,6 +82,7 @@ struct Cfg {
   static constexpr int OFF_ROWS = OFF_BAR + 2 * SLOTS * 8;
   static constexpr int SMEM = OFF_ROWS + ROWB;
   static_assert(SLOTS >= 4, "too few page slots");
+  static_assert(SMEM + 1024 <= 227 * 1024, "shared memory per CTA");
   static_assert(EPL % 2 == 0 && (D / 2) % EPL == 0, "vector layout");
 };
 

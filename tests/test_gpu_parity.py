@@ -18,6 +18,8 @@ CASES = [
     dict(name="early", scale=1 / 16, batch=3),
     dict(name="mixed", scale=1 / 32),
     dict(name="mixed", scale=1 / 32, ragged=True),
+    # 72 short requests: 576 attention rows, more than the proposal kernel scans in shared memory at once
+    dict(name="mixed", scale=1 / 64, batch=72, ragged=True),
     dict(name="llama", scale=1 / 32, n_q_override=5),   # verify window k + 1 (carry + 4 candidates)
     dict(name="llama", scale=1 / 32, n_q_override=2),   # window shorter than the proposals: appends stay visible
     # proposal steps as separate kap_append_kv + kap_attn_propose calls (the others use kap_append_propose)
