@@ -52,6 +52,8 @@ def _load():
             lib.orc_scores.restype = I
             lib.orc_topk_ark.argtypes = [P, I, I, I, I, P]
             lib.orc_topk_ark.restype = I
+            lib.orc_prior_scores.argtypes = [P, I, I, I, P]
+            lib.orc_prior_scores.restype = I
             lib.orc_select_spans.argtypes = [I, P, I, I, I, P]
             lib.orc_select_spans.restype = I
             lib.orc_compile_view_row.argtypes = [P, I, I, I, P, I, P, P, P]
@@ -124,6 +126,16 @@ def topk_ark(scores_row, N: int, a: int, r: int, k: int):
     out = np.zeros(max(N, 1), dtype=np.int32)
     n = _load().orc_topk_ark(_p(s), N, a, r, k, _p(out))
     return out[:n].copy()
+
+
+def prior_scores(aff):
+    """aff [L][H][N] external-prior block affinities of one request -> mean-pooled scores [N] (fp32, fixed order)."""
+    a = _f32(aff)
+    L, H, N = a.shape
+    out = np.zeros(N, dtype=np.float32)
+    if _load().orc_prior_scores(_p(a), L, H, N, _p(out)) != 0:
+        raise ValueError("bad prior shape")
+    return out
 
 
 def select_spans(N: int, spans, a: int, r: int):

@@ -174,6 +174,27 @@ int orc_scores(const float *q, const float *S, int hq, int hkv, int d, const int
   return 0;
 }
 
+// External-prior page scores (KRI page, "Required output shape" and the prior schema: a baked
+// block_affinities[L][H][N] tensor that the connector mean-pools across layers and heads before taking the top-K of
+// each request). aff holds M = L*H rows of N block scores, row i = l*H + h. The page is silent on the summation
+// order, so the library fixes one and this function states it plainly in fp32: the M values of a block are summed
+// in chunks of 32 consecutive rows (each chunk from 0.0f, rows ascending), the chunk sums are added in ascending
+// chunk order (from 0.0f), and the total is divided by M once. out[N].
+int orc_prior_scores(const float *aff, int L, int H, int N, float *out) {
+  const int M = L * H;
+  if (L <= 0 || H <= 0 || N < 0) return -1;
+  for (int n = 0; n < N; ++n) {
+    float total = 0.0f;
+    for (int c0 = 0; c0 < M; c0 += 32) {
+      float chunk = 0.0f;
+      for (int i = c0; i < std::min(c0 + 32, M); ++i) chunk = chunk + aff[static_cast<size_t>(i) * N + n];
+      total = total + chunk;
+    }
+    out[n] = total / static_cast<float>(M);
+  }
+  return 0;
+}
+
 // A<a>R<r>K<k> selection over N prompt pages (KRI page, "The A<a>R<r>K<k> tag"): pages [0, a) and the last r
 // pages are pinned; from the middle [a, N-r) the k best by score are chosen, ties to the lower page id. The
 // result is written ascending; the return value is its length. Plain full sort, no selection algorithm.

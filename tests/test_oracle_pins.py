@@ -167,6 +167,57 @@ def test_scores_fp32_close_to_fp64(orc):
 
 
 # ------------------------------------------------------------------------------------------------ spans
+# ------------------------------------------------------------------ external-prior scores (KRI prior schema)
+def test_prior_scores_exact_mean_on_dyadic_values(orc):
+    """Integer affinities with L*H a power of two: every partial sum and the division are exact, so the pooled score
+    is the exact arithmetic mean over layers and heads (KRI page: the connector mean-pools block_affinities)."""
+    rng = np.random.default_rng(11)
+    for L, H in [(1, 1), (4, 8), (8, 8), (32, 8), (2, 16)]:
+        aff = rng.integers(-1000, 1000, size=(L, H, 37)).astype(np.float32)
+        got = orc.prior_scores(aff)
+        want = aff.astype(np.float64).sum(axis=(0, 1)) / (L * H)
+        assert np.array_equal(got.astype(np.float64), want), (L, H)
+
+
+def test_prior_scores_chunked_order_hand_value(orc):
+    """The stated order sums 32 rows at a time: one huge value and 31 ones in the first chunk lose the ones, the
+    second chunk's 32 ones survive as 32. Worked by hand: (2^25 + 32) / 64 = 524288.5. A plain running sum would lose
+    all 63 ones (524288.0), a pairwise or fp64 sum would keep them (524288.984...)."""
+    aff = np.ones((8, 8, 1), dtype=np.float32)
+    aff[0, 0, 0] = 2.0 ** 25
+    assert orc.prior_scores(aff)[0] == np.float32(524288.5)
+    # Row index i = l*H + h: the huge value at (l=3, h=7) is row 31, the last of chunk 0, where the 31 ones before it
+    # round up to 32 (spacing 4 at 2^25); chunk 1 adds 32: (2^25 + 64) / 64 = 524289. With rows taken as h*L + l it
+    # would be row 59 and give 524288.9375.
+    aff = np.ones((8, 8, 1), dtype=np.float32)
+    aff[3, 7, 0] = 2.0 ** 25
+    assert orc.prior_scores(aff)[0] == np.float32(524289.0)
+
+
+def test_prior_scores_within_fp32_summation_bound(orc):
+    """Random affinities: the fp32 pooled score is within the recursive-summation bound of the exact mean."""
+    rng = np.random.default_rng(12)
+    L, H, N = 32, 8, 257
+    aff = rng.standard_normal((L, H, N)).astype(np.float32)
+    got = orc.prior_scores(aff).astype(np.float64)
+    a64 = aff.astype(np.float64)
+    exact = a64.sum(axis=(0, 1)) / (L * H)
+    bound = (L * H + 2) * 2.0 ** -24 * np.abs(a64).sum(axis=(0, 1)) / (L * H) + 2.0 ** -24 * np.abs(exact)
+    assert np.all(np.abs(got - exact) <= bound)
+
+
+def test_prior_selection_keeps_planted_blocks(orc):
+    """A/R/K over pooled priors: blocks whose affinity is raised in every layer and head are the k chosen, next to
+    the pinned anchor and recent blocks (KRI page, A1R2K13 over a 128-block prefix)."""
+    rng = np.random.default_rng(13)
+    L, H, N = 4, 8, 128
+    aff = rng.standard_normal((L, H, N)).astype(np.float32)
+    planted = np.sort(rng.choice(np.arange(1, 126), size=13, replace=False))
+    aff[:, :, planted] += 20.0
+    ids = orc.topk_ark(orc.prior_scores(aff), N, 1, 2, 13)
+    assert list(ids) == sorted([0] + planted.tolist() + [126, 127])
+
+
 def test_select_spans_brute_force(orc):
     rng = np.random.default_rng(4)
     for _ in range(100):

@@ -297,3 +297,24 @@ def make_workload(name: str, device="cpu", scale: float = 1.0, ragged: bool = Fa
         k_new_ver=k_new_ver, v_new_ver=v_new_ver, ark=dev(torch.tensor(ark, dtype=torch.int32)),
         per_kv_head=per_kv_head, spans=dev(spans), span_offsets=dev(span_offsets), needles=needles,
         sigma=sigma)
+
+
+def make_prior(w: Workload, num_layers: int = 32, device="cpu", seed_offset: int = 0,
+               needle_lift: float = 3.0, quantize: Optional[float] = None) -> torch.Tensor:
+    """Seeded external-prior affinities for workload `w`: [R][num_layers][Hkv][max_pages] fp32.
+
+    Stands in for a baked KRI prior (block_affinities[L][H][N] per request prefix): N(0, 1) per (layer, head,
+    block), with every needle page of the request lifted by `needle_lift` in all layers and heads, so that a prior
+    that "knows" the evidence favours those pages. Columns at or past a request's prompt pages are filled too; the
+    selection ignores them. quantize = q rounds every value to a multiple of q, which makes pooled scores tie.
+    """
+    R, Hkv = w.R, w.Hkv
+    max_pages = int(w.block_table.shape[1])
+    g = _gen("cpu", SEED_BASE + 77 + 1000 * seed_offset)
+    aff = torch.randn(R, num_layers, Hkv, max_pages, generator=g, dtype=torch.float32)
+    for r, nd in enumerate(w.needles):
+        if nd:
+            aff[r, :, :, torch.tensor(nd, dtype=torch.long)] += needle_lift
+    if quantize is not None:
+        aff = torch.round(aff / quantize) * quantize
+    return aff.to(device)
