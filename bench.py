@@ -44,6 +44,7 @@ def parse_args(argv=None):
     ap.add_argument("--layers", type=int, default=8)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prior", action="store_true", help="skip the external-prior selection timing")
     ap.add_argument("--unfused", action="store_true", help="separate KV-append and proposal launches per step")
     ap.add_argument("--no-overlap", action="store_true",
                     help="proposal kernels wait for the previous kernel before reading their view")
@@ -165,6 +166,61 @@ def step_bytes(w, cyc, sel_ids, n_sel):
     ver = int(((seq0 + nq) * w.Hkv * kv_tok).sum())
     app = int((w.k_prop * w.R + nq.sum()) * w.Hkv * w.d * 2 * 2)
     return dict(score=score, propose=prop, verify=ver, append=app)
+
+
+# ----------------------------------------------------------------------------------- external-prior selection
+PRIOR_LAYERS = 32   # layers of a baked prior (block_affinities[L][H][N]); H is the KV head count
+
+
+def time_prior(layers, steps: int, hbm_peak: float, dev):
+    """Times kap_prior_topk (KRI page, prior schema: pool a baked block_affinities[L][H][N] over layers and heads,
+    then take each request's A/R/K top-K) on every layer's page map, three distinct priors per layer so that the
+    priors read per replay exceed L2. Returns per-call time, the prior bytes a call reads and its GB/s."""
+    import torch
+    import selected_kv_sparse_gb300 as kap
+    from workloads import make_prior
+    calls = []
+    for li, (w, _, _) in enumerate(layers):
+        a, r, k = (int(x) for x in w.ark[0].tolist())
+        cap = int(w.sel_cap())
+        pol = kap.AccessPolicy(a, r, k, False, cap)
+        pmap = kap.PageMap(w.block_table, w.ctx_len)
+        max_pages = int(w.block_table.shape[1])
+        for rep in range(3):
+            aff = make_prior(w, PRIOR_LAYERS, device=dev, seed_offset=li * 3 + rep)
+            sel = torch.zeros((w.R, 1, cap), dtype=torch.int32, device=dev)
+            nsel = torch.zeros((w.R, 1), dtype=torch.int32, device=dev)
+            ws = torch.zeros(kap.kap_score_workspace_size(w.R, 1, max_pages) // 4, dtype=torch.float32, device=dev)
+            calls.append((pmap, aff, pol, sel, nsel, ws))
+
+    def run():
+        for pmap, aff, pol, sel, nsel, ws in calls:
+            kap.kap_prior_topk(pmap, aff, pol, sel, nsel, ws)
+    run()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    n = max(3, min(steps, 50))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (n * len(calls))
+    # algorithmic bytes: every prompt page's L*H affinities of every request
+    import numpy as np
+    w0 = layers[0][0]
+    N = ((w0.ctx_len.cpu().numpy().astype(np.int64) + PAGE - 1) // PAGE)
+    b = int(N.sum()) * PRIOR_LAYERS * w0.Hkv * 4
+    total = sum(c[1].numel() * 4 for c in calls)
+    return {"us_per_call": us, "bytes_per_call": b, "gbs": b / (us * 1e-6) / 1e9,
+            "pct_of_roofline": 100 * b / (us * 1e-6) / 1e9 / hbm_peak, "prior_layers": PRIOR_LAYERS,
+            "l2": f"{len(calls)} distinct priors, {total / 1e6:.0f} MB per replay"}
 
 
 # ------------------------------------------------------------------------------------------------ arenas
@@ -466,6 +522,8 @@ def run_kap(args, world, rank, local):
         e2e = {"value": bytes_all / (e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": n_e2e, "ms_per_step": e_ms}
 
+    prior = None if args.no_prior else time_prior(layers, K, hbm_peak, dev)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
@@ -502,6 +560,7 @@ def run_kap(args, world, rank, local):
                        "us_per_launch": ver_launch_ms * 1e3, "bytes_per_launch": ver_bytes_launch,
                        "steps_per_s": 1e3 / ver_launch_ms},
             "plan_us_per_layer": plan_ms * 1e3,
+            "prior_topk": prior,
             "phase_ms_per_step": {k2: v / K for k2, v in phase_ms.items()},
             "roofline": {"bound": "hbm", "kernel": "verify_tc_kernel", "achieved": ver_gbs, "peak": hbm_peak,
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": ver_gbs / hbm_peak, "traffic": traffic},

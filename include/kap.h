@@ -143,6 +143,22 @@ kap_status kap_score_topk_view(const kap_kv_pool *pool, const kap_page_map *map,
                                int32_t *fallback_dev, float s_max, int64_t *slot_out, int32_t *pos_out,
                                kap_stream stream);
 
+/* External-prior selection. KRI page, prior schema and connector: a baked prior block_affinities[L][H][N] per
+ * request prefix is mean-pooled across layers and heads and the top-K is taken per request (one selection row
+ * shared by all heads), here under the A<a>R<r>K<k> split of `policy`, whose per_kv_head must be 0.
+ *   affinities_dev [R][L][H][max_pages] fp32: the prior's block scores of each request; columns at or past
+ *                  ceil(ctx_len/16) are ignored. L * H <= 2048.
+ *   pooled score   = (sum over rows i = l*H + h, in chunks of 32 consecutive rows each summed from 0 with i
+ *                    ascending, the chunk sums added in ascending order, all in fp32) / (L*H), one rounding.
+ *                    The page states no order; this one is fixed so that selections reproduce bit for bit.
+ *   sel_ids [R][1][policy->cap] out, ascending; n_sel [R][1] out (same rule and ties as kap_score_topk).
+ *   workspace >= kap_score_workspace_size(R, 1, max_pages) bytes (the pooled scores).
+ * Errors: KAP_EINVAL for a null pointer, L or H < 1, L*H > 2048 or per_kv_head != 0; KAP_ECAPACITY for a cap or
+ * workspace that is too small. Follow with kap_compile_view (sel_rows_per_seq = 1) for the compact view. */
+kap_status kap_prior_topk(const kap_page_map *map, const float *affinities_dev, int32_t num_layers,
+                          int32_t num_heads, const kap_access_policy *policy, int32_t *sel_ids, int32_t *n_sel,
+                          void *workspace, size_t workspace_bytes, kap_stream stream);
+
 /* Span selection. KAP paper, compiler stage 3 (selected spans resolved to KV pages): a prompt page is kept when
  * any token of a selected span falls in it; pinned anchor/recent pages (policy a, r) are added. One row per
  * request (shared by all heads).

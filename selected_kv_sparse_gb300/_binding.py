@@ -67,6 +67,7 @@ def _declare(lib):
     sig = {
         "kap_build_summaries": ([P, P, P], I),
         "kap_score_topk": ([P, P, P, P, P, P, P, Z, P], I),
+        "kap_prior_topk": ([P, P, I, I, P, P, P, P, Z, P], I),
         "kap_score_workspace_size": ([I, I, I], Z),
         "kap_score_topk_view": ([P, P, P, P, P, P, P, Z, I, P, P, F, P, P, P], I),
         "kap_select_spans": ([P, P, P, P, P, P, P], I),
@@ -254,6 +255,21 @@ def kap_score_topk(pool: KVPool, pmap: PageMap, q: torch.Tensor, policy: AccessP
         raise TypeError("q must have the pool dtype")
     p, m, pol = pool._c(), pmap._c(), policy._c()
     _check("kap_score_topk", lib.kap_score_topk(ctypes.byref(p), ctypes.byref(m), _ptr(q), ctypes.byref(pol),
+                                                _i32(sel_ids, "sel_ids"), _i32(n_sel, "n_sel"), _ptr(workspace),
+                                                workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def kap_prior_topk(pmap: PageMap, affinities: torch.Tensor, policy: AccessPolicy, sel_ids: torch.Tensor,
+                   n_sel: torch.Tensor, workspace: torch.Tensor, stream=None):
+    """affinities [R][L][H][max_pages] fp32 external prior -> per-request A/R/K selection (one row per request)."""
+    lib = load()
+    if affinities.dtype != torch.float32 or affinities.dim() != 4 or not affinities.is_contiguous():
+        raise TypeError("affinities must be a contiguous fp32 [R][L][H][max_pages] tensor")
+    if affinities.shape[0] != pmap.block_table.shape[0] or affinities.shape[3] != pmap.block_table.shape[1]:
+        raise ValueError("affinities must be [R][L][H][max_pages] for this page map")
+    m, pol = pmap._c(), policy._c()
+    _check("kap_prior_topk", lib.kap_prior_topk(ctypes.byref(m), _ptr(affinities), int(affinities.shape[1]),
+                                                int(affinities.shape[2]), ctypes.byref(pol),
                                                 _i32(sel_ids, "sel_ids"), _i32(n_sel, "n_sel"), _ptr(workspace),
                                                 workspace.numel() * workspace.element_size(), _stream(stream)))
 

@@ -144,6 +144,48 @@ __global__ void __launch_bounds__(256) score_kernel(const T *__restrict__ q, con
 // ------------------------------------------------------------------------------------ compaction helper
 // Writes, in ascending order, every id in [0, N) whose flag is set; the flags come from `flag(j)`. Each thread
 // owns a contiguous range of ids. Returns the total count (to every thread).
+// ------------------------------------------------------------------------------ external-prior scores
+// KRI page, prior schema: a baked block_affinities[L][H][N] per request is mean-pooled over layers and heads before
+// the per-request top-K. The page fixes no summation order; this one is fixed so selections reproduce bit for bit:
+// rows i = l*H + h are summed in chunks of 32 (each chunk from 0, i ascending), the chunk sums are added in
+// ascending order (from 0), and the total is divided by L*H once (round to nearest). One CTA covers 32 consecutive
+// blocks of one request: lane = block, so each load is one 128-byte row segment; warp w sums chunks w, w+8, ...
+// with all 32 loads of a chunk in flight; warp 0 adds the chunk sums in order.
+constexpr int kPriorWarps = 8;
+constexpr int kPriorMaxChunks = 64;  // L*H <= 2048
+
+__global__ void __launch_bounds__(kPriorWarps * 32) prior_score_kernel(const float *__restrict__ aff, int M,
+                                                                       int max_pages,
+                                                                       const int32_t *__restrict__ ctx_len,
+                                                                       float *__restrict__ scores) {
+  __shared__ float csum[kPriorMaxChunks][32];
+  grid_dependency_sync();
+  const int r = blockIdx.y;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int n = blockIdx.x * 32 + lane;
+  const int N = min(max_pages, (ctx_len[r] + kPage - 1) / kPage);
+  const bool ok = n < N;
+  const int nch = (M + 31) / 32;
+  const float *col = aff + static_cast<size_t>(r) * M * max_pages + (ok ? n : 0);  // clamped: always in bounds
+  for (int c = warp; c < nch; c += kPriorWarps) {
+    const int i0 = c * 32;
+    float x[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) x[j] = (i0 + j < M) ? __ldcs(col + static_cast<size_t>(i0 + j) * max_pages) : 0.0f;
+    float sum = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (i0 + j < M) sum = __fadd_rn(sum, x[j]);
+    csum[c][lane] = sum;
+  }
+  __syncthreads();
+  if (warp == 0 && ok) {
+    float t = 0.0f;
+    for (int c = 0; c < nch; ++c) t = __fadd_rn(t, csum[c][lane]);
+    scores[static_cast<size_t>(r) * max_pages + n] = __fdiv_rn(t, static_cast<float>(M));
+  }
+}
+
 template <class F>
 __device__ int compact_ascending(int N, F flag, int32_t *out, int cap, int *scan_scratch, int *err) {
   const int per = (N + blockDim.x - 1) / blockDim.x;
@@ -581,6 +623,18 @@ cudaError_t launch_topk(const MapArgs &m, const float *scores, int rows, int a, 
   launch_pdl(kern, dim3(m.R * rows), dim3(kTopkThreads), smem, s, scores, rows, m.ctx_len, m.max_pages, a, r, k,
              per_seq_ark, cap, sel, n_sel, m.bt, m.seq_len, vo, err);
   return cudaGetLastError();
+}
+
+cudaError_t launch_prior_topk(const MapArgs &m, const float *aff, int L, int H, int a, int r, int k,
+                              const int32_t *per_seq_ark, int cap, int32_t *sel, int32_t *n_sel, float *scores,
+                              int *err, cudaStream_t s) {
+  const int M = L * H;
+  if (M < 1 || M > 32 * kPriorMaxChunks) return cudaErrorInvalidValue;
+  dim3 grid((m.max_pages + 31) / 32, m.R);
+  launch_pdl(prior_score_kernel, grid, dim3(kPriorWarps * 32), 0, s, aff, M, m.max_pages, m.ctx_len, scores);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_topk(m, scores, 1, a, r, k, per_seq_ark, cap, sel, n_sel, nullptr, err, s);
 }
 
 cudaError_t launch_select_spans(const MapArgs &m, const int32_t *spans, const int32_t *span_offsets, int a, int r,

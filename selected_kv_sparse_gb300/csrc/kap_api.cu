@@ -175,6 +175,26 @@ kap_status kap_score_topk_view(const kap_kv_pool *pool, const kap_page_map *map,
   return score_topk_common(pool, map, q_dev, policy, sel_ids, n_sel, workspace, workspace_bytes, &vw, stream);
 }
 
+kap_status kap_prior_topk(const kap_page_map *map, const float *affinities_dev, int32_t num_layers,
+                          int32_t num_heads, const kap_access_policy *policy, int32_t *sel_ids, int32_t *n_sel,
+                          void *workspace, size_t workspace_bytes, kap_stream stream) {
+  kap_status st = check_map(map, false);
+  if (st != KAP_OK) return st;
+  if (!affinities_dev || !policy || !sel_ids || !n_sel || !workspace) return KAP_EINVAL;
+  if (num_layers < 1 || num_heads < 1 || static_cast<int64_t>(num_layers) * num_heads > 2048) return KAP_EINVAL;
+  if (policy->anchor < 0 || policy->recent < 0 || policy->topk < 0 || policy->cap <= 0) return KAP_EINVAL;
+  if (policy->per_kv_head != 0) return KAP_EINVAL;
+  if (!policy->per_seq_ark &&
+      static_cast<int64_t>(policy->anchor) + policy->recent + policy->topk > policy->cap &&
+      policy->cap < map->max_pages)
+    return KAP_ECAPACITY;
+  if (static_cast<size_t>(map->max_pages) * 4 > 200 * 1024) return KAP_EUNSUPPORTED;
+  if (workspace_bytes < kap_score_workspace_size(map->num_seqs, 1, map->max_pages)) return KAP_ECAPACITY;
+  return cuda_status(launch_prior_topk(map_args(map), affinities_dev, num_layers, num_heads, policy->anchor,
+                                       policy->recent, policy->topk, policy->per_seq_ark, policy->cap, sel_ids,
+                                       n_sel, static_cast<float *>(workspace), error_word(), cs(stream)));
+}
+
 kap_status kap_select_spans(const kap_page_map *map, const int32_t *spans_dev, const int32_t *span_offsets_dev,
                             const kap_access_policy *policy, int32_t *sel_ids, int32_t *n_sel, kap_stream stream) {
   kap_status st = check_map(map, false);

@@ -41,6 +41,10 @@ struct ViewArgsOut {
 cudaError_t launch_topk(const MapArgs &m, const float *scores, int rows, int a, int r, int k,
                         const int32_t *per_seq_ark, int cap, int32_t *sel, int32_t *n_sel, const ViewArgsOut *view,
                         int *err, cudaStream_t s);
+// external-prior scores [R][L][H][max_pages] pooled into scores [R][max_pages], then the per-request top-K
+cudaError_t launch_prior_topk(const MapArgs &m, const float *aff, int L, int H, int a, int r, int k,
+                              const int32_t *per_seq_ark, int cap, int32_t *sel, int32_t *n_sel, float *scores,
+                              int *err, cudaStream_t s);
 cudaError_t launch_select_spans(const MapArgs &m, const int32_t *spans, const int32_t *span_offsets, int a, int r,
                                 const int32_t *per_seq_ark, int cap, int32_t *sel, int32_t *n_sel, int *err,
                                 cudaStream_t s);
