@@ -54,6 +54,8 @@ def _load():
             lib.orc_topk_ark.restype = I
             lib.orc_prior_scores.argtypes = [P, I, I, I, P]
             lib.orc_prior_scores.restype = I
+            lib.orc_accept_commit.argtypes = [P, I, I, P, I, I, P, P, P]
+            lib.orc_accept_commit.restype = I
             lib.orc_select_spans.argtypes = [I, P, I, I, I, P]
             lib.orc_select_spans.restype = I
             lib.orc_compile_view_row.argtypes = [P, I, I, I, P, I, P, P, P]
@@ -136,6 +138,18 @@ def prior_scores(aff):
     if _load().orc_prior_scores(_p(a), L, H, N, _p(out)) != 0:
         raise ValueError("bad prior shape")
     return out
+
+
+def accept_commit(logits, tokens, top_n: int, start_pos: int):
+    """One verify window: logits [rows][V], tokens [rows] (carry, then proposals) -> (m, next carry, seq_len)."""
+    lg = _f32(logits)
+    tk = _i32(tokens)
+    rows, V = lg.shape
+    assert tk.shape == (rows,)
+    m, c, sl = (np.zeros(1, np.int32) for _ in range(3))
+    if _load().orc_accept_commit(_p(lg), rows, V, _p(tk), top_n, start_pos, _p(m), _p(c), _p(sl)) != 0:
+        raise ValueError("bad window")
+    return int(m[0]), int(c[0]), int(sl[0])
 
 
 def select_spans(N: int, spans, a: int, r: int):

@@ -369,6 +369,43 @@ int orc_attn_verify(const float *q, const float *K, const float *V, int num_page
 }
 
 // Number of hardware threads of this host (reported beside CPU timings).
+// Tolerant acceptance and commit of one verify window (KAP paper, verifier: the window is the carry token followed by
+// the k proposals; a proposal is accepted when it lies within the target's top-n candidates under the full context,
+// the Top-3 rule being n = 3; m counts the proposals accepted consecutively from the start; the verifier then emits
+// the next carry and commits). logits [rows][V]: row j is the verifier's prediction after window token j;
+// tokens [rows]: token 0 is the carry, tokens 1..rows-1 the proposals. Proposal j is checked against row j - 1 by
+// its rank under (logit descending, token id ascending, NaN last): accepted when fewer than n tokens come before it.
+// The next carry is the first token of row m under the same order (the target's top choice after the accepted
+// prefix); the committed length is start + 1 + m (the carry and the accepted proposals). Plain full sorts.
+int orc_accept_commit(const float *logits, int rows, int V, const int32_t *tokens, int top_n, int start_pos,
+                      int32_t *m_out, int32_t *carry_out, int32_t *seq_len_out) {
+  if (rows < 1 || V < 1 || top_n < 1) return -1;
+  auto ranked = [&](int j) {  // the tokens of row j in rank order
+    std::vector<int> ids(V);
+    for (int t = 0; t < V; ++t) ids[t] = t;
+    const float *row = logits + static_cast<size_t>(j) * V;
+    std::stable_sort(ids.begin(), ids.end(), [&](int x, int y) {
+      const uint32_t kx = order_key(row[x]), ky = order_key(row[y]);
+      if (kx != ky) return kx > ky;
+      return x < y;
+    });
+    return ids;
+  };
+  int m = 0;
+  for (int j = 1; j < rows; ++j) {
+    const int x = tokens[j];
+    if (x < 0 || x >= V) break;  // not a token of the vocabulary: rejected
+    const std::vector<int> ids = ranked(j - 1);
+    const int rank = static_cast<int>(std::find(ids.begin(), ids.end(), x) - ids.begin());
+    if (rank >= top_n) break;
+    ++m;
+  }
+  *m_out = m;
+  *carry_out = ranked(m)[0];
+  *seq_len_out = start_pos + 1 + m;
+  return 0;
+}
+
 int orc_hardware_threads(void) { return static_cast<int>(std::thread::hardware_concurrency()); }
 
 }  // extern "C"

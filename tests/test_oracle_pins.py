@@ -218,6 +218,70 @@ def test_prior_selection_keeps_planted_blocks(orc):
     assert list(ids) == sorted([0] + planted.tolist() + [126, 127])
 
 
+# ------------------------------------------------------- tolerant acceptance and commit (KAP paper, verifier)
+def test_accept_commit_worked_windows(orc):
+    """Hand-worked windows of a 5-token vocabulary (carry, then proposals; row j predicts after token j)."""
+    lg = np.array([[0, 5, 4, 3, 1], [9, 8, 7, 6, 5], [1, 1, 1, 1, 1]], np.float32)
+    # token 3 is third in row 0 (5, 4, 3): accepted; token 2 is third in row 1: accepted; all-equal row 2 -> token 0
+    assert orc.accept_commit(lg, [0, 3, 2], 3, 100) == (2, 0, 103)
+    # token 4 is fourth in row 0: rejected at once; the carry is row 0's first (token 1); only the carry commits
+    assert orc.accept_commit(lg, [0, 4, 2], 3, 100) == (0, 1, 101)
+    # the second proposal fails (token 0 is fifth in row 1) after the first passes: carry = first of row 1 (token 0)
+    assert orc.accept_commit(lg, [0, 1, 4], 3, 7) == (1, 0, 9)
+    # a token outside the vocabulary is rejected
+    assert orc.accept_commit(lg, [0, 5, 2], 3, 0) == (0, 1, 1)
+
+
+def test_accept_commit_greedy_special_case(orc):
+    """With n = 1 the rule is greedy speculative verification: the accepted prefix is the longest run where each
+    proposal equals the argmax of the row before it, and the carry is the argmax after that prefix."""
+    rng = np.random.default_rng(21)
+    for _ in range(300):
+        rows, V = int(rng.integers(1, 7)), int(rng.integers(1, 9))
+        lg = rng.integers(0, 4, size=(rows, V)).astype(np.float32)
+        am = lg.argmax(axis=1)   # first maximum: lower id on ties
+        toks = [0] + [int(am[j - 1]) if rng.random() < 0.7 else int(rng.integers(0, V)) for j in range(1, rows)]
+        m = 0
+        while m + 1 < rows and toks[m + 1] == am[m]:
+            m += 1
+        assert orc.accept_commit(lg, toks, 1, 50) == (m, int(am[m]), 51 + m)
+
+
+def test_accept_commit_counting_brute_force(orc):
+    """Random tied and NaN logits: a proposal passes iff fewer than n tokens beat it (a higher logit, or an equal one
+    with a lower id; NaN beats nothing and loses to every number)."""
+    rng = np.random.default_rng(22)
+
+    def beats(a, ia, b, ib):  # does (a, ia) come before (b, ib)?
+        if np.isnan(a):
+            return bool(np.isnan(b)) and ia < ib
+        if np.isnan(b):
+            return True
+        return a > b or (a == b and ia < ib)
+
+    for _ in range(300):
+        rows, V, n = int(rng.integers(2, 6)), int(rng.integers(2, 10)), int(rng.integers(1, 5))
+        lg = rng.integers(0, 3, size=(rows, V)).astype(np.float32)
+        lg[rng.random((rows, V)) < 0.15] = np.nan
+        toks = [int(rng.integers(0, V)) for _ in range(rows)]
+        m = 0
+        for j in range(1, rows):
+            x = toks[j]
+            nb = sum(beats(lg[j - 1, t], t, lg[j - 1, x], x) for t in range(V) if t != x)
+            if nb >= n:
+                break
+            m += 1
+        first = [t for t in range(V) if not any(beats(lg[m, u], u, lg[m, t], t) for u in range(V) if u != t)]
+        assert orc.accept_commit(lg, toks, n, 3) == (m, first[0], 4 + m)
+
+
+def test_accept_commit_everything_passes_with_n_at_least_v(orc):
+    rng = np.random.default_rng(23)
+    lg = rng.standard_normal((5, 6)).astype(np.float32)
+    m, c, sl = orc.accept_commit(lg, [1, 2, 3, 4, 5], 6, 10)
+    assert (m, sl) == (4, 15) and c == int(lg[4].argmax())
+
+
 def test_select_spans_brute_force(orc):
     rng = np.random.default_rng(4)
     for _ in range(100):

@@ -318,3 +318,33 @@ def make_prior(w: Workload, num_layers: int = 32, device="cpu", seed_offset: int
     if quantize is not None:
         aff = torch.round(aff / quantize) * quantize
     return aff.to(device)
+
+
+def make_verify_logits(w: Workload, vocab: int = 128256, accept: float = 0.95, device="cpu", seed_offset: int = 0,
+                       dtype=torch.float32, ties: bool = False):
+    """Seeded verifier logits for the windows of workload `w` (the carry row plus k = n_q - 1 proposals each).
+
+    Returns (logits [total_rows][vocab], tokens [total_rows] int32, window offsets [R+1] int32). Token 0 of a window
+    is the carry, drawn uniformly; each later token is a proposal. Background logits are N(0, 1). For each proposal
+    the generator decides, with probability `accept`, that it should pass: its logit in the row before it is set to
+    8 + U(0, 1) (far above the background), else to -8. ties=True draws the background from {0, 1, 2} instead, so
+    that many tokens share a logit. Nothing here ranks tokens: the decision is planted in the data.
+    """
+    g = _gen("cpu", SEED_BASE + 91 + 1000 * seed_offset)
+    n_q = w.n_q.cpu().tolist()
+    offs = [0]
+    for n in n_q:
+        offs.append(offs[-1] + int(n))
+    rows = offs[-1]
+    if ties:
+        lg = torch.randint(0, 3, (rows, vocab), generator=g).to(torch.float32)
+    else:
+        lg = torch.randn(rows, vocab, generator=g, dtype=torch.float32)
+    tok = torch.randint(0, vocab, (rows,), generator=g, dtype=torch.int64)
+    u = torch.rand(rows, generator=g, dtype=torch.float64)
+    lift = torch.rand(rows, generator=g, dtype=torch.float32)
+    for r in range(len(n_q)):
+        for j in range(offs[r] + 1, offs[r + 1]):
+            lg[j - 1, tok[j]] = (8.0 + float(lift[j])) if float(u[j]) < accept else -8.0
+    return (lg.to(dtype).to(device), tok.to(torch.int32).to(device),
+            torch.tensor(offs, dtype=torch.int32, device=device))
