@@ -45,6 +45,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prior", action="store_true", help="skip the external-prior selection timing")
+    ap.add_argument("--no-accept", action="store_true", help="skip the acceptance and commit timing")
     ap.add_argument("--unfused", action="store_true", help="separate KV-append and proposal launches per step")
     ap.add_argument("--no-overlap", action="store_true",
                     help="proposal kernels wait for the previous kernel before reading their view")
@@ -221,6 +222,57 @@ def time_prior(layers, steps: int, hbm_peak: float, dev):
     return {"us_per_call": us, "bytes_per_call": b, "gbs": b / (us * 1e-6) / 1e9,
             "pct_of_roofline": 100 * b / (us * 1e-6) / 1e9 / hbm_peak, "prior_layers": PRIOR_LAYERS,
             "l2": f"{len(calls)} distinct priors, {total / 1e6:.0f} MB per replay"}
+
+
+# ------------------------------------------------------------------------------- tolerant acceptance, commit
+ACCEPT_VOCAB = 128256   # Llama-3 vocabulary
+
+
+def time_accept(layers, steps: int, hbm_peak: float, dev):
+    """Times kap_accept_commit (KAP paper, verifier: Top-3 tolerant acceptance of the carry + k proposal window, next
+    carry, committed length) on fp32 logits of the carry + 4 proposals of every request, three distinct logit sets
+    per layer so that the logits read per replay exceed L2."""
+    import torch
+    import selected_kv_sparse_gb300 as kap
+    from workloads import make_verify_logits, make_workload
+    w0 = layers[0][0]
+    calls = []
+    for li in range(len(layers)):
+        for rep in range(3):
+            wk = make_workload(CONFIG, device="cpu", scale=1 / 64, poison=False, n_q_override=w0.k_prop + 1)
+            lg, tok, off = make_verify_logits(wk, ACCEPT_VOCAB, device=dev, seed_offset=li * 3 + rep)
+            R, rows = wk.R, int(off[-1].item())
+            start = torch.full((R,), 32768, dtype=torch.int32, device=dev)
+            outs = [torch.zeros(R, dtype=torch.int32, device=dev) for _ in range(3)]
+            ws = torch.zeros(kap.kap_accept_workspace_size(R, rows, ACCEPT_VOCAB), dtype=torch.uint8, device=dev)
+            calls.append((lg, off, tok, start, outs, ws))
+
+    def run():
+        for lg, off, tok, start, (acc, car, sl), ws in calls:
+            kap.kap_accept_commit(lg, off, tok, 3, acc, car, ws, start_pos=start, seq_len_out=sl)
+    run()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    n = max(3, min(steps, 50))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (n * len(calls))
+    b = calls[0][0].numel() * 4
+    acc_rate = float(torch.stack([c[4][0] for c in calls]).float().mean()) / w0.k_prop
+    return {"us_per_call": us, "bytes_per_call": b, "gbs": b / (us * 1e-6) / 1e9,
+            "pct_of_roofline": 100 * b / (us * 1e-6) / 1e9 / hbm_peak, "vocab": ACCEPT_VOCAB, "top_n": 3,
+            "window": f"carry + {w0.k_prop} proposals x {w0.R} requests, fp32 logits",
+            "acceptance_rate": acc_rate, "l2": f"{len(calls)} distinct logit sets, "
+                                              f"{len(calls) * b / 1e6:.0f} MB per replay"}
 
 
 # ------------------------------------------------------------------------------------------------ arenas
@@ -523,6 +575,7 @@ def run_kap(args, world, rank, local):
                "d2h_bytes_per_step": d2h, "steps": n_e2e, "ms_per_step": e_ms}
 
     prior = None if args.no_prior else time_prior(layers, K, hbm_peak, dev)
+    accept = None if args.no_accept else time_accept(layers, K, hbm_peak, dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -561,6 +614,7 @@ def run_kap(args, world, rank, local):
                        "steps_per_s": 1e3 / ver_launch_ms},
             "plan_us_per_layer": plan_ms * 1e3,
             "prior_topk": prior,
+            "accept_commit": accept,
             "phase_ms_per_step": {k2: v / K for k2, v in phase_ms.items()},
             "roofline": {"bound": "hbm", "kernel": "verify_tc_kernel", "achieved": ver_gbs, "peak": hbm_peak,
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": ver_gbs / hbm_peak, "traffic": traffic},

@@ -159,6 +159,31 @@ kap_status kap_prior_topk(const kap_page_map *map, const float *affinities_dev, 
                           int32_t num_heads, const kap_access_policy *policy, int32_t *sel_ids, int32_t *n_sel,
                           void *workspace, size_t workspace_bytes, kap_stream stream);
 
+/* Tolerant acceptance and commit of verify windows. KAP paper, verifier: the window is the verifier-approved carry
+ * token followed by the k proposals; a proposal is accepted when it lies within the target's top-n candidates under
+ * the full context (the Top-3 rule: top_n = 3; top_n = 1 is greedy exact match); m counts the proposals accepted
+ * consecutively from the start; the same transition emits the next carry and advances the committed state.
+ *   logits_dev         [total_rows][vocab] of logits_dtype (KAP_BF16 or KAP_F32): row j is the verifier's prediction
+ *                      after window token j (the verify attention's window rows, through the model's head).
+ *   window_offsets_dev [num_seqs+1] int32: request r owns rows [off[r], off[r+1]); every window holds >= 1 row and
+ *                      off[num_seqs] = total_rows.
+ *   tokens_dev         [total_rows] int32: the window's tokens; row off[r] is the carry, the rest are proposals.
+ *   Rank order of a row: logit descending, lower token id first, NaN last. Proposal j passes when fewer than top_n
+ *   tokens of row j - 1 come before it; a token outside [0, vocab) fails.
+ *   accepted_out [num_seqs] = m; carry_out [num_seqs] = the first token of row m (the next carry);
+ *   seq_len_out [num_seqs] (may be NULL, may alias a page map's seq_len) = start_pos[r] + 1 + m, the committed length:
+ *   the carry at start_pos[r] and the accepted proposals after it, whose KV the window append already wrote.
+ *   workspace >= kap_accept_workspace_size(num_seqs, total_rows, vocab) bytes, zeroed once before the first call
+ *   (the call leaves its counters at zero).
+ * Errors: KAP_EINVAL for null pointers, vocab or top_n < 1, total_rows < num_seqs; KAP_EUNSUPPORTED for another
+ * dtype or more than 65535 rows; KAP_ECAPACITY for a small workspace. */
+kap_status kap_accept_commit(const void *logits_dev, int32_t logits_dtype, int32_t vocab, int32_t num_seqs,
+                             int32_t total_rows, const int32_t *window_offsets_dev, const int32_t *tokens_dev,
+                             const int32_t *start_pos_dev, int32_t top_n, int32_t *accepted_out,
+                             int32_t *carry_out, int32_t *seq_len_out, void *workspace, size_t workspace_bytes,
+                             kap_stream stream);
+size_t kap_accept_workspace_size(int32_t num_seqs, int32_t total_rows, int32_t vocab);
+
 /* Span selection. KAP paper, compiler stage 3 (selected spans resolved to KV pages): a prompt page is kept when
  * any token of a selected span falls in it; pinned anchor/recent pages (policy a, r) are added. One row per
  * request (shared by all heads).

@@ -68,6 +68,8 @@ def _declare(lib):
         "kap_build_summaries": ([P, P, P], I),
         "kap_score_topk": ([P, P, P, P, P, P, P, Z, P], I),
         "kap_prior_topk": ([P, P, I, I, P, P, P, P, Z, P], I),
+        "kap_accept_commit": ([P, I, I, I, I, P, P, P, I, P, P, P, P, Z, P], I),
+        "kap_accept_workspace_size": ([I, I, I], Z),
         "kap_score_workspace_size": ([I, I, I], Z),
         "kap_score_topk_view": ([P, P, P, P, P, P, P, Z, I, P, P, F, P, P, P], I),
         "kap_select_spans": ([P, P, P, P, P, P, P], I),
@@ -272,6 +274,28 @@ def kap_prior_topk(pmap: PageMap, affinities: torch.Tensor, policy: AccessPolicy
                                                 int(affinities.shape[2]), ctypes.byref(pol),
                                                 _i32(sel_ids, "sel_ids"), _i32(n_sel, "n_sel"), _ptr(workspace),
                                                 workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def kap_accept_workspace_size(num_seqs: int, total_rows: int, vocab: int) -> int:
+    return int(load().kap_accept_workspace_size(num_seqs, total_rows, vocab))
+
+
+def kap_accept_commit(logits: torch.Tensor, window_offsets: torch.Tensor, tokens: torch.Tensor, top_n: int,
+                      accepted: torch.Tensor, carry: torch.Tensor, workspace: torch.Tensor,
+                      start_pos: Optional[torch.Tensor] = None, seq_len_out: Optional[torch.Tensor] = None,
+                      stream=None):
+    """Top-n tolerant acceptance of verify windows (logits [total_rows][vocab], bf16 or fp32) and their commit."""
+    lib = load()
+    if logits.dim() != 2 or not logits.is_contiguous() or logits.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("logits must be a contiguous [total_rows][vocab] bf16 or fp32 tensor")
+    dt = KAP_BF16 if logits.dtype == torch.bfloat16 else KAP_F32
+    total_rows, vocab = int(logits.shape[0]), int(logits.shape[1])
+    R = int(window_offsets.numel()) - 1
+    _check("kap_accept_commit", lib.kap_accept_commit(
+        _ptr(logits), dt, vocab, R, total_rows, _i32(window_offsets, "window_offsets"), _i32(tokens, "tokens"),
+        _i32(start_pos, "start_pos") if start_pos is not None else None, int(top_n), _i32(accepted, "accepted"),
+        _i32(carry, "carry"), _i32(seq_len_out, "seq_len_out") if seq_len_out is not None else None,
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def kap_score_topk_view(pool: KVPool, pmap: PageMap, q: torch.Tensor, policy: AccessPolicy, sel_ids: torch.Tensor,

@@ -195,6 +195,28 @@ kap_status kap_prior_topk(const kap_page_map *map, const float *affinities_dev, 
                                        n_sel, static_cast<float *>(workspace), error_word(), cs(stream)));
 }
 
+size_t kap_accept_workspace_size(int32_t num_seqs, int32_t total_rows, int32_t vocab) {
+  if (num_seqs <= 0 || total_rows <= 0 || vocab <= 0) return 0;
+  return accept_workspace_bytes(num_seqs, total_rows, vocab);
+}
+
+kap_status kap_accept_commit(const void *logits_dev, int32_t logits_dtype, int32_t vocab, int32_t num_seqs,
+                             int32_t total_rows, const int32_t *window_offsets_dev, const int32_t *tokens_dev,
+                             const int32_t *start_pos_dev, int32_t top_n, int32_t *accepted_out,
+                             int32_t *carry_out, int32_t *seq_len_out, void *workspace, size_t workspace_bytes,
+                             kap_stream stream) {
+  if (!logits_dev || !window_offsets_dev || !tokens_dev || !accepted_out || !carry_out || !workspace)
+    return KAP_EINVAL;
+  if (seq_len_out && !start_pos_dev) return KAP_EINVAL;
+  if (logits_dtype != KAP_BF16 && logits_dtype != KAP_F32) return KAP_EUNSUPPORTED;
+  if (vocab <= 0 || num_seqs <= 0 || total_rows < num_seqs || top_n <= 0) return KAP_EINVAL;
+  if (total_rows > 65535) return KAP_EUNSUPPORTED;  // grid rows
+  if (workspace_bytes < accept_workspace_bytes(num_seqs, total_rows, vocab)) return KAP_ECAPACITY;
+  return cuda_status(launch_accept(logits_dev, logits_dtype, vocab, window_offsets_dev, num_seqs, total_rows,
+                                   tokens_dev, start_pos_dev, top_n, workspace, accepted_out, carry_out, seq_len_out,
+                                   error_word(), cs(stream)));
+}
+
 kap_status kap_select_spans(const kap_page_map *map, const int32_t *spans_dev, const int32_t *span_offsets_dev,
                             const kap_access_policy *policy, int32_t *sel_ids, int32_t *n_sel, kap_stream stream) {
   kap_status st = check_map(map, false);

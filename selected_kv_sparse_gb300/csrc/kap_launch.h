@@ -55,6 +55,12 @@ cudaError_t launch_compile_view(const MapArgs &m, const int32_t *sel, const int3
 cudaError_t launch_slot_mapping(const MapArgs &m, const int32_t *tok_offsets, const int32_t *start_pos, int T,
                                 int64_t *slot_out, int32_t *pos_out, cudaStream_t s);
 
+// tolerant acceptance and commit of verify windows (k_accept.cu)
+size_t accept_workspace_bytes(int num_seqs, int total_rows, int vocab);
+cudaError_t launch_accept(const void *logits, int dtype, int V, const int32_t *woff, int R, int total_rows,
+                          const int32_t *tokens, const int32_t *start_pos, int top_n, void *ws, int32_t *m_out,
+                          int32_t *carry_out, int32_t *seq_out, int *err, cudaStream_t s);
+
 // KV append (k_append.cu)
 cudaError_t launch_append(const PoolArgs &p, const void *k_new, const void *v_new, void *q_inout,
                           const int32_t *pos, const int64_t *slots, int T, int tok_stride, const float *inv_freq,

@@ -53,6 +53,8 @@ def test_null_arguments_are_rejected_without_a_gpu(lib):
     assert lib.kap_attn_propose(None, None, None, None, None, None, None, ctypes.c_size_t(0), None) == -1
     assert lib.kap_score_topk(None, None, None, None, None, None, None, ctypes.c_size_t(0), None) == -1
     assert lib.kap_prior_topk(None, None, 32, 8, None, None, None, None, ctypes.c_size_t(0), None) == -1
+    assert lib.kap_accept_commit(None, 1, 128, 1, 5, None, None, None, 3, None, None, None, None,
+                                 ctypes.c_size_t(0), None) == -1
 
 
 def test_parse_ark():
