@@ -165,8 +165,8 @@ kap_status kap_prior_topk(const kap_page_map *map, const float *affinities_dev, 
  * consecutively from the start; the same transition emits the next carry and advances the committed state.
  *   logits_dev         [total_rows][vocab] of logits_dtype (KAP_BF16 or KAP_F32): row j is the verifier's prediction
  *                      after window token j (the verify attention's window rows, through the model's head).
- *   window_offsets_dev [num_seqs+1] int32: request r owns rows [off[r], off[r+1]); every window holds >= 1 row and
- *                      off[num_seqs] = total_rows.
+ *   window_offsets_dev [num_seqs+1] int32: request r owns rows [off[r], off[r+1]); every window holds 1 to 32 rows
+ *                      and off[num_seqs] = total_rows (rows past 32 are not judged and set device error bit 4).
  *   tokens_dev         [total_rows] int32: the window's tokens; row off[r] is the carry, the rest are proposals.
  *   Rank order of a row: logit descending, lower token id first, NaN last. Proposal j passes when fewer than top_n
  *   tokens of row j - 1 come before it; a token outside [0, vocab) fails.
