@@ -406,6 +406,25 @@ int orc_accept_commit(const float *logits, int rows, int V, const int32_t *token
   return 0;
 }
 
+// Materialisation of one compact view row into a fixed-capacity workspace (KAP paper, compiler: the selected spans
+// are resolved to KV pages and materialised as a compact physical view that keeps logical positions; a plan that
+// exceeds the compact workspace falls back). The workspace of the row's request is the ws_pages pool pages from
+// ws_base. The i-th selected entry is copied to page ws_base + i; tail entries (generated tokens, written through
+// the full table) keep their pages; logical pages are unchanged. Writes the new row and the (source, destination)
+// page pairs to copy; returns their count, or -1 when the selection does not fit (the row is then left as it is and
+// nothing is copied).
+int orc_materialize_row(const int32_t *bt_row, int n_entries, int n_selected, int ws_base, int ws_pages,
+                        int32_t *out_bt_row, int32_t *copy_src, int32_t *copy_dst) {
+  for (int i = 0; i < n_entries; ++i) out_bt_row[i] = bt_row[i];
+  if (n_selected > ws_pages) return -1;
+  for (int i = 0; i < n_selected; ++i) {
+    copy_src[i] = bt_row[i];
+    copy_dst[i] = ws_base + i;
+    out_bt_row[i] = ws_base + i;
+  }
+  return n_selected;
+}
+
 int orc_hardware_threads(void) { return static_cast<int>(std::thread::hardware_concurrency()); }
 
 }  // extern "C"

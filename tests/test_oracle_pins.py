@@ -282,6 +282,50 @@ def test_accept_commit_everything_passes_with_n_at_least_v(orc):
     assert (m, sl) == (4, 15) and c == int(lg[4].argmax())
 
 
+# -------------------------------------------------- materialised compact workspace (KAP paper, compiler / fallback)
+def test_materialize_row_layout_and_fallback(orc):
+    """Selected entries go to consecutive workspace pages from the request's base, in access order; tail entries keep
+    their pages; a selection larger than the workspace is left as it is and nothing is copied."""
+    row = [5, 9, 2, 40, 41]
+    out, pairs, fits = orc.materialize_row(row, 5, 3, 100, 8)
+    assert fits and out.tolist() == [100, 101, 102, 40, 41] and pairs == [(5, 100), (9, 101), (2, 102)]
+    out, pairs, fits = orc.materialize_row(row, 5, 3, 100, 2)
+    assert not fits and out.tolist() == row and pairs == []
+    out, pairs, fits = orc.materialize_row(row, 5, 0, 100, 2)
+    assert fits and out.tolist() == row and pairs == []
+
+
+def test_materialized_view_keeps_attention_exact(orc):
+    """Copying the selected pages into the workspace and pointing the table there leaves proposal attention
+    unchanged bit for bit: the same values sit at the same logical positions (one view shared by all heads)."""
+    R, hq, hkv, d = 2, 8, 2, 64
+    ctx = np.array([70, 100], np.int32)
+    seq = ctx + 3
+    rng, bt, K, V = _toy(30, R, hq, hkv, d, tuple(ctx))
+    P0 = K.shape[0]
+    ws_pages = 6
+    K2 = np.concatenate([K, np.full((R * ws_pages,) + K.shape[1:], np.nan, np.float32)])
+    V2 = np.concatenate([V, np.full((R * ws_pages,) + V.shape[1:], np.nan, np.float32)])
+    q = rng.standard_normal((R, hq, d)).astype(np.float32)
+    cap = 5
+    sel = np.zeros((R, 1, cap), np.int32)
+    nsel = np.zeros((R, 1), np.int32)
+    bt2 = bt.copy()
+    for r in range(R):
+        N = (ctx[r] + 15) // 16
+        s = sorted(rng.choice(N, size=4, replace=False).tolist())
+        sel[r, 0, :4] = s
+        nsel[r, 0] = 4
+        out_row, pairs, fits = orc.materialize_row(bt[r, s], 4, 4, P0 + r * ws_pages, ws_pages)
+        assert fits
+        for (src, dst), lp in zip(pairs, s):
+            K2[dst], V2[dst] = K[src], V[src]
+            bt2[r, lp] = dst
+    o1, l1 = orc.attn_propose(q, K, V, bt, ctx, seq, sel, nsel)
+    o2, l2 = orc.attn_propose(q, K2, V2, bt2, ctx, seq, sel, nsel)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
 def test_select_spans_brute_force(orc):
     rng = np.random.default_rng(4)
     for _ in range(100):
