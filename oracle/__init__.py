@@ -56,7 +56,7 @@ def _load():
             lib.orc_prior_scores.restype = I
             lib.orc_accept_commit.argtypes = [P, I, I, P, I, I, P, P, P]
             lib.orc_accept_commit.restype = I
-            lib.orc_materialize_row.argtypes = [P, I, I, I, I, P, P, P]
+            lib.orc_materialize_row.argtypes = [P, P, I, I, I, I, I, P, P, P]
             lib.orc_materialize_row.restype = I
             lib.orc_select_spans.argtypes = [I, P, I, I, I, P]
             lib.orc_select_spans.restype = I
@@ -154,13 +154,15 @@ def accept_commit(logits, tokens, top_n: int, start_pos: int):
     return int(m[0]), int(c[0]), int(sl[0])
 
 
-def materialize_row(bt_row, n_entries: int, n_selected: int, ws_base: int, ws_pages: int):
+def materialize_row(bt_row, lp_row, n_entries: int, n_selected: int, ctx_len: int, ws_base: int, ws_pages: int):
     """One view row into its workspace -> (new row [n_entries], [(src page, dst page)], fits)."""
     bt = _i32(np.asarray(bt_row)[:max(n_entries, 1)])
+    lp = _i32(np.asarray(lp_row)[:max(n_entries, 1)])
     out = np.zeros(max(n_entries, 1), np.int32)
     src = np.zeros(max(n_selected, 1), np.int32)
     dst = np.zeros(max(n_selected, 1), np.int32)
-    n = _load().orc_materialize_row(_p(bt), n_entries, n_selected, ws_base, ws_pages, _p(out), _p(src), _p(dst))
+    n = _load().orc_materialize_row(_p(bt), _p(lp), n_entries, n_selected, ctx_len, ws_base, ws_pages, _p(out),
+                                    _p(src), _p(dst))
     pairs = [] if n < 0 else list(zip(src[:n].tolist(), dst[:n].tolist()))
     return out[:n_entries], pairs, n >= 0
 

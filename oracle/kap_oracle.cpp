@@ -409,20 +409,24 @@ int orc_accept_commit(const float *logits, int rows, int V, const int32_t *token
 // Materialisation of one compact view row into a fixed-capacity workspace (KAP paper, compiler: the selected spans
 // are resolved to KV pages and materialised as a compact physical view that keeps logical positions; a plan that
 // exceeds the compact workspace falls back). The workspace of the row's request is the ws_pages pool pages from
-// ws_base. The i-th selected entry is copied to page ws_base + i; tail entries (generated tokens, written through
-// the full table) keep their pages; logical pages are unchanged. Writes the new row and the (source, destination)
-// page pairs to copy; returns their count, or -1 when the selection does not fit (the row is then left as it is and
-// nothing is copied).
-int orc_materialize_row(const int32_t *bt_row, int n_entries, int n_selected, int ws_base, int ws_pages,
-                        int32_t *out_bt_row, int32_t *copy_src, int32_t *copy_dst) {
+// ws_base. The i-th selected entry is copied to page ws_base + i when all its tokens are prompt tokens (logical page
+// lp with 16 * (lp + 1) <= ctx_len); a selected page that also holds positions >= ctx_len keeps its own page, since
+// generated tokens are written through the full table into it after the copy. Tail entries keep their pages;
+// logical pages are unchanged. Writes the new row and the (source, destination) page pairs to copy; returns their
+// count, or -1 when the selection does not fit (the row is then left as it is and nothing is copied).
+int orc_materialize_row(const int32_t *bt_row, const int32_t *lp_row, int n_entries, int n_selected, int ctx_len,
+                        int ws_base, int ws_pages, int32_t *out_bt_row, int32_t *copy_src, int32_t *copy_dst) {
   for (int i = 0; i < n_entries; ++i) out_bt_row[i] = bt_row[i];
   if (n_selected > ws_pages) return -1;
+  int n = 0;
   for (int i = 0; i < n_selected; ++i) {
-    copy_src[i] = bt_row[i];
-    copy_dst[i] = ws_base + i;
+    if (kPage * (lp_row[i] + 1) > ctx_len) continue;
+    copy_src[n] = bt_row[i];
+    copy_dst[n] = ws_base + i;
+    ++n;
     out_bt_row[i] = ws_base + i;
   }
-  return n_selected;
+  return n;
 }
 
 int orc_hardware_threads(void) { return static_cast<int>(std::thread::hardware_concurrency()); }

@@ -285,13 +285,16 @@ def test_accept_commit_everything_passes_with_n_at_least_v(orc):
 # -------------------------------------------------- materialised compact workspace (KAP paper, compiler / fallback)
 def test_materialize_row_layout_and_fallback(orc):
     """Selected entries go to consecutive workspace pages from the request's base, in access order; tail entries keep
-    their pages; a selection larger than the workspace is left as it is and nothing is copied."""
-    row = [5, 9, 2, 40, 41]
-    out, pairs, fits = orc.materialize_row(row, 5, 3, 100, 8)
+    their pages; a selected page that also holds positions at or past ctx_len stays in place (generated tokens are
+    written into it through the full table later); a selection larger than the workspace is left as it is."""
+    row, lp = [5, 9, 2, 40, 41], [0, 3, 6, 7, 8]
+    out, pairs, fits = orc.materialize_row(row, lp, 5, 3, 112, 100, 8)     # 112 = 7 full pages: 0, 3, 6 all prompt
     assert fits and out.tolist() == [100, 101, 102, 40, 41] and pairs == [(5, 100), (9, 101), (2, 102)]
-    out, pairs, fits = orc.materialize_row(row, 5, 3, 100, 2)
+    out, pairs, fits = orc.materialize_row(row, lp, 5, 3, 100, 100, 8)     # page 6 holds positions 96..111 > 100
+    assert fits and out.tolist() == [100, 101, 2, 40, 41] and pairs == [(5, 100), (9, 101)]
+    out, pairs, fits = orc.materialize_row(row, lp, 5, 3, 112, 100, 2)
     assert not fits and out.tolist() == row and pairs == []
-    out, pairs, fits = orc.materialize_row(row, 5, 0, 100, 2)
+    out, pairs, fits = orc.materialize_row(row, lp, 5, 0, 112, 100, 2)
     assert fits and out.tolist() == row and pairs == []
 
 
@@ -316,11 +319,12 @@ def test_materialized_view_keeps_attention_exact(orc):
         s = sorted(rng.choice(N, size=4, replace=False).tolist())
         sel[r, 0, :4] = s
         nsel[r, 0] = 4
-        out_row, pairs, fits = orc.materialize_row(bt[r, s], 4, 4, P0 + r * ws_pages, ws_pages)
+        out_row, pairs, fits = orc.materialize_row(bt[r, s], s, 4, 4, int(ctx[r]), P0 + r * ws_pages, ws_pages)
         assert fits
-        for (src, dst), lp in zip(pairs, s):
+        for src, dst in pairs:
             K2[dst], V2[dst] = K[src], V[src]
-            bt2[r, lp] = dst
+        for i, lp in enumerate(s):
+            bt2[r, lp] = out_row[i]
     o1, l1 = orc.attn_propose(q, K, V, bt, ctx, seq, sel, nsel)
     o2, l2 = orc.attn_propose(q, K2, V2, bt2, ctx, seq, sel, nsel)
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
