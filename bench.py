@@ -46,6 +46,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prior", action="store_true", help="skip the external-prior selection timing")
     ap.add_argument("--no-accept", action="store_true", help="skip the acceptance and commit timing")
+    ap.add_argument("--no-materialize", action="store_true", help="skip the materialised-workspace timing")
     ap.add_argument("--unfused", action="store_true", help="separate KV-append and proposal launches per step")
     ap.add_argument("--no-overlap", action="store_true",
                     help="proposal kernels wait for the previous kernel before reading their view")
@@ -222,6 +223,66 @@ def time_prior(layers, steps: int, hbm_peak: float, dev):
     return {"us_per_call": us, "bytes_per_call": b, "gbs": b / (us * 1e-6) / 1e9,
             "pct_of_roofline": 100 * b / (us * 1e-6) / 1e9 / hbm_peak, "prior_layers": PRIOR_LAYERS,
             "l2": f"{len(calls)} distinct priors, {total / 1e6:.0f} MB per replay"}
+
+
+# --------------------------------------------------------------------------- materialised compact workspace
+def time_materialize(layers, steps: int, hbm_peak: float, dev):
+    """Times kap_materialize_view (KAP paper, compiler: the selected pages copied into a compact workspace) on every
+    layer's compiled view, and the first proposal step over the materialised views, each as a CUDA graph over the
+    layers. Every layer gets a copy of its pool followed by R * cap workspace pages."""
+    import torch
+    import selected_kv_sparse_gb300 as kap
+    import numpy as np
+    mats, cycles = [], []
+    gather_bytes = 0
+    for w, cyc, x in layers:
+        ws = cyc.sel_cap
+        pad = (w.R * ws,) + tuple(w.K.shape[1:])
+        K2 = torch.cat([w.K, torch.zeros(pad, dtype=w.K.dtype, device=dev)])
+        V2 = torch.cat([w.V, torch.zeros(pad, dtype=w.V.dtype, device=dev)])
+        pool2 = kap.KVPool(K2, V2, w.Hq, torch.zeros(K2.shape[0], w.Hkv, w.d, dtype=torch.float32, device=dev))
+        kap.kap_build_summaries(pool2, kap.PageMap(w.block_table, w.ctx_len, w.seq_len0))
+        tmp = kap.View.empty(w.R, cyc.rows, cyc.view_cap, dev)
+        mats.append((pool2, kap.PageMap(w.block_table, w.ctx_len), cyc.view, w.num_pages, ws, tmp))
+        c2 = kap.DecodeCycle(pool2, w.block_table, w.ctx_len, w.seq_len0, w.k_prop, w.n_q,
+                             kap.rope_inv_freq(w.d, w.theta, dev), policy=cyc.policy, workspace_pages=(w.num_pages, ws))
+        c2.plan(x["q_route"])
+        cycles.append((c2, x))
+        ns = cyc.n_sel.cpu().numpy().astype(np.int64)
+        gather_bytes += int(ns.sum()) * 2 * PAGE * w.d * 2 * 2   # K and V chunks, read once and written once
+
+    def run_mat():
+        for pool2, pmap, view, first, ws, tmp in mats:
+            kap.kap_materialize_view(pool2, pmap, view, first, ws, out_view=tmp)
+
+    def run_prop():
+        for c2, x in cycles:
+            c2.propose_step(0, x["q_prop"][0], x["k_prop"][0], x["v_prop"][0], settled=True)
+
+    out = {}
+    for name, fn in (("gather", run_mat), ("propose", run_prop)):
+        fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        n = max(3, min(steps, 50))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        out[name] = e0.elapsed_time(e1) * 1e3 / (n * len(layers))
+    gb = gather_bytes / len(layers)
+    return {"gather_us_per_layer": out["gather"], "gather_bytes_per_layer": gb,
+            "gather_gbs": gb / (out["gather"] * 1e-6) / 1e9,
+            "gather_pct_of_roofline": 100 * gb / (out["gather"] * 1e-6) / 1e9 / hbm_peak,
+            "propose_us_per_launch": out["propose"],
+            "note": "bytes = selected K+V read and written once; proposal = step 0 over the materialised views"}
 
 
 # ------------------------------------------------------------------------------- tolerant acceptance, commit
@@ -576,6 +637,7 @@ def run_kap(args, world, rank, local):
 
     prior = None if args.no_prior else time_prior(layers, K, hbm_peak, dev)
     accept = None if args.no_accept else time_accept(layers, K, hbm_peak, dev)
+    mat = None if args.no_materialize else time_materialize(layers, K, hbm_peak, dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -615,6 +677,7 @@ def run_kap(args, world, rank, local):
             "plan_us_per_layer": plan_ms * 1e3,
             "prior_topk": prior,
             "accept_commit": accept,
+            "materialize": mat,
             "phase_ms_per_step": {k2: v / K for k2, v in phase_ms.items()},
             "roofline": {"bound": "hbm", "kernel": "verify_tc_kernel", "achieved": ver_gbs, "peak": hbm_peak,
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": ver_gbs / hbm_peak, "traffic": traffic},

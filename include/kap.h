@@ -159,6 +159,25 @@ kap_status kap_prior_topk(const kap_page_map *map, const float *affinities_dev, 
                           int32_t num_heads, const kap_access_policy *policy, int32_t *sel_ids, int32_t *n_sel,
                           void *workspace, size_t workspace_bytes, kap_stream stream);
 
+/* Materialised compact workspace. KAP paper, compiler (the selected spans are resolved to KV pages and materialised
+ * as a compact physical view that keeps logical positions) and fallback (full-context access when the plan exceeds
+ * the compact workspace). Request r owns the ws_pages_per_seq pool pages from ws_first_page + r * ws_pages_per_seq,
+ * pages that no block table or view may reference otherwise (e.g. pages reserved at the end of the pool).
+ * For every row (r, v) of `view`, selected entry i is copied to workspace page i of request r when all its tokens
+ * are prompt tokens (16 * (logical page + 1) <= map->ctx_len[r]): K and V of head v for a per-head view
+ * (rows_per_seq = Hkv), of every head for a shared view (rows_per_seq = 1). A selected page that also holds
+ * positions >= ctx_len keeps its own page: generated tokens are written into it through the full table later.
+ * out_view gets the row with the copied entries pointing at the workspace; tail entries, logical pages and counts
+ * are copied unchanged. out_view may be `view` itself (rewritten in place); its cap >= view->cap.
+ * A row whose n_selected exceeds ws_pages_per_seq is copied unchanged (attention over it stays correct, reading the
+ * pool's own pages) and sets fallback_dev[r] = 1 when fallback_dev is given; the call never clears a flag.
+ * Proposal attention over out_view equals attention over `view` bit for bit.
+ * Errors: KAP_EINVAL for null pointers or sizes < 1; KAP_ESHAPE when rows_per_seq is neither 1 nor Hkv or the two
+ * views differ in it; KAP_ECAPACITY when the workspace pages run past the pool or out_view->cap < view->cap. */
+kap_status kap_materialize_view(const kap_kv_pool *pool, const kap_page_map *map, const kap_view *view,
+                                int32_t ws_first_page, int32_t ws_pages_per_seq, const kap_view *out_view,
+                                int32_t *fallback_dev, kap_stream stream);
+
 /* Tolerant acceptance and commit of verify windows. KAP paper, verifier: the window is the verifier-approved carry
  * token followed by the k proposals; a proposal is accepted when it lies within the target's top-n candidates under
  * the full context (the Top-3 rule: top_n = 3; top_n = 1 is greedy exact match); m counts the proposals accepted

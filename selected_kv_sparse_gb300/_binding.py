@@ -69,6 +69,7 @@ def _declare(lib):
         "kap_score_topk": ([P, P, P, P, P, P, P, Z, P], I),
         "kap_prior_topk": ([P, P, I, I, P, P, P, P, Z, P], I),
         "kap_accept_commit": ([P, I, I, I, I, P, P, P, I, P, P, P, P, Z, P], I),
+        "kap_materialize_view": ([P, P, P, I, I, P, P, P], I),
         "kap_accept_workspace_size": ([I, I, I], Z),
         "kap_score_workspace_size": ([I, I, I], Z),
         "kap_score_topk_view": ([P, P, P, P, P, P, P, Z, I, P, P, F, P, P, P], I),
@@ -274,6 +275,18 @@ def kap_prior_topk(pmap: PageMap, affinities: torch.Tensor, policy: AccessPolicy
                                                 int(affinities.shape[2]), ctypes.byref(pol),
                                                 _i32(sel_ids, "sel_ids"), _i32(n_sel, "n_sel"), _ptr(workspace),
                                                 workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def kap_materialize_view(pool: KVPool, pmap: PageMap, view: View, ws_first_page: int, ws_pages_per_seq: int,
+                         out_view: Optional[View] = None, fallback: Optional[torch.Tensor] = None, stream=None):
+    """Copies each view row's selected pages into its request's workspace pages of the pool and points the row
+    there (in place when out_view is None)."""
+    lib = load()
+    out_view = view if out_view is None else out_view
+    p, m, v, o = pool._c(), pmap._c(), view._c(), out_view._c()
+    _check("kap_materialize_view", lib.kap_materialize_view(
+        ctypes.byref(p), ctypes.byref(m), ctypes.byref(v), int(ws_first_page), int(ws_pages_per_seq), ctypes.byref(o),
+        _i32(fallback, "fallback") if fallback is not None else None, _stream(stream)))
 
 
 def kap_accept_workspace_size(num_seqs: int, total_rows: int, vocab: int) -> int:

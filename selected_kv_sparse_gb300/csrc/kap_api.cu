@@ -195,6 +195,32 @@ kap_status kap_prior_topk(const kap_page_map *map, const float *affinities_dev, 
                                        n_sel, static_cast<float *>(workspace), error_word(), cs(stream)));
 }
 
+kap_status kap_materialize_view(const kap_kv_pool *pool, const kap_page_map *map, const kap_view *view,
+                                int32_t ws_first_page, int32_t ws_pages_per_seq, const kap_view *out_view,
+                                int32_t *fallback_dev, kap_stream stream) {
+  kap_status st = check_pool(pool, false);
+  if (st != KAP_OK) return st;
+  if ((st = check_map(map, false)) != KAP_OK) return st;
+  if (!view || !out_view) return KAP_EINVAL;
+  const int32_t num_seqs = map->num_seqs;
+  if (!view->block_table || !view->logical_page || !view->n_entries || !view->n_selected) return KAP_EINVAL;
+  if (!out_view->block_table || !out_view->logical_page || !out_view->n_entries || !out_view->n_selected)
+    return KAP_EINVAL;
+  if (view->rows_per_seq != 1 && view->rows_per_seq != pool->num_kv_heads) return KAP_ESHAPE;
+  if (out_view->rows_per_seq != view->rows_per_seq || view->cap <= 0) return KAP_ESHAPE;
+  if (out_view->cap < view->cap) return KAP_ECAPACITY;
+  if (ws_first_page < 0 || ws_pages_per_seq <= 0) return KAP_EINVAL;
+  if (static_cast<int64_t>(ws_first_page) + static_cast<int64_t>(num_seqs) * ws_pages_per_seq > pool->num_pages)
+    return KAP_ECAPACITY;
+  if (static_cast<int64_t>(num_seqs) * view->rows_per_seq > 65535) return KAP_EUNSUPPORTED;
+  const ViewArgs in{view->rows_per_seq, view->cap, view->block_table, view->logical_page, view->n_entries,
+                    view->n_selected, 0};
+  return cuda_status(launch_materialize(pool_args(pool), num_seqs, map->ctx_len, in, out_view->block_table,
+                                        out_view->logical_page, out_view->n_entries, out_view->n_selected,
+                                        out_view->cap, ws_first_page, ws_pages_per_seq, fallback_dev, error_word(),
+                                        cs(stream)));
+}
+
 size_t kap_accept_workspace_size(int32_t num_seqs, int32_t total_rows, int32_t vocab) {
   if (num_seqs <= 0 || total_rows <= 0 || vocab <= 0) return 0;
   return accept_workspace_bytes(num_seqs, total_rows, vocab);

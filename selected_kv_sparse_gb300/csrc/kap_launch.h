@@ -55,6 +55,12 @@ cudaError_t launch_compile_view(const MapArgs &m, const int32_t *sel, const int3
 cudaError_t launch_slot_mapping(const MapArgs &m, const int32_t *tok_offsets, const int32_t *start_pos, int T,
                                 int64_t *slot_out, int32_t *pos_out, cudaStream_t s);
 
+// materialised compact workspace (k_materialize.cu): selected entries of `in` copied to the workspace pages
+cudaError_t launch_materialize(const PoolArgs &p, int R, const int32_t *ctx_len, const ViewArgs &in, int32_t *obt,
+                               int32_t *olp, int32_t *on,
+                               int32_t *onsel, int ocap, int ws_first, int ws_pages, int32_t *fallback, int *err,
+                               cudaStream_t s);
+
 // tolerant acceptance and commit of verify windows (k_accept.cu)
 size_t accept_workspace_bytes(int num_seqs, int total_rows, int vocab);
 cudaError_t launch_accept(const void *logits, int dtype, int V, const int32_t *woff, int R, int total_rows,

@@ -28,9 +28,12 @@ class DecodeCycle:
                  k_prop: int, n_q: torch.Tensor, inv_freq: torch.Tensor, policy: Optional[kb.AccessPolicy] = None,
                  spans: Optional[torch.Tensor] = None, span_offsets: Optional[torch.Tensor] = None,
                  sel_cap: Optional[int] = None, s_max: float = 1.0, fused: bool = True,
-                 outputs: Optional[dict] = None, overlap: bool = True):
+                 outputs: Optional[dict] = None, overlap: bool = True,
+                 workspace_pages: Optional[tuple] = None):
         dev = block_table.device
         self.fused = bool(fused)
+        # (first pool page, pages per request) of a materialised compact workspace, or None for the zero-copy view
+        self.workspace_pages = tuple(workspace_pages) if workspace_pages is not None else None
         self.overlap = bool(overlap)
         self._view_fresh = True  # the last launch of this cycle wrote the view (or none has run yet)
         self.pool = pool
@@ -121,6 +124,10 @@ class DecodeCycle:
                                 self.s_max, self.slots_prop, self.pos_prop, stream)
         if not self.window_is_horizon:
             kb.kap_slot_mapping(self.map_plan, self.q_offsets, self.q_start, self.slots_ver, self.pos_ver, stream)
+        if self.workspace_pages is not None:   # copy the selected pages into the workspace, view rewritten in place
+            kb.kap_materialize_view(self.pool, self.map_plan, self.view, self.workspace_pages[0],
+                                    self.workspace_pages[1],
+                                    fallback=self.fallback, stream=stream)
         self._view_fresh = True
 
     def _settled(self, override: Optional[bool]) -> bool:
@@ -176,8 +183,9 @@ class DecodeCycle:
         """Kernel launches of one run(): selection and view (score + top-K with the view fused in; unfused score,
         top-K and view; or spans and view), a separate window slot mapping when the windows differ from the
         horizon, per step one fused kernel (or an append and a proposal kernel), then the window append and
-        verification."""
+        verification; plus the materialisation when a workspace is used."""
         sel_view = 2 if self.spans is not None else (2 if self.fused else 3)
+        sel_view += 1 if self.workspace_pages is not None else 0
         slots = 0 if self.window_is_horizon else 1
         per_step = 1 if self.fused else 2
         return sel_view + slots + per_step * self.k_prop + 2

@@ -32,13 +32,26 @@ def policy_of(w, cap=None):
     return kap.AccessPolicy(a, r, k, w.per_kv_head, cap, None if same else w.ark.contiguous())
 
 
-def make_cycle(w, cap=None, fused=True, overlap=True):
-    pool = kap.KVPool(w.K, w.V, w.Hq, torch.zeros(w.num_pages, w.Hkv, w.d, dtype=torch.float32, device=w.K.device))
+def make_cycle(w, cap=None, fused=True, overlap=True, ws_pages=0, K=None, V=None):
+    """The library's cycle on workload w. ws_pages > 0: the pool tensors K, V carry ws_pages * R extra pages after
+    the workload's pool, used as the materialised compact workspace."""
+    K = w.K if K is None else K
+    V = w.V if V is None else V
+    pool = kap.KVPool(K, V, w.Hq, torch.zeros(K.shape[0], w.Hkv, w.d, dtype=torch.float32, device=w.K.device))
     inv = kap.rope_inv_freq(w.d, w.theta, w.K.device)
     pol = policy_of(w, cap)
     cyc = kap.DecodeCycle(pool, w.block_table, w.ctx_len, w.seq_len0, w.k_prop, w.n_q, inv, policy=pol,
-                          spans=w.spans, span_offsets=w.span_offsets, sel_cap=pol.cap, fused=fused, overlap=overlap)
+                          spans=w.spans, span_offsets=w.span_offsets, sel_cap=pol.cap, fused=fused, overlap=overlap,
+                          workspace_pages=(w.num_pages, ws_pages) if ws_pages else None)
     return pool, cyc
+
+
+def with_workspace(w, ws_pages):
+    """Pool tensors of w followed by R * ws_pages NaN pages (the workspace; NaN shows any read of an unused page)."""
+    pad = (w.R * ws_pages,) + tuple(w.K.shape[1:])
+    K = torch.cat([w.K, torch.full(pad, float("nan"), dtype=w.K.dtype, device=w.K.device)])
+    V = torch.cat([w.V, torch.full(pad, float("nan"), dtype=w.V.dtype, device=w.V.device)])
+    return K, V
 
 
 def oracle_selection(w, S_np, q_route_np):
@@ -72,7 +85,7 @@ def oracle_selection(w, S_np, q_route_np):
     return sel, nsel
 
 
-def run_cycle_and_oracle(w, check_rows=None, nthreads=8, fused=True):
+def run_cycle_and_oracle(w, check_rows=None, nthreads=8, fused=True, ws_pages=0):
     """Runs one full cycle on the GPU and the oracle on identical inputs (proposal steps fused with their KV append,
     or as separate append and proposal calls).
 
@@ -81,7 +94,8 @@ def run_cycle_and_oracle(w, check_rows=None, nthreads=8, fused=True):
     tokens 0..i appended (RoPE'd by the oracle itself), verify sees the window tokens appended.
     """
     dev = w.K.device
-    pool, cyc = make_cycle(w, fused=fused)
+    Kp, Vp = with_workspace(w, ws_pages) if ws_pages else (w.K, w.V)
+    pool, cyc = make_cycle(w, fused=fused, ws_pages=ws_pages, K=Kp, V=Vp)
     kap.kap_build_summaries(pool, kap.PageMap(w.block_table, w.ctx_len, w.seq_len0))
     # snapshot inputs before the cycle mutates them (q is rotated in place, the pool receives new tokens)
     K0, V0 = f32(w.K), f32(w.V)
@@ -134,8 +148,9 @@ def run_cycle_and_oracle(w, check_rows=None, nthreads=8, fused=True):
         torch.from_numpy(qrot).to(torch.bfloat16).float().numpy()
     out, lse = oracle.attn_verify(qin, K, V, bt, qo, seq0, nthreads=nthreads)
     res["ver"] = dict(o_orc=out, lse_orc=lse, o_gpu=f32(cyc.o_ver), lse_gpu=f32(cyc.lse_ver))
-    res["K_after_orc"], res["K_after_gpu"] = K, f32(w.K)
-    res["V_after_orc"], res["V_after_gpu"] = V, f32(w.V)
+    res["K_after_orc"], res["K_after_gpu"] = K, f32(Kp[:w.num_pages])
+    res["V_after_orc"], res["V_after_gpu"] = V, f32(Vp[:w.num_pages])
+    res["K_pool"], res["V_pool"] = Kp, Vp
     return res
 
 
