@@ -47,6 +47,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-prior", action="store_true", help="skip the external-prior selection timing")
     ap.add_argument("--no-accept", action="store_true", help="skip the acceptance and commit timing")
     ap.add_argument("--no-materialize", action="store_true", help="skip the materialised-workspace timing")
+    ap.add_argument("--no-side-flow", action="store_true", help="skip the EarlySelectKV side-flow timing")
     ap.add_argument("--unfused", action="store_true", help="separate KV-append and proposal launches per step")
     ap.add_argument("--no-overlap", action="store_true",
                     help="proposal kernels wait for the previous kernel before reading their view")
@@ -223,6 +224,58 @@ def time_prior(layers, steps: int, hbm_peak: float, dev):
     return {"us_per_call": us, "bytes_per_call": b, "gbs": b / (us * 1e-6) / 1e9,
             "pct_of_roofline": 100 * b / (us * 1e-6) / 1e9 / hbm_peak, "prior_layers": PRIOR_LAYERS,
             "l2": f"{len(calls)} distinct priors, {total / 1e6:.0f} MB per replay"}
+
+
+# ------------------------------------------------------------------------------ EarlySelectKV side flow
+def time_side_flow(steps: int, dev, layers_n: int = 8):
+    """EarlySelectKV-shaped decode steps (40960-token prompts, Hq 32, Hkv 8, d 128, A0R0K8 per KV head on a proxy
+    query = q + N(0, 0.3^2)) over a stack of layers, batch 1 and 8: routing (scores, top-K, view) and the step's
+    append + proposal attention per layer, run in turn on one stream or with the next layer's routing on a second
+    stream (SideFlowDecode). Each schedule is one CUDA graph per decode step."""
+    import torch
+    import selected_kv_sparse_gb300 as kap
+    from workloads import make_workload
+    out = {}
+    for batch in (1, 8):
+        layers = []
+        for l in range(layers_n):
+            w = make_workload("early", device=dev, batch=batch, seed_offset=100 + l, poison=False)
+            pool = kap.KVPool(w.K, w.V, w.Hq, torch.zeros(w.num_pages, w.Hkv, w.d, dtype=torch.float32, device=dev))
+            kap.kap_build_summaries(pool, kap.PageMap(w.block_table, w.ctx_len, w.seq_len0))
+            a, r, k = (int(x) for x in w.ark[0].tolist())
+            cyc = kap.DecodeCycle(pool, w.block_table, w.ctx_len, w.seq_len0, w.k_prop, w.n_q,
+                                  kap.rope_inv_freq(w.d, w.theta, dev), policy=kap.AccessPolicy(a, r, k, True, w.sel_cap()))
+            layers.append((w, cyc))
+        flow = kap.SideFlowDecode([c for _, c in layers])
+        args = ([w.q_route for w, _ in layers], [w.q_prop[0] for w, _ in layers],
+                [w.k_new_prop[0] for w, _ in layers], [w.v_new_prop[0] for w, _ in layers])
+        res = {}
+        for name, ov in (("sequential", False), ("side_flow", True)):
+            flow.step(*args, overlap=ov)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                flow.step(*args, overlap=ov)
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize()
+            n = max(3, min(steps, 50))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(n):
+                g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            res[name] = e0.elapsed_time(e1) * 1e3 / n
+        out[f"batch{batch}"] = {"us_per_step_sequential": res["sequential"], "us_per_step_side_flow": res["side_flow"],
+                                "decode_steps_per_s": 1e6 / res["side_flow"],
+                                "speedup": res["sequential"] / res["side_flow"]}
+        del layers, flow
+        torch.cuda.empty_cache()
+    out["layers"] = layers_n
+    out["workload"] = ("EarlySelectKV-shaped: 40960-token prompts, Hq 32, Hkv 8, d 128, A0R0K8 per KV head on a "
+                       "proxy query; a step = routing + append + proposal attention per layer")
+    return out
 
 
 # --------------------------------------------------------------------------- materialised compact workspace
@@ -638,6 +691,7 @@ def run_kap(args, world, rank, local):
     prior = None if args.no_prior else time_prior(layers, K, hbm_peak, dev)
     accept = None if args.no_accept else time_accept(layers, K, hbm_peak, dev)
     mat = None if args.no_materialize else time_materialize(layers, K, hbm_peak, dev)
+    side = None if args.no_side_flow else time_side_flow(K, dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -678,6 +732,7 @@ def run_kap(args, world, rank, local):
             "prior_topk": prior,
             "accept_commit": accept,
             "materialize": mat,
+            "early_side_flow": side,
             "phase_ms_per_step": {k2: v / K for k2, v in phase_ms.items()},
             "roofline": {"bound": "hbm", "kernel": "verify_tc_kernel", "achieved": ver_gbs, "peak": hbm_peak,
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": ver_gbs / hbm_peak, "traffic": traffic},

@@ -822,7 +822,12 @@ cudaError_t launch_tdg(const Params &prm, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr[dev & 63] = true;
   }
+  // One CTA per SM, but no more CTAs than the view can feed with a page per consumer warp (its capacity bounds
+  // the entries): a small launch then leaves SMs free for work on other streams, at the same latency, since a
+  // CTA's warps take its pages in parallel.
   int nb = device_sm_count();
+  const int64_t feed = (static_cast<int64_t>(prm.nrows) * prm.vcap + kNCW - 1) / kNCW;
+  if (feed < nb) nb = static_cast<int>(feed < 1 ? 1 : feed);
   if (nb > kMaxSlotsExtraCtas) nb = kMaxSlotsExtraCtas;
   launch_pdl(kern, dim3(nb), dim3(kThreads), C::SMEM, s, prm);
   return cudaGetLastError();

@@ -189,3 +189,46 @@ class DecodeCycle:
         slots = 0 if self.window_is_horizon else 1
         per_step = 1 if self.fused else 2
         return sel_view + slots + per_step * self.k_prop + 2
+
+
+class SideFlowDecode:
+    """EarlySelectKV side flow over a stack of layers: the routing of layer l + 1 (scores on a proxy query, top-K,
+    compact view) runs on a second stream while layer l appends its token and attends on the main stream.
+
+    EarlySelectKV page: selection stops waiting for the target layer's query; a proxy available earlier drives the
+    routing, so its latency hides behind the attention of the layers before. Layer l's attention waits only for its
+    own routing (an event); the routing of layer l + 1 waits for nothing of layer l. Every call allocates nothing,
+    so a step can be captured in a CUDA graph (the side stream forks from and joins the capturing stream).
+    `cycles` are one DecodeCycle per layer, each with one proposal step per decode step.
+    """
+
+    def __init__(self, cycles, side_stream: Optional[torch.cuda.Stream] = None):
+        self.cycles = list(cycles)
+        self.side = side_stream if side_stream is not None else torch.cuda.Stream(self.cycles[0].view.block_table.device)
+        self.routed = [torch.cuda.Event() for _ in self.cycles]
+
+    def step(self, q_route, q, k_new, v_new, overlap: bool = True):
+        """One decode step over every layer: q_route[l] is layer l's proxy query, q[l], k_new[l], v_new[l] its
+        step token's query, key and value. overlap=False runs routing and attention of each layer in turn on the
+        current stream (the same calls, the same results)."""
+        main = torch.cuda.current_stream()
+        L = len(self.cycles)
+        if not overlap:
+            for l, c in enumerate(self.cycles):
+                c.plan(q_route[l], main)
+                c.propose_step(0, q[l], k_new[l], v_new[l], main)
+            return
+        self.side.wait_stream(main)  # the step's inputs are ready on the main stream
+        with torch.cuda.stream(self.side):
+            self.cycles[0].plan(q_route[0], self.side)
+            self.routed[0].record(self.side)
+        for l, c in enumerate(self.cycles):
+            if l + 1 < L:   # next layer's routing goes out first, so that it runs while this layer attends
+                with torch.cuda.stream(self.side):
+                    self.cycles[l + 1].plan(q_route[l + 1], self.side)
+                    self.routed[l + 1].record(self.side)
+            main.wait_event(self.routed[l])
+            # the view was written on the other stream and is complete: the kernel just ahead of this one on the
+            # main stream is the previous layer's proposal, so the view may be treated as settled
+            c.propose_step(0, q[l], k_new[l], v_new[l], main, settled=True)
+        main.wait_stream(self.side)
