@@ -85,7 +85,7 @@ def oracle_selection(w, S_np, q_route_np):
     return sel, nsel
 
 
-def run_cycle_and_oracle(w, check_rows=None, nthreads=8, fused=True, ws_pages=0):
+def run_cycle_and_oracle(w, check_rows=None, nthreads=8, fused=True, ws_pages=0, cap=None):
     """Runs one full cycle on the GPU and the oracle on identical inputs (proposal steps fused with their KV append,
     or as separate append and proposal calls).
 
@@ -95,7 +95,7 @@ def run_cycle_and_oracle(w, check_rows=None, nthreads=8, fused=True, ws_pages=0)
     """
     dev = w.K.device
     Kp, Vp = with_workspace(w, ws_pages) if ws_pages else (w.K, w.V)
-    pool, cyc = make_cycle(w, fused=fused, ws_pages=ws_pages, K=Kp, V=Vp)
+    pool, cyc = make_cycle(w, cap=cap, fused=fused, ws_pages=ws_pages, K=Kp, V=Vp)
     kap.kap_build_summaries(pool, kap.PageMap(w.block_table, w.ctx_len, w.seq_len0))
     # snapshot inputs before the cycle mutates them (q is rotated in place, the pool receives new tokens)
     K0, V0 = f32(w.K), f32(w.V)
