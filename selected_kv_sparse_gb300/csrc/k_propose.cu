@@ -71,7 +71,9 @@ struct Cfg {
   static constexpr int SLOT = 2 * CHUNK;                  // K and V of one entry
   static constexpr int SLOTS_FIT = (226 * 1024 - FIXED) / (SLOT + 32);  // 1 KiB left for static shared memory
   static constexpr int SLOTS = SLOTS_FIT > 32 ? 32 : SLOTS_FIT;
-  static constexpr int BATCH = SLOTS < 16 ? SLOTS : 16;   // entries the producer handles per step
+  // entries the producer handles per step: small enough that a step waiting on one slot's consumer holds back few
+  // copies (8 measured best against 2, 4 and 16)
+  static constexpr int BATCH = SLOTS < 8 ? SLOTS : 8;
   static constexpr int OFF_KV = 0;
   static constexpr int OFF_COMB = OFF_KV + SLOTS * SLOT;
   static constexpr int OFF_WLOG = OFF_COMB + COMB;
@@ -226,14 +228,12 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
 
   // Entry offsets of the rows (one parallel load of every row's count, a block scan in shared memory), then E,
   // this CTA's range and the row holding its first entry. Rows beyond kMaxRowsScan use a warp scan in global order.
-  if (tid == 0) {
-    for (int i = 0; i < C::SLOTS; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
-    }
+  if (tid < C::SLOTS) {  // one slot's barriers per thread
+    mbar_init(&full[tid], 1);
+    mbar_init(&empty[tid], 1);
     fence_barrier_init();
+    smeta[tid].w = -1;  // no entry issued yet (shared memory keeps an earlier launch's stamps)
   }
-  if (tid < C::SLOTS) smeta[tid].w = -1;  // no entry issued yet (shared memory keeps an earlier launch's stamps)
   // A settled view lets the row scan, the segment tables and the copies of pure prompt pages run while the previous
   // kernel finishes; everything else waits for it (consumers below, the producer at its first other entry).
   if (!p.settled) grid_dependency_sync();
