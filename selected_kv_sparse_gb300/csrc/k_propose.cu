@@ -14,7 +14,7 @@
 //  * A producer warp streams the CTA's entries through a ring of page slots: per entry one 1-D bulk copy
 //    (cp.async.bulk) of the 4 KiB (page, head) chunk of K and one of V, completing on the slot's mbarrier. A view
 //    entry and its row's lengths are loaded together, so a copy leaves two dependent loads after the kernel starts.
-//  * The range is cut into windows of at most 11 row segments. Each segment gets its own group of consumer warps
+//  * The range is cut into windows of at most 10 row segments. Each segment gets its own group of consumer warps
 //    (one at least, the others in proportion to its entries) that takes the segment's entries round-robin, so all
 //    segments of a window stream at once. Lane l holds 16 bytes of each token row; packed fp32 pair FMAs form the
 //    G heads' partial dot products and the P.V update, and a reduce-scatter across the lanes of a token row leaves
@@ -31,7 +31,7 @@
 namespace kap {
 namespace {
 
-constexpr int kNCW = 11;                     // consumer warps (12 warps in all: 3 per SM sub-partition)
+constexpr int kNCW = 10;                     // consumer warps (11 in all with the producer; 9, 10, 11 measured)
 constexpr int kThreads = (kNCW + 1) * 32;    // + the producer warp (warp kNCW)
 constexpr int kMaxSlotsExtraCtas = 4096;     // bound on the grid, for workspace sizing
 constexpr int kMaxSeg = kNCW;                // row segments per window (each gets at least one warp)
