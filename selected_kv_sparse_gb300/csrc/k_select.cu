@@ -43,7 +43,7 @@ __global__ void __launch_bounds__(128) summaries_kernel(const T *__restrict__ K,
 // summary loads are in flight (unconditionally, from clamped page ids) while the group-summed query is formed.
 // Dot products follow the fixed order: lane l accumulates fmaf over i = l, l+32, ...; then an xor-butterfly
 // 16, 8, 4, 2, 1.
-constexpr int kScorePagesPerWarp = 8;
+constexpr int kScorePagesPerWarp = 4;  // 4 and 8 measured: more, smaller CTAs (fewer registers) win slightly
 constexpr int kScorePagesPerCta = 8 * kScorePagesPerWarp;
 constexpr int kMaxPooledHeads = 16;
 
