@@ -13,6 +13,7 @@ BIG = [
     dict(name="llama"),                                  # the benchmark workload: 4 x 32768 tokens, A1R2K125
     dict(name="llama", unfused=True),
     dict(name="long"),                                   # 131072 tokens, 451-page span view, 8 proposals
+    dict(name="early", batch=8),                         # 8 x 40960 tokens, A0R0K8 per KV head on a noisy proxy
     dict(name="mixed", scale=1 / 4),                     # 32 requests, 1K-32K tokens, many short rows per CTA
 ]
 
