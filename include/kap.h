@@ -126,7 +126,9 @@ kap_status kap_build_summaries(const kap_kv_pool *pool, const kap_page_map *map,
  *               Shared selection (per_kv_head = 0): score = sum over h ascending of the per-head scores.
  *   sel_ids   [R][rows][cap] out: selected prompt pages ascending; rows = Hkv or 1.
  *   n_sel     [R][rows] out: count = min(N, a + r + k) with N = ceil(ctx_len/16).
- *   workspace >= kap_score_workspace_size(...) bytes of device memory (scores). */
+ *   workspace >= kap_score_workspace_size(...) bytes of device memory (scores).
+ * Errors: KAP_EINVAL for a null or misaligned pointer or a negative a, r or k; KAP_ECAPACITY for a workspace or a
+ * cap too small; KAP_EUNSUPPORTED when R * rows > 65535 or the top-K row (4 bytes per page) exceeds 200 KiB. */
 kap_status kap_score_topk(const kap_kv_pool *pool, const kap_page_map *map, const void *q_dev,
                           const kap_access_policy *policy, int32_t *sel_ids, int32_t *n_sel,
                           void *workspace, size_t workspace_bytes, kap_stream stream);

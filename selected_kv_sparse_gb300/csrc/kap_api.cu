@@ -141,6 +141,7 @@ kap_status score_topk_common(const kap_kv_pool *pool, const kap_page_map *map, c
   const size_t topk_smem = static_cast<size_t>(map->max_pages) * 4 + (vw ? static_cast<size_t>(policy->cap) * 4 : 0);
   if (topk_smem > 200 * 1024) return KAP_EUNSUPPORTED;
   const int rows = policy->per_kv_head ? pool->num_kv_heads : 1;
+  if (static_cast<int64_t>(map->num_seqs) * rows > 65535) return KAP_EUNSUPPORTED;  // score grid rows
   if (workspace_bytes < kap_score_workspace_size(map->num_seqs, rows, map->max_pages)) return KAP_ECAPACITY;
   const PoolArgs pa = pool_args(pool);
   const MapArgs ma = map_args(map);

@@ -57,6 +57,10 @@ def test_capacities_are_checked(abi):
     assert call(b._Policy(1, 1, 5, 1, 3, None), 16, 1 << 20) == KAP_ECAPACITY
     # a score workspace one byte short
     assert call(b._Policy(1, 1, 1, 1, 4, None), 4, ws_need - 1) == KAP_ECAPACITY
+    # more (request, KV head) rows than the scoring grid can hold: 32768 requests x 2 KV heads
+    assert lib.kap_score_topk(_ref(_pool(b)), _ref(_map(b, R=32768)), ctypes.c_void_p(ADDR),
+                              _ref(b._Policy(1, 1, 1, 1, 4, None)), ctypes.c_void_p(ADDR), ctypes.c_void_p(ADDR),
+                              ctypes.c_void_p(ADDR), Z(1 << 40), None) == KAP_EUNSUPPORTED
     # a view too small for the selection plus the horizon's tail pages: cap 4 + ceil(16/16) + 1 > 5
     view = b._View(2, 5, ADDR, ADDR, ADDR, ADDR, 0)
     assert lib.kap_compile_view(_ref(_map(b)), ctypes.c_void_p(ADDR), ctypes.c_void_p(ADDR), 2, 4, 16, _ref(view),
