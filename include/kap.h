@@ -117,6 +117,19 @@ typedef struct {
  * Requires pool->k_summary. Pages shared between requests must agree on n. */
 kap_status kap_build_summaries(const kap_kv_pool *pool, const kap_page_map *map, kap_stream stream);
 
+/* Refresh of the K summaries of listed pages: for each i < num_listed, the physical page pages_dev[i] with
+ * n = n_valid_dev[i] valid tokens (1 <= n <= 16) gets k_summary[page][h][:] = (sum over t < n of K[page][h][t][:],
+ * fp32, t ascending) / n, the same arithmetic as kap_build_summaries, so a refreshed page equals a full rebuild bit
+ * for bit. EarlySelectKV page (the K-summary cache is kept up to date as the context grows). Use it when committed
+ * tokens enter the prompt (ctx_len grows): the partial last prompt page and any new prompt pages are listed; a full
+ * rebuild would re-read every prompt page. Appends of generated tokens need no refresh, since summaries cover prompt
+ * tokens only. Listed pages must be distinct (two CTAs would write one summary).
+ *   pages_dev, n_valid_dev [num_listed] int32, device.
+ * Errors: KAP_EINVAL for a null pointer or num_listed < 0; the pool checks of kap_build_summaries. A page outside the
+ * pool or a count outside [1, 16] is skipped on the device and reported through kap_device_error. */
+kap_status kap_refresh_summaries(const kap_kv_pool *pool, const int32_t *pages_dev, const int32_t *n_valid_dev,
+                                 int32_t num_listed, kap_stream stream);
+
 /* Page scoring and A/R/K top-K. KRI page (KRI-Q row; A<a>R<r>K<k> tag and its 128-block example) and
  * EarlySelectKV page (routing ranks pages by their K summaries, possibly against a proxy query).
  *   q_dev     [R][Hq][d] pool dtype: the routing query (the real query or a proxy).

@@ -66,6 +66,7 @@ def _declare(lib):
     F = ctypes.c_float
     sig = {
         "kap_build_summaries": ([P, P, P], I),
+        "kap_refresh_summaries": ([P, P, P, I, P], I),
         "kap_score_topk": ([P, P, P, P, P, P, P, Z, P], I),
         "kap_prior_topk": ([P, P, I, I, P, P, P, P, Z, P], I),
         "kap_accept_commit": ([P, I, I, I, I, P, P, P, I, P, P, P, P, Z, P], I),
@@ -245,6 +246,17 @@ def kap_build_summaries(pool: KVPool, pmap: PageMap, stream=None):
     lib = load()
     p, m = pool._c(), pmap._c()
     _check("kap_build_summaries", lib.kap_build_summaries(ctypes.byref(p), ctypes.byref(m), _stream(stream)))
+
+
+def kap_refresh_summaries(pool: KVPool, pages: torch.Tensor, n_valid: torch.Tensor, stream=None):
+    """Recomputes the K summaries of the listed physical pages (int32, device) over their n_valid first tokens."""
+    lib = load()
+    if pages.shape != n_valid.shape or pages.dim() != 1:
+        raise ValueError("pages and n_valid must be 1-D and of equal length")
+    p = pool._c()
+    _check("kap_refresh_summaries", lib.kap_refresh_summaries(ctypes.byref(p), _i32(pages, "pages"),
+                                                              _i32(n_valid, "n_valid"), pages.numel(),
+                                                              _stream(stream)))
 
 
 def kap_score_workspace_size(R: int, rows_per_seq: int, max_pages: int) -> int:

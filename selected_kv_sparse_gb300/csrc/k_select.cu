@@ -37,6 +37,33 @@ __global__ void __launch_bounds__(128) summaries_kernel(const T *__restrict__ K,
   }
 }
 
+// Refresh of listed pages: one CTA per (physical page, valid-token count) pair, the same arithmetic as
+// summaries_kernel, so a refreshed page equals a full rebuild of it bit for bit.
+template <class T>
+__global__ void __launch_bounds__(128) refresh_summaries_kernel(const T *__restrict__ K, float *__restrict__ S,
+                                                                int num_pages, int hkv, int d,
+                                                                const int32_t *__restrict__ pages,
+                                                                const int32_t *__restrict__ n_valid, int *err) {
+  grid_dependency_sync();
+  const int page = pages[blockIdx.x];
+  const int n = n_valid[blockIdx.x];
+  if (page < 0 || page >= num_pages) {
+    if (threadIdx.x == 0) set_error(err, kErrPage);
+    return;
+  }
+  if (n < 1 || n > kPage) {
+    if (threadIdx.x == 0) set_error(err, kErrLength);
+    return;
+  }
+  for (int idx = threadIdx.x; idx < hkv * d; idx += blockDim.x) {
+    const int h = idx / d, i = idx - h * d;
+    const T *base = K + (static_cast<size_t>(page) * hkv + h) * kPage * d + i;
+    float acc = 0.0f;
+    for (int t = 0; t < n; ++t) acc = __fadd_rn(acc, to_f(base[static_cast<size_t>(t) * d]));
+    S[(static_cast<size_t>(page) * hkv + h) * d + i] = __fdiv_rn(acc, static_cast<float>(n));
+  }
+}
+
 // ---------------------------------------------------------------------------------------------- scores
 // grid.x: chunks of 64 logical pages; grid.y: (request, selection row). 8 warps; each warp scores 8 pages. The
 // prompt length, the warp's block-table entries and the query rows are loaded together, and the first head's
@@ -588,6 +615,18 @@ cudaError_t launch_build_summaries(const PoolArgs &p, const MapArgs &m, int *err
   else
     launch_pdl(summaries_kernel<float>, grid, dim3(128), 0, s, static_cast<const float *>(p.k), p.ksum, p.num_pages,
                p.hkv, p.d, m.bt, m.max_pages, m.ctx_len, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_refresh_summaries(const PoolArgs &p, const int32_t *pages, const int32_t *n_valid, int n, int *err,
+                                     cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  if (p.dtype == 0)
+    launch_pdl(refresh_summaries_kernel<__nv_bfloat16>, dim3(n), dim3(128), 0, s,
+               static_cast<const __nv_bfloat16 *>(p.k), p.ksum, p.num_pages, p.hkv, p.d, pages, n_valid, err);
+  else
+    launch_pdl(refresh_summaries_kernel<float>, dim3(n), dim3(128), 0, s, static_cast<const float *>(p.k), p.ksum,
+               p.num_pages, p.hkv, p.d, pages, n_valid, err);
   return cudaGetLastError();
 }
 

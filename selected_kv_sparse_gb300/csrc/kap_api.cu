@@ -117,6 +117,17 @@ kap_status kap_build_summaries(const kap_kv_pool *pool, const kap_page_map *map,
   return cuda_status(launch_build_summaries(pool_args(pool), map_args(map), error_word(), cs(stream)));
 }
 
+kap_status kap_refresh_summaries(const kap_kv_pool *pool, const int32_t *pages_dev, const int32_t *n_valid_dev,
+                                 int32_t num_listed, kap_stream stream) {
+  kap_status st = check_pool(pool, true);
+  if (st != KAP_OK) return st;
+  if (num_listed < 0) return KAP_EINVAL;
+  if (num_listed == 0) return KAP_OK;
+  if (!pages_dev || !n_valid_dev) return KAP_EINVAL;
+  return cuda_status(
+      launch_refresh_summaries(pool_args(pool), pages_dev, n_valid_dev, num_listed, error_word(), cs(stream)));
+}
+
 size_t kap_score_workspace_size(int32_t num_seqs, int32_t rows_per_seq, int32_t max_pages) {
   if (num_seqs <= 0 || rows_per_seq <= 0 || max_pages <= 0) return 0;
   return static_cast<size_t>(num_seqs) * rows_per_seq * max_pages * sizeof(float);

@@ -26,6 +26,8 @@ struct ViewArgs {
 
 // selection kernels (k_select.cu)
 cudaError_t launch_build_summaries(const PoolArgs &p, const MapArgs &m, int *err, cudaStream_t s);
+cudaError_t launch_refresh_summaries(const PoolArgs &p, const int32_t *pages, const int32_t *n_valid, int n, int *err,
+                                     cudaStream_t s);
 cudaError_t launch_score(const PoolArgs &p, const MapArgs &m, const void *q, int per_head, float *scores,
                          int *err, cudaStream_t s);
 // Outputs of view compilation fused into top-K (see kap_score_topk_view).

@@ -94,3 +94,16 @@ def test_next_row_entry_points_check_their_arguments(abi):
     v3 = b._View(3, 6, ADDR, ADDR, ADDR, ADDR, 0)
     assert lib.kap_materialize_view(_ref(_pool(b, P=8)), _ref(_map(b)), _ref(v3), 0, 2, _ref(v3), None, None) == \
         KAP_ESHAPE
+
+
+def test_refresh_checks_its_arguments(abi):
+    b, lib = abi
+    P = ctypes.c_void_p(ADDR)
+    assert lib.kap_refresh_summaries(_ref(_pool(b)), P, P, -1, None) == KAP_EINVAL      # negative count
+    assert lib.kap_refresh_summaries(_ref(_pool(b)), None, P, 3, None) == KAP_EINVAL    # no page list
+    assert lib.kap_refresh_summaries(_ref(_pool(b)), P, None, 3, None) == KAP_EINVAL    # no counts
+    assert lib.kap_refresh_summaries(_ref(_pool(b)), P, P, 0, None) == 0               # nothing listed: no launch
+    bad = _pool(b)
+    bad.k_summary = None
+    assert lib.kap_refresh_summaries(_ref(bad), P, P, 3, None) == KAP_EINVAL            # pool without summaries
+    assert lib.kap_refresh_summaries(_ref(_pool(b, d=96)), P, P, 3, None) == KAP_EUNSUPPORTED
