@@ -13,7 +13,8 @@
  * Conventions shared by every entry point
  *   - Every pointer argument named *_dev, and every pointer inside the structs below, is DEVICE memory owned by
  *     the caller. The library never allocates, frees or synchronises on these calls; all launches go to `stream`
- *     (NULL = the legacy default stream), so every call can be captured in a CUDA graph.
+ *     (NULL = the legacy default stream), so the calls that take their workspace from the caller can be captured
+ *     in a CUDA graph.
  *   - KV pool layout: K and V are separate arrays [num_pages][num_kv_heads][16][head_dim] of the pool dtype.
  *     One (page, head) chunk is 16*head_dim*elem bytes and contiguous.
  *   - Query head hq reads KV head hq / (num_q_heads / num_kv_heads) (grouped-query attention).
