@@ -22,6 +22,7 @@ CASES = [
     dict(name="mixed", scale=1 / 64, batch=72, ragged=True),
     dict(name="llama", scale=1 / 32, n_q_override=5),   # verify window k + 1 (carry + 4 candidates)
     dict(name="llama", scale=1 / 32, n_q_override=2),   # window shorter than the proposals: appends stay visible
+    dict(name="llama", scale=1 / 32, n_q_override=16),  # G * n_q = 64 query columns: the widest verification tile
     # proposal steps as separate kap_append_kv + kap_attn_propose calls (the others use kap_append_propose)
     dict(name="tiny", unfused=True),
     dict(name="llama", scale=1 / 16, unfused=True),
