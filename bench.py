@@ -729,6 +729,11 @@ def run_kap(args, world, rank, local):
                        "us_per_launch": ver_launch_ms * 1e3, "bytes_per_launch": ver_bytes_launch,
                        "steps_per_s": 1e3 / ver_launch_ms},
             "plan_us_per_layer": plan_ms * 1e3,
+            "plan": {"us_per_layer": plan_ms * 1e3, "score_bytes_per_layer": b_score / L,
+                     "gbs": (b_score / L) / (plan_ms * 1e-3) / 1e9,
+                     "pct_of_roofline": 100 * (b_score / L) / (plan_ms * 1e-3) / 1e9 / hbm_peak,
+                     "note": "scoring bytes (one fp32 summary per prompt page and KV head) over the whole plan "
+                             "phase: scores, top-K and view"},
             "prior_topk": prior,
             "accept_commit": accept,
             "materialize": mat,
