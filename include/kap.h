@@ -121,10 +121,11 @@ kap_status kap_build_summaries(const kap_kv_pool *pool, const kap_page_map *map,
 /* Refresh of the K summaries of listed pages: for each i < num_listed, the physical page pages_dev[i] with
  * n = n_valid_dev[i] valid tokens (1 <= n <= 16) gets k_summary[page][h][:] = (sum over t < n of K[page][h][t][:],
  * fp32, t ascending) / n, the same arithmetic as kap_build_summaries, so a refreshed page equals a full rebuild bit
- * for bit. EarlySelectKV page (the K-summary cache is kept up to date as the context grows). Use it when committed
- * tokens enter the prompt (ctx_len grows): the partial last prompt page and any new prompt pages are listed; a full
- * rebuild would re-read every prompt page. Appends of generated tokens need no refresh, since summaries cover prompt
- * tokens only. Listed pages must be distinct (two CTAs would write one summary).
+ * for bit. EarlySelectKV page: routing scores pages against a K-summary cache held beside the KV pool; the page
+ * does not say when that cache is updated. Here it changes only when committed tokens enter the prompt (ctx_len
+ * grows): list the partial last prompt page and any new prompt pages; a full rebuild would re-read every prompt
+ * page. Appends of generated tokens need no refresh, since summaries cover prompt tokens only. Listed pages must be
+ * distinct (two CTAs would write one summary).
  *   pages_dev, n_valid_dev [num_listed] int32, device.
  * Errors: KAP_EINVAL for a null pointer or num_listed < 0; the pool checks of kap_build_summaries. A page outside the
  * pool or a count outside [1, 16] is skipped on the device and reported through kap_device_error. */
