@@ -14,37 +14,52 @@
 //  * A producer warp streams the CTA's entries through a ring of page slots: per entry one 1-D bulk copy
 //    (cp.async.bulk) of the 4 KiB (page, head) chunk of K and one of V, completing on the slot's mbarrier. A view
 //    entry and its row's lengths are loaded together, so a copy leaves two dependent loads after the kernel starts.
-//  * The range is cut into windows of at most 10 row segments. Each segment gets its own group of consumer warps
+//    The window's entries past the ring's first fill are prefetched into L2 at the same time.
+//  * The range is cut into windows of at most NSEG row segments. Each segment gets its own group of consumer warps
 //    (one at least, the others in proportion to its entries) that takes the segment's entries round-robin, so all
-//    segments of a window stream at once. Lane l holds 16 bytes of each token row; packed fp32 pair FMAs form the
-//    G heads' partial dot products and the P.V update, and a reduce-scatter across the lanes of a token row leaves
-//    each lane a few finished logits. Each warp keeps its own running max, sum and output; the max is only raised
-//    (and the state rescaled) when a page exceeds it by more than 2^8, which is exact.
+//    segments of a window stream at once. The group's first warp prepares the segment's query once (rotated,
+//    rounded, scaled) and, fused, the step token's key and value, in shared memory for the whole group. Lane l
+//    holds 16 bytes of each token row; packed fp32 pair FMAs form the G heads' partial dot products, a few vector
+//    rows at a time, and a reduce-scatter across the lanes of a token row leaves each lane a few finished logits.
+//    Each warp keeps its own running max, sum and output; the max is only raised (and the state rescaled) when a
+//    page exceeds it by more than 2^8, which is exact.
 //  * A group that has finished its segment combines its warps' states behind its own named barrier and writes the
 //    row's output, or hands a partial record to the row's last CTA, while the other groups keep streaming.
-//  * Fused append: the step token of request r sits at position P = seq_len[r] - 1. Every warp loads the token's
-//    key and value with its query and rotates both key and query at P; the warp that consumes the page holding P
-//    writes K and V into the pool and patches its shared-memory copy of the page before using it.
+//  * Fused append: the step token of request r sits at position P = seq_len[r] - 1. The warp that consumes the page
+//    holding P writes the prepared K and V into the pool and patches its shared-memory copy of the page first.
 #include "kap_device.cuh"
 #include "kap_launch.h"
 
 namespace kap {
 namespace {
 
-constexpr int kNCW = 10;                     // consumer warps (11 in all with the producer; 9, 10, 11 measured)
-constexpr int kThreads = (kNCW + 1) * 32;    // + the producer warp (warp kNCW)
 constexpr int kMaxSlotsExtraCtas = 4096;     // bound on the grid, for workspace sizing
-constexpr int kMaxSeg = kNCW;                // row segments per window (each gets at least one warp)
-constexpr int kMaxRowsScan = 512;            // rows whose entry offsets are scanned into shared memory at once
-constexpr int kBarSeg0 = 1;                  // named barriers kBarSeg0 .. kBarSeg0 + kMaxSeg - 1, one per segment
+constexpr int kMaxRowsScan = 256;            // rows whose entry offsets are scanned into shared memory at once
+constexpr int kBarSeg0 = 1;                  // named barriers kBarSeg0 .. kBarSeg0 + NSEG - 1, one per segment
 constexpr int kMergeChunk = 8;               // partial records loaded at once by a merging CTA
+constexpr int kPrefetchAhead = 32;           // entries beyond the ring prefetched into L2 per window
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;    // log2 units
-static_assert(kBarSeg0 + kMaxSeg <= 16, "named barriers");
+
+// Consumer warps per CTA (one CTA per SM). A CTA's warps are a multiple of 4 less the producer's share: each of
+// the SM's four sub-partitions holds a quarter of the register file and warps are dealt to them in turn, so 12
+// warps leave 168 registers a lane. fp32 pages of d = 128 (twice the bytes per slot) keep 8 warps so that the ring
+// still holds more slots than there are consumers. (Half-SM CTAs, which let the next launch's CTA start beside
+// this one, and 15 consumer warps at 128 registers were measured slower.)
+template <class T, int D, int G> struct Shape {
+  static constexpr int NCW = (sizeof(T) == 4 && D == 128) ? 7 : 11;
+  static constexpr int MINB = 1;
+  static constexpr int THREADS = (NCW + 1) * 32;  // + the producer warp (warp NCW)
+  // registers per thread: the SM's 64K over the resident threads, a multiple of 8, at most 248
+  static constexpr int MAXREG = ((65536 / (MINB * THREADS)) / 8) * 8 > 248 ? 248 : ((65536 / (MINB * THREADS)) / 8) * 8;
+};
 
 template <class T, int D, int G>
 struct Cfg {
+  static constexpr int NCW = Shape<T, D, G>::NCW;
+  static constexpr int MINB = Shape<T, D, G>::MINB;
+  static constexpr int THREADS = Shape<T, D, G>::THREADS;
   static constexpr int ESZ = sizeof(T);
   static constexpr int EPL = 16 / ESZ;           // elements per 16-byte vector
   static constexpr int EP2 = EPL / 2;            // fp32 pairs per vector
@@ -52,24 +67,37 @@ struct Cfg {
   static constexpr int TPI = 32 / LPT;           // token rows per warp-wide 16-byte load
   static constexpr int NI = kPage / TPI;         // 16-byte vectors per lane per (page, head) chunk
   static constexpr int CHUNK = kPage * D * ESZ;  // bytes of one (page, head) chunk
-  static constexpr int NV = ((NI * G + LPT - 1) / LPT) * LPT;  // reduce-scatter values (padded)
-  static constexpr int VPL = NV / LPT;           // finished logits owned by each lane
   static constexpr int LOG_LPT = LPT == 8 ? 3 : (LPT == 16 ? 4 : 5);
-  static constexpr int REC = G * D + 2 * G;      // floats of one warp's state record (o, m, l)
-  // Select-free reduce-scatter: when the NI*G partial values are a power of two (G a power of two) and at least LPT,
-  // a lane keeps logical value v in register v ^ PERM(lane), so every butterfly level sends the upper half of the
-  // registers and keeps the lower half. The lane loads token row j ^ PJ(lane) and query head g ^ PG(lane) for it.
-  static constexpr bool XPERM = (G & (G - 1)) == 0 && NI * G >= LPT;
+  static constexpr bool POW2G = (G & (G - 1)) == 0;
   static constexpr int LOG_G = G == 1 ? 0 : (G == 2 ? 1 : (G == 4 ? 2 : 3));
+  // The logits of a page are formed RC vector rows at a time (RC * G partial values per lane, reduce-scattered over
+  // the LPT lanes of a token row), so that few partial sums are live at once.
+  static constexpr int RC = (POW2G && NI * G > LPT) ? LPT / G : NI;
+  static constexpr int NCH = NI / RC;                          // chunks per page
+  static constexpr int NVC = ((RC * G + LPT - 1) / LPT) * LPT;  // reduce-scatter values per chunk (padded)
+  static constexpr int VPC = NVC / LPT;                        // finished logits a lane owns per chunk
+  static constexpr int VPL = NCH * VPC;                        // ... per page
+  static constexpr int REC = G * D + 2 * G;      // floats of one warp's state record (o, m, l)
+  static constexpr int NSEG = NCW < 4 ? NCW : 4;  // row segments per window (each gets at least one warp)
+  // per segment: the group's query, rotated, rounded to T and scaled (fp32 [G][D]), then the step token's K
+  // (rotated) and V as T
+  static constexpr int QPB = G * D * 4 + 2 * D * ESZ;
+  // Select-free reduce-scatter: when the RC*G values of a chunk are a power of two (G a power of two) and at least
+  // LPT, a lane keeps logical value v in register v ^ PERM(lane), so every butterfly level sends the upper half of
+  // the registers and keeps the lower half. The lane loads vector row j ^ PJ(lane) and query head g ^ PG(lane).
+  static constexpr bool XPERM = POW2G && RC * G >= LPT;
   // shared memory carve-up (bytes)
-  static constexpr int COMB = kNCW * REC * 4;             // per-warp state records
-  static constexpr int WLOG = kNCW * G * kPage * 8;       // per-warp logits, or probability pairs, of one page
-  static constexpr int SWT = kMaxSeg * G * (kNCW + 2) * 4;  // per segment: warp weights, max and sum per head
-  static constexpr int SEGB = kMaxSeg * 48;               // segment table
+  static constexpr int COMB = NCW * REC * 4;              // per-warp state records
+  static constexpr int WLOG = NCW * G * kPage * 8;        // per-warp logits, or probability pairs, of one page
+  static constexpr int SWT = NSEG * G * (NCW + 2) * 4;    // per segment: warp weights, max and sum per head
+  static constexpr int SEGB = NSEG * 48;                  // segment table
+  static constexpr int QPREP = NSEG * QPB;                // per-segment query and step token
   static constexpr int ROWB = (kMaxRowsScan + 1) * 4;     // per-row entry offsets (row scan)
-  static constexpr int FIXED = COMB + WLOG + SWT + SEGB + ROWB + 1024;
+  static constexpr int FIXED = COMB + WLOG + SWT + SEGB + QPREP + ROWB + 256;
   static constexpr int SLOT = 2 * CHUNK;                  // K and V of one entry
-  static constexpr int SLOTS_FIT = (226 * 1024 - FIXED) / (SLOT + 32);  // 1 KiB left for static shared memory
+  // per CTA: 227 KB alone on an SM, else its share of the SM's 228 KB less the 1 KB each CTA reserves
+  static constexpr int BUDGET = MINB == 1 ? 226 * 1024 : (228 / MINB - 2) * 1024;
+  static constexpr int SLOTS_FIT = (BUDGET - FIXED) / (SLOT + 32);
   static constexpr int SLOTS = SLOTS_FIT > 32 ? 32 : SLOTS_FIT;
   // entries the producer handles per step: small enough that a step waiting on one slot's consumer holds back few
   // copies (8 measured best against 2, 4 and 16)
@@ -79,13 +107,18 @@ struct Cfg {
   static constexpr int OFF_WLOG = OFF_COMB + COMB;
   static constexpr int OFF_SWT = OFF_WLOG + WLOG;
   static constexpr int OFF_SEG = ((OFF_SWT + SWT + 15) / 16) * 16;
-  static constexpr int OFF_SMETA = OFF_SEG + SEGB;        // [SLOTS] int4 (tlo | thi << 16, step token, page, entry)
+  static constexpr int OFF_QP = OFF_SEG + SEGB;          // [NSEG][QPB]
+  static constexpr int OFF_SMETA = OFF_QP + QPREP;        // [SLOTS] int4 (tlo | thi << 16, step token, page, entry)
   static constexpr int OFF_BAR = OFF_SMETA + SLOTS * 16;  // full[SLOTS], empty[SLOTS]
   static constexpr int OFF_ROWS = OFF_BAR + 2 * SLOTS * 8;
   static constexpr int SMEM = OFF_ROWS + ROWB;
   static_assert(SLOTS >= 4, "too few page slots");
-  static_assert(SMEM + 1024 <= 227 * 1024, "shared memory per CTA");
+  static_assert(SMEM + 256 <= BUDGET, "shared memory per CTA");
   static_assert(EPL % 2 == 0 && (D / 2) % EPL == 0, "vector layout");
+  static_assert(NI % RC == 0, "chunk rows");
+  static_assert(kBarSeg0 + NSEG <= 16, "named barriers");
+  static_assert(QPB % 16 == 0, "query area alignment");
+  static_assert(NCW < SLOTS, "a warp's next entry lies in a later slot");
 };
 
 struct Params {
@@ -155,19 +188,6 @@ __device__ __forceinline__ bool wait_entry(const int *stamp, uint64_t *full, int
   return false;
 }
 
-// Inverse frequencies of the EPL consecutive rotary pairs starting at pair index i0 (a multiple of EPL).
-template <int EPL>
-__device__ __forceinline__ void load_inv_freq(const float *inv_freq, int i0, float *fr) {
-#pragma unroll
-  for (int k = 0; k < EPL; k += 4) {
-    const float4 f = *reinterpret_cast<const float4 *>(inv_freq + i0 + k);
-    fr[k] = f.x;
-    fr[k + 1] = f.y;
-    fr[k + 2] = f.z;
-    fr[k + 3] = f.w;
-  }
-}
-
 // Four consecutive output elements, rounded to the output type, in one store (8 bytes bf16, 16 bytes fp32).
 template <class T>
 __device__ __forceinline__ void store4(T *dst, float a, float b, float c, float d);
@@ -182,37 +202,16 @@ __device__ __forceinline__ void store4<float>(float *dst, float a, float b, floa
   *reinterpret_cast<float4 *>(dst) = make_float4(a, b, c, d);
 }
 
-// Rotary factors (cos, sin) at position pos of the EPL pairs whose elements this lane holds (dims base_dim ..).
-template <int EPL, int D>
-__device__ __forceinline__ void rope_lane_factors(int base_dim, int pos, const float *inv_freq, float *cs, float *sn) {
-  float fr[EPL];
-  load_inv_freq<EPL>(inv_freq, base_dim < D / 2 ? base_dim : base_dim - D / 2, fr);
-#pragma unroll
-  for (int k = 0; k < EPL; ++k) rope_factors(pos, fr[k], cs[k], sn[k]);
-}
-
-// RoPE of the EPL values a lane holds: the other element of each pair is held by the lane LPT/2 away. Results are
-// rounded to the pool dtype, as a stored key or query would be.
-template <class T, int EPL, int LPT, int D>
-__device__ __forceinline__ void rope_lane_apply(float *x, int base_dim, const float *cs, const float *sn) {
-  const bool first = base_dim < D / 2;
-#pragma unroll
-  for (int k = 0; k < EPL; ++k) {
-    const float y = __shfl_xor_sync(0xffffffffu, x[k], LPT / 2);
-    float a, b;
-    rope_rotate(first ? x[k] : y, first ? y : x[k], cs[k], sn[k], a, b);
-    x[k] = to_f(from_f<T>(first ? a : b));
-  }
-}
-
 template <class T, int D, int G>
-__global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
+__global__ void __launch_bounds__((Shape<T, D, G>::THREADS)) __maxnreg__((Shape<T, D, G>::MAXREG)) propose_kernel(
+    const Params p) {
   using C = Cfg<T, D, G>;
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char *kv = smem + C::OFF_KV;
-  float *comb = reinterpret_cast<float *>(smem + C::OFF_COMB);      // [kNCW][REC]
-  float *wlog_all = reinterpret_cast<float *>(smem + C::OFF_WLOG);  // [kNCW][16][G] float2 (or [G][16] float)
-  float *swt_all = reinterpret_cast<float *>(smem + C::OFF_SWT);    // [kMaxSeg][G * kNCW + 2G]
+  float *comb = reinterpret_cast<float *>(smem + C::OFF_COMB);      // [C::NCW][REC]
+  float *wlog_all = reinterpret_cast<float *>(smem + C::OFF_WLOG);  // [C::NCW][16][G] float2 (or [G][16] float)
+  float *swt_all = reinterpret_cast<float *>(smem + C::OFF_SWT);    // [NSEG][G * NCW + 2G]
+  unsigned char *qprep_all = smem + C::OFF_QP;                       // [NSEG][QPB]
   Seg *segs = reinterpret_cast<Seg *>(smem + C::OFF_SEG);
   int4 *smeta = reinterpret_cast<int4 *>(smem + C::OFF_SMETA);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
@@ -220,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
   int *rowoff = reinterpret_cast<int *>(smem + C::OFF_ROWS);  // [nrows + 1] when nrows <= kMaxRowsScan
   __shared__ int64_t s_total, s_rb0, s_wnext_rb;
   __shared__ int s_row0, s_nseg, s_wnext_row;
-  __shared__ int s_last[kMaxSeg];
+  __shared__ int s_last[C::NSEG];
   __shared__ int scan_scratch[32];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -239,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
   if (!p.settled) grid_dependency_sync();
   const bool small_rows = p.nrows <= kMaxRowsScan;
   if (small_rows) {
-    const int per = (p.nrows + kThreads - 1) / kThreads;  // thread t owns rows [t*per, (t+1)*per)
+    const int per = (p.nrows + C::THREADS - 1) / C::THREADS;  // thread t owns rows [t*per, (t+1)*per)
     const int lo = min(p.nrows, tid * per), hi = min(p.nrows, lo + per);
     int cnt = 0;
     for (int rr = lo; rr < hi; ++rr) {
@@ -254,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
       rowoff[rr] = run;
       run += c;
     }
-    if (tid == kThreads - 1) {
+    if (tid == C::THREADS - 1) {
       rowoff[p.nrows] = incl;
       s_total = incl;
     }
@@ -327,9 +326,9 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
   bool waited = !p.settled;
 
   for (int64_t cur = cta_begin; cur < cta_end;) {
-    if (warp == kNCW) {
+    if (warp == C::NCW) {
       // ---- segment table of this window: rows w_row .. w_row+31 intersected with [cur, cta_end), at most
-      // kMaxSeg non-empty segments; each gets one warp plus a share of the spare warps by its entry count.
+      // NSEG non-empty segments; each gets one warp plus a share of the spare warps by its entry count.
       const int row = w_row + lane;
       const int c = row < p.nrows ? (small_rows ? rowoff[row + 1] - rowoff[row] : row_entries(p, row)) : 0;
       int incl = c;
@@ -343,8 +342,8 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
       const bool nonempty = c > 0 && sb < se;
       const unsigned mask = __ballot_sync(0xffffffffu, nonempty);
       const int idx = __popc(mask & ((1u << lane) - 1u));
-      const int nseg = min(__popc(mask), kMaxSeg);
-      const bool keep = nonempty && idx < kMaxSeg;
+      const int nseg = min(__popc(mask), C::NSEG);
+      const bool keep = nonempty && idx < C::NSEG;
       const int cnt = keep ? static_cast<int>(se - sb) : 0;
       int cinc = cnt;
 #pragma unroll
@@ -355,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
       const int n = __shfl_sync(0xffffffffu, cinc, 31);
       if (keep) {
         const int64_t cum = cinc - cnt;
-        const int64_t spare = kNCW - nseg;
+        const int64_t spare = C::NCW - nseg;
         Seg sg;
         sg.b = sb;
         sg.e = se;
@@ -367,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
         sg.nw = idx + 1 + static_cast<int>(spare * (cum + cnt) / n) - sg.w0;
         segs[idx] = sg;
       }
-      const unsigned dmask = __ballot_sync(0xffffffffu, nonempty && idx == kMaxSeg);  // first row left over
+      const unsigned dmask = __ballot_sync(0xffffffffu, nonempty && idx == C::NSEG);  // first row left over
       const int tot = __shfl_sync(0xffffffffu, incl, 31);
       if (dmask) {
         const int dl = __ffs(dmask) - 1;
@@ -386,9 +385,33 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
     const int nseg = s_nseg;
     const int64_t win_end = (nseg > 0) ? segs[nseg - 1].e : cur;  // a window of empty rows only moves the rows on
 
-    if (warp == kNCW) {
+    if (warp == C::NCW) {
       // ============================================================================================== producer
       const uint64_t pol = l2_evict_first_policy();  // the selected pages are streamed once per launch
+      // The window's entries past the ring's first fill are prefetched into L2 at once (up to kPrefetchAhead), so
+      // that the ring refills from L2 when the consumers free their slots; before the dependency wait, only pages
+      // whose visible tokens are all prompt tokens.
+      if (nseg > 0) {
+        const int64_t pf_lo = segs[0].b + C::SLOTS, pf_hi = min(win_end, pf_lo + kPrefetchAhead);
+        for (int si = 0; si < nseg && pf_lo < pf_hi; ++si) {
+          const Seg sg = segs[si];
+          const int64_t lo = sg.b > pf_lo ? sg.b : pf_lo, hi = sg.e < pf_hi ? sg.e : pf_hi;
+          if (lo >= hi) continue;
+          const int r = sg.row / p.hkv, h = sg.row - r * p.hkv;
+          const int L = p.ctx_len[r], S = p.seq_len[r], nsel = p.vnsel[sg.vr];
+          for (int64_t e = lo + lane; e < hi; e += 32) {
+            const int i = static_cast<int>(e - sg.rb);
+            const size_t o = static_cast<size_t>(sg.vr) * p.vcap + i;
+            const int page = p.vbt[o], base = p.vlp[o] * kPage;
+            const int thi = min(kPage, S - base), tlo = (i < nsel) ? 0 : max(0, L - base);
+            if (thi > tlo && page >= 0 && page < p.num_pages && (waited || base + thi <= L)) {
+              const size_t off = (static_cast<size_t>(page) * p.hkv + h) * kPage * D;
+              bulk_prefetch_l2(Kp + off, C::CHUNK);
+              bulk_prefetch_l2(Vp + off, C::CHUNK);
+            }
+          }
+        }
+      }
       for (int si = 0; si < nseg; ++si) {
         const Seg sg = segs[si];
         const int r = sg.row / p.hkv, h = sg.row - r * p.hkv;
@@ -448,77 +471,106 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
       const Seg sg = segs[si];
       const int gw = warp - sg.w0, nw = sg.nw;
       const int r = sg.row / p.hkv, h = sg.row - r * p.hkv;
+      const int bar_id = kBarSeg0 + si, bar_n = nw * 32;
       float *wlog = wlog_all + warp * G * kPage * 2;  // logits [g][token] for a rescale, then (p, p) [token][g]
       float2 *wpair = reinterpret_cast<float2 *>(wlog);
-      float2 qf[G][C::EP2], o[G][C::EP2];
-      float m_run[G], l_own[C::VPL];
-      const int P = fused ? p.seq_len[r] - 1 : 0;  // position of the step token (fused append)
-      uint4 kw_step = make_uint4(0u, 0u, 0u, 0u), vw_step = kw_step;  // this row's step token, K rotated at P
-      {
-        // The rotary factors depend only on the page map and the frequencies, which a settled view covers, so they
-        // are formed before the dependency wait; q is read after it.
-        float cs[C::EPL], sn[C::EPL];  // the same angles for every head of the group
-        if (fused) rope_lane_factors<C::EPL, D>(base_dim, P, p.inv_freq, cs, sn);
-        if (!waited) {
-          grid_dependency_sync();  // before q, the step token, outputs and the workspace
-          waited = true;
-        }
-        const T *qrow = static_cast<const T *>(p.q) + (static_cast<size_t>(r) * p.hq + h * G) * D + base_dim;
-        uint4 qraw[G];
-        const int pg = C::XPERM ? (((lane % C::LPT) * C::VPL) & (G - 1)) : 0;  // register g holds head g ^ pg
+      unsigned char *qp = qprep_all + si * C::QPB;
+      float *qprep = reinterpret_cast<float *>(qp);          // [G][D] query of the group, ready for the dot products
+      T *stepkv = reinterpret_cast<T *>(qp + G * D * 4);     // [D] step key (rotated), then [D] step value
+      if (!waited) {
+        grid_dependency_sync();  // before q, the step token, outputs and the workspace
+        waited = true;
+      }
+      if (gw == 0) {
+        // The group's first warp prepares what every warp of the group needs once: the G query heads, rotated at
+        // the step position P (fused form), rounded to T as a stored query would be and scaled by log2(e)/sqrt(D);
+        // in the fused form also the step token's key (rotated by the same angles) and value. Lane l takes the
+        // rotary pairs (i, i + D/2) with i = l, l + 32, ..., so it forms D/64 angles.
+        const T *qrow = static_cast<const T *>(p.q) + (static_cast<size_t>(r) * p.hq + h * G) * D;
+        const int P = fused ? p.seq_len[r] - 1 : 0;
+        const size_t src = (static_cast<size_t>(r) * p.hkv + h) * D;
+        for (int i = lane; i < D / 2; i += 32) {
+          float cs = 1.0f, sn = 0.0f;
+          if (fused) rope_factors(P, p.inv_freq[i], cs, sn);
 #pragma unroll
-        for (int g = 0; g < G; ++g)
-          qraw[g] = *reinterpret_cast<const uint4 *>(qrow + static_cast<size_t>(g ^ pg) * D);
-        if (fused) {
-          // The step token's key and value travel with q, and its key turns by the same angles as q: the warp that
-          // meets the token's page only stores them.
-          const size_t src = (static_cast<size_t>(r) * p.hkv + h) * D + base_dim;
-          const uint4 kraw = *reinterpret_cast<const uint4 *>(static_cast<const T *>(p.k_new) + src);
-          vw_step = *reinterpret_cast<const uint4 *>(static_cast<const T *>(p.v_new) + src);
-          float kx[C::EPL];
-          Vec16<T>::unpack(kraw, kx);
-          rope_lane_apply<T, C::EPL, C::LPT, D>(kx, base_dim, cs, sn);
-          kw_step = Vec16<T>::pack(kx);
+          for (int g = 0; g < G; ++g) {
+            float x = to_f(qrow[g * D + i]), y = to_f(qrow[g * D + i + D / 2]);
+            if (fused) {
+              float xr, yr;
+              rope_rotate(x, y, cs, sn, xr, yr);
+              x = to_f(from_f<T>(xr));
+              y = to_f(from_f<T>(yr));
+            }
+            qprep[g * D + i] = x * qscale;
+            qprep[g * D + i + D / 2] = y * qscale;
+          }
+          if (fused) {
+            const T *kn = static_cast<const T *>(p.k_new) + src, *vn = static_cast<const T *>(p.v_new) + src;
+            float xr, yr;
+            rope_rotate(to_f(kn[i]), to_f(kn[i + D / 2]), cs, sn, xr, yr);
+            stepkv[i] = from_f<T>(xr);
+            stepkv[i + D / 2] = from_f<T>(yr);
+            stepkv[D + i] = vn[i];
+            stepkv[D + i + D / 2] = vn[i + D / 2];
+          }
         }
+      }
+      group_sync(bar_id, bar_n);
+      float2 qf[G][C::EP2], o[G][C::EP2];
+      float m_run[G], m_own[C::VPL], l_own[C::VPL];
+      {
+        const int pg = C::XPERM ? (((lane % C::LPT) * C::VPC) & (G - 1)) : 0;  // register g holds head g ^ pg
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          float tmp[C::EPL];
-          Vec16<T>::unpack(qraw[g], tmp);
-          if (fused) rope_lane_apply<T, C::EPL, C::LPT, D>(tmp, base_dim, cs, sn);
+          const float4 *src = reinterpret_cast<const float4 *>(qprep + (g ^ pg) * D + base_dim);
 #pragma unroll
-          for (int k = 0; k < C::EP2; ++k) {
-            qf[g][k] = make_float2(tmp[2 * k] * qscale, tmp[2 * k + 1] * qscale);
+          for (int k = 0; k < C::EP2; k += 2) {
+            const float4 f = src[k / 2];
+            qf[g][k] = make_float2(f.x, f.y);
+            qf[g][k + 1] = make_float2(f.z, f.w);
             o[g][k] = make_float2(0.0f, 0.0f);
+            o[g][k + 1] = make_float2(0.0f, 0.0f);
           }
           m_run[g] = -INFINITY;
         }
 #pragma unroll
-        for (int k = 0; k < C::VPL; ++k) l_own[k] = 0.0f;
+        for (int k = 0; k < C::VPL; ++k) {
+          l_own[k] = 0.0f;
+          m_own[k] = -INFINITY;
+        }
       }
-      // owned (token, head) pairs after the reduce-scatter: value v = j*G + g is token j*TPI + ts of head g
-      int g_own[C::VPL], tok_own[C::VPL];
+      // owned (token, head) pairs after the reduce-scatter: chunk c's value v = j*G + g is vector row c*RC + j,
+      // i.e. token (c*RC + j)*TPI + ts, of head g; the lane keeps values [(lane%LPT)*VPC, +VPC) of every chunk
+      int g_own[C::VPL], tok_own[C::VPL], wp_off[C::VPL];
       bool ok_own[C::VPL];
 #pragma unroll
-      for (int k = 0; k < C::VPL; ++k) {
-        const int v = (lane % C::LPT) * C::VPL + k;
-        const int j = v / G;
-        g_own[k] = v - j * G;
-        tok_own[k] = j * C::TPI + ts;
-        ok_own[k] = v < C::NI * G;
-      }
-      // this warp's entries: kk = kk0, kk0 + nw, ... (CTA-local indices, fewer than 2^31), slot kk % SLOTS
+      for (int c = 0; c < C::NCH; ++c)
+#pragma unroll
+        for (int k = 0; k < C::VPC; ++k) {
+          const int v = (lane % C::LPT) * C::VPC + k;
+          const int j = v / G;
+          g_own[c * C::VPC + k] = v - j * G;
+          tok_own[c * C::VPC + k] = (c * C::RC + j) * C::TPI + ts;
+          ok_own[c * C::VPC + k] = v < C::RC * G;
+          wp_off[c * C::VPC + k] = tok_own[c * C::VPC + k] * G + g_own[c * C::VPC + k];
+        }
+      // this warp's entries: kk = kk0, kk0 + nw, ... (CTA-local indices, fewer than 2^31) in slot kk % SLOTS,
+      // phase parity (kk / SLOTS) & 1, both advanced as kk moves on (nw < SLOTS)
       const int kk0 = static_cast<int>(sg.b - cta_begin) + gw, kk_end = static_cast<int>(sg.e - cta_begin);
+      int slot = kk0 % C::SLOTS;
+      uint32_t ph = static_cast<uint32_t>(kk0 / C::SLOTS) & 1u;
       for (int kk = kk0; kk < kk_end; kk += nw) {
-        const int slot = kk % C::SLOTS;
-        wait_entry(&smeta[slot].w, &full[slot], kk, static_cast<uint32_t>(kk / C::SLOTS) & 1u, p.err);
+        wait_entry(&smeta[slot].w, &full[slot], kk, ph, p.err);
         const int4 mt = smeta[slot];
         const int tlo = mt.x & 0xffff, thi = mt.x >> 16;
         unsigned char *kb = kv + slot * C::SLOT;
         if (mt.y >= 0) {
-          // the step token of this row lies in this page: RoPE'd key and value into the pool and into this copy
+          // the step token of this row lies in this page: its rotated key and its value into the pool and into
+          // this copy of the page
           const int tok = mt.y;
           if (lane < C::LPT) {
-            const uint4 kw = kw_step, vw = vw_step;
+            const uint4 kw = *reinterpret_cast<const uint4 *>(stepkv + base_dim);
+            const uint4 vw = *reinterpret_cast<const uint4 *>(stepkv + D + base_dim);
             const int rowb = (tok * D + base_dim) * C::ESZ;
             *reinterpret_cast<uint4 *>(kb + rowb) = kw;
             *reinterpret_cast<uint4 *>(kb + C::CHUNK + rowb) = vw;
@@ -529,58 +581,56 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
           }
           __syncwarp();
         }
-        // ---- logits of the page's 16 tokens for the G heads
-        float part[C::NV];
-#pragma unroll
-        for (int v = 0; v < C::NV; ++v) part[v] = 0.0f;
-        if (thi > tlo) {
+        // ---- logits of the page's 16 tokens for the G heads, RC vector rows at a time. Slots of invisible tokens
+        // (or of an entry with nothing to read) may hold anything: their logits are masked below.
+        float s_own[C::VPL];
+        {
           const uint4 *kvec = reinterpret_cast<const uint4 *>(kb);
-          uint4 w4[C::NI];
-          const int pj = C::XPERM ? (((lane % C::LPT) * C::VPL) >> C::LOG_G) : 0;  // register j: row j ^ pj
+          const int pj = C::XPERM ? (((lane % C::LPT) * C::VPC) >> C::LOG_G) : 0;  // register j: row j ^ pj
 #pragma unroll
-          for (int j = 0; j < C::NI; ++j) w4[j] = kvec[(j ^ pj) * 32 + lane];
+          for (int c = 0; c < C::NCH; ++c) {
+            float part[C::NVC];
 #pragma unroll
-          for (int j = 0; j < C::NI; ++j) {
-            float2 kf[C::EP2];
-            Vec16<T>::unpack2(w4[j], kf);
+            for (int j = 0; j < C::RC; ++j) {
+              float2 kf[C::EP2];
+              Vec16<T>::unpack2(kvec[(c * C::RC + (j ^ pj)) * 32 + lane], kf);
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-              float2 acc = __fmul2_rn(qf[g][0], kf[0]);
+              for (int g = 0; g < G; ++g) {
+                float2 acc = __fmul2_rn(qf[g][0], kf[0]);
 #pragma unroll
-              for (int k = 1; k < C::EP2; ++k) acc = __ffma2_rn(qf[g][k], kf[k], acc);
-              part[j * G + g] = acc.x + acc.y;
+                for (int k = 1; k < C::EP2; ++k) acc = __ffma2_rn(qf[g][k], kf[k], acc);
+                part[j * G + g] = acc.x + acc.y;
+              }
             }
+#pragma unroll
+            for (int v = C::RC * G; v < C::NVC; ++v) part[v] = 0.0f;  // padding of the reduce-scatter
+            // reduce-scatter over the LPT lanes of a token row: the lane keeps values [(lane%LPT)*VPC, +VPC)
+#pragma unroll
+            for (int step = 0; step < C::LOG_LPT; ++step) {
+              const int msk = (C::LPT >> 1) >> step;
+              const int half = C::NVC >> (step + 1);
+              const bool upper = (lane & msk) != 0;
+#pragma unroll
+              for (int k = 0; k < half; ++k) {
+                if (C::XPERM) {
+                  part[k] += __shfl_xor_sync(0xffffffffu, part[k + half], msk);
+                } else {
+                  const float send = upper ? part[k] : part[k + half];
+                  const float keep = upper ? part[k + half] : part[k];
+                  part[k] = keep + __shfl_xor_sync(0xffffffffu, send, msk);
+                }
+              }
+            }
+#pragma unroll
+            for (int k = 0; k < C::VPC; ++k) s_own[c * C::VPC + k] = part[k];
           }
         }
-        // reduce-scatter over the LPT lanes of a token row: lane keeps values [(lane%LPT)*VPL, +VPL)
-#pragma unroll
-        for (int step = 0; step < C::LOG_LPT; ++step) {
-          const int msk = (C::LPT >> 1) >> step;
-          const int half = C::NV >> (step + 1);
-          const bool upper = (lane & msk) != 0;
-#pragma unroll
-          for (int k = 0; k < half; ++k) {
-            if (C::XPERM) {
-              part[k] += __shfl_xor_sync(0xffffffffu, part[k + half], msk);
-            } else {
-              const float send = upper ? part[k] : part[k + half];
-              const float keep = upper ? part[k + half] : part[k];
-              part[k] = keep + __shfl_xor_sync(0xffffffffu, send, msk);
-            }
-          }
-        }
-        float s_own[C::VPL], mr_own[C::VPL];
         bool over = false;
 #pragma unroll
         for (int k = 0; k < C::VPL; ++k) {
           const bool vis = ok_own[k] && tok_own[k] >= tlo && tok_own[k] < thi;
-          s_own[k] = vis ? part[k] : -INFINITY;
-          float mr = -INFINITY;
-#pragma unroll
-          for (int g = 0; g < G; ++g)
-            if (g == g_own[k]) mr = m_run[g];
-          mr_own[k] = mr;
-          over |= vis && (s_own[k] > mr + kRescaleThreshold);
+          if (!vis) s_own[k] = -INFINITY;
+          over |= s_own[k] > m_own[k] + kRescaleThreshold;
         }
         if (__any_sync(0xffffffffu, over)) {
           // raise the running max of every head to this page's max, rescaling the state accumulated so far
@@ -601,7 +651,7 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
             for (int k = 0; k < C::VPL; ++k)
               if (g_own[k] == g) {
                 l_own[k] *= a;
-                mr_own[k] = mn;
+                m_own[k] = mn;
               }
           }
           __syncwarp();
@@ -610,9 +660,9 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
 #pragma unroll
         for (int k = 0; k < C::VPL; ++k) {
           if (ok_own[k]) {
-            const float pv = (s_own[k] == -INFINITY) ? 0.0f : exp2f(s_own[k] - mr_own[k]);
+            const float pv = (s_own[k] == -INFINITY) ? 0.0f : exp2f(s_own[k] - m_own[k]);
             l_own[k] += pv;
-            wpair[tok_own[k] * G + g_own[k]] = make_float2(pv, pv);
+            wpair[wp_off[k]] = make_float2(pv, pv);
           }
         }
         __syncwarp();
@@ -650,6 +700,11 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
+        slot += nw;
+        if (slot >= C::SLOTS) {
+          slot -= C::SLOTS;
+          ph ^= 1u;
+        }
       }
 
       // ---- end of this warp's share of the segment: its state into comb[warp]
@@ -681,14 +736,13 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
           cw[G * D + G + g] = lsum;
         }
       }
-      const int bar_id = kBarSeg0 + si, bar_n = nw * 32;
       group_sync(bar_id, bar_n);
 
       // ---- the group combines its warps' states. The group's first warp derives, per head, the max M over the
       // warps, each warp's weight 2^(m_w - M) and the weighted sum L (lane j = warp j of the group); then every
       // thread forms its elements' weighted sums with all the group's loads in flight.
       const int gt = gw * 32 + lane, GT = nw * 32;
-      float *wts = swt_all + si * (G * kNCW + 2 * G);  // [G][kNCW] weights, then M[G], L[G]
+      float *wts = swt_all + si * (G * C::NCW + 2 * G);  // [G][NCW] weights, then M[G], L[G]
       if (gw == 0) {
 #pragma unroll
         for (int g = 0; g < G; ++g) {
@@ -698,20 +752,20 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
           const float M = warp_max(mw);
           const float wgt = (mw == -INFINITY) ? 0.0f : exp2f(mw - M);
           const float Ls = warp_sum(lw * wgt);
-          if (lane < kNCW) wts[g * kNCW + lane] = wgt;
+          if (lane < C::NCW) wts[g * C::NCW + lane] = wgt;
           if (lane == 0) {
-            wts[G * kNCW + g] = M;
-            wts[G * kNCW + G + g] = Ls;
+            wts[G * C::NCW + g] = M;
+            wts[G * C::NCW + G + g] = Ls;
           }
         }
       }
       group_sync(bar_id, bar_n);
       auto combined = [&](int i, int g) {
         const float *ci = comb + sg.w0 * C::REC + i;
-        const float *wg = wts + g * kNCW;
+        const float *wg = wts + g * C::NCW;
         float acc = 0.0f;
 #pragma unroll
-        for (int j = 0; j < kNCW; ++j)
+        for (int j = 0; j < C::NCW; ++j)
           if (j < nw) acc = fmaf(ci[j * C::REC], wg[j], acc);
         return acc;
       };
@@ -724,7 +778,7 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
       if (b_first == b_last) {
         for (int i = gt; i < G * D; i += GT) {
           const int g = i / D;
-          const float M = wts[G * kNCW + g], Ls = wts[G * kNCW + G + g];
+          const float M = wts[G * C::NCW + g], Ls = wts[G * C::NCW + G + g];
           const float acc = combined(i, g);
           outp[out_base + i] = from_f<T>(Ls > 0.0f ? acc / Ls : 0.0f);
           if (i - g * D == 0) {
@@ -736,7 +790,7 @@ __global__ void __launch_bounds__(kThreads, 1) propose_kernel(const Params p) {
         const size_t pslot = static_cast<size_t>(blockIdx.x) + sg.row;
         for (int i = gt; i < G * D; i += GT) {
           const int g = i / D;
-          const float M = wts[G * kNCW + g], Ls = wts[G * kNCW + G + g];
+          const float M = wts[G * C::NCW + g], Ls = wts[G * C::NCW + G + g];
           __stcg(p.part + pslot * G * D + i, combined(i, g));
           if (i - g * D == 0) {
             __stcg(reinterpret_cast<float2 *>(p.ml) + pslot * G + g, make_float2(M, Ls));
@@ -820,16 +874,19 @@ cudaError_t launch_tdg(const Params &prm, cudaStream_t s) {
   if (!attr[dev & 63]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
+    // The whole unified L1 as shared memory (MINB CTAs of this shape fit on one SM only with it).
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
     attr[dev & 63] = true;
   }
   // One CTA per SM, but no more CTAs than the view can feed with a page per consumer warp (its capacity bounds
   // the entries): a small launch then leaves SMs free for work on other streams, at the same latency, since a
   // CTA's warps take its pages in parallel.
   int nb = device_sm_count();
-  const int64_t feed = (static_cast<int64_t>(prm.nrows) * prm.vcap + kNCW - 1) / kNCW;
+  const int64_t feed = (static_cast<int64_t>(prm.nrows) * prm.vcap + C::NCW - 1) / C::NCW;
   if (feed < nb) nb = static_cast<int>(feed < 1 ? 1 : feed);
   if (nb > kMaxSlotsExtraCtas) nb = kMaxSlotsExtraCtas;
-  launch_pdl(kern, dim3(nb), dim3(kThreads), C::SMEM, s, prm);
+  launch_pdl(kern, dim3(nb), dim3(C::THREADS), C::SMEM, s, prm);
   return cudaGetLastError();
 }
 

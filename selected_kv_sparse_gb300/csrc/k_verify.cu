@@ -446,7 +446,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (done1 && t2 == t1) break;
         if (progressed) {
           idle = 0;
-        } else if (++idle > 16u * kWaitPolls) {
+        } else if (++idle > kSpinPolls) {
           set_error(p.err, kErrTimeout);
           okrun = false;
           break;

@@ -157,14 +157,18 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// A waiting thread is suspended in hardware until the phase completes (it is woken at once) or kSuspendNs pass,
+// so a wait costs a few instructions per kSuspendNs instead of a busy loop that takes issue slots from the warps
+// doing the work.
+constexpr uint32_t kSuspendNs = 1u << 20;  // about 1 ms
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
       : "memory");
   return ok != 0;
 }
@@ -182,9 +186,11 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete. Gives up after a bounded number of polls (each
-// try_wait itself suspends for a hardware-defined time), records kErrTimeout and returns false.
-constexpr uint32_t kWaitPolls = 1u << 22;
+// Waits for the phase with the given parity to complete. Gives up after a bounded number of polls (each suspends
+// for at most kSuspendNs, about a second in all), records kErrTimeout and returns false.
+constexpr uint32_t kWaitPolls = 1u << 10;
+// Bound on the polls of a loop that tests barriers without suspending (the verification MMA issuer).
+constexpr uint32_t kSpinPolls = 1u << 26;
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err) {
   for (uint32_t i = 0; i < kWaitPolls; ++i)
     if (mbar_try_wait(bar, parity)) return true;
@@ -234,6 +240,12 @@ __device__ __forceinline__ void tma_load_2d_stream(void *dst_smem, const void *t
       " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst_smem)),
       "l"(tmap), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(pol)
       : "memory");
+}
+
+// Prefetch of `bytes` (a multiple of 16, 16-byte aligned source) from global memory into L2, with no destination
+// in shared memory and no completion to wait for.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src_gmem, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src_gmem), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
