@@ -141,7 +141,9 @@ kap_status kap_refresh_summaries(const kap_kv_pool *pool, const int32_t *pages_d
  *               Shared selection (per_kv_head = 0): score = sum over h ascending of the per-head scores.
  *   sel_ids   [R][rows][cap] out: selected prompt pages ascending; rows = Hkv or 1.
  *   n_sel     [R][rows] out: count = min(N, a + r + k) with N = ceil(ctx_len/16).
- *   workspace >= kap_score_workspace_size(...) bytes of device memory (scores).
+ *   workspace >= kap_score_workspace_size(...) bytes of device memory. On completion it holds the page scores,
+ *             fp32 [R][rows][max_pages] from its first byte: entry (r, v, j) for j < N is the score above, entries
+ *             at or past N are unspecified.
  * Errors: KAP_EINVAL for a null or misaligned pointer or a negative a, r or k; KAP_ECAPACITY for a workspace or a
  * cap too small; KAP_EUNSUPPORTED when R * rows > 65535 or the top-K row (4 bytes per page) exceeds 200 KiB. */
 kap_status kap_score_topk(const kap_kv_pool *pool, const kap_page_map *map, const void *q_dev,
@@ -250,6 +252,13 @@ kap_status kap_compile_view(const kap_page_map *map, const int32_t *sel_ids, con
 kap_status kap_slot_mapping(const kap_page_map *map, const int32_t *tok_offsets_dev, const int32_t *start_pos_dev,
                             int32_t num_tokens, int64_t *slot_out, int32_t *pos_out, kap_stream stream);
 
+/* RoPE inverse frequencies. KAP paper, selected-KV view: the proposal and the verifier keep the same logical
+ * positions, so every call that rotates (kap_append_kv, kap_append_propose) takes the one table this fills.
+ * Writes inv_freq_host[i] = theta^(-2i/d) for 0 <= i < d/2, formed in double precision and rounded once to fp32,
+ * into HOST memory of d/2 floats owned by the caller (who copies it to the device). No device work, no stream.
+ * Returns KAP_EINVAL for a NULL pointer, d <= 0, odd d, or theta not finite and > 0. */
+kap_status kap_rope_inv_freq(int32_t head_dim, double theta, float *inv_freq_host);
+
 /* KV append with RoPE. KAP paper, executor (proposal KV written through the slot mapping; the verifier advances
  * the full-context KV state). For token t (0 <= t < T) with p = pos[t*tok_stride], s = slots[t*tok_stride]:
  * when s >= 0, K[s] = RoPE(k_new[t], p), V[s] = v_new[t] (fp32 math, round-to-nearest into the pool dtype);
@@ -311,7 +320,10 @@ size_t kap_verify_workspace_size(int32_t num_seqs, int32_t num_kv_heads, int32_t
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine. Each call clears the scratch's
  *     counters with cudaMemsetAsync on `stream`, then launches the same kernel as kap_attn_propose.
  *   - The first call on a device looks up the scratch's device address (cudaGetSymbolAddress) with that device
- *     current; make that first call before any stream capture.
+ *     current; make that first call before any stream capture. The address is kept for the life of the process:
+ *     after a cudaDeviceReset of that device the library must not be called on it again in the same process.
+ *   - A failed CUDA call (the address lookup, the clearing of the counters, the launch) returns KAP_ECUDA with its
+ *     text in kap_last_cuda_error, as for every other call.
  *   - Every call on a device shares the one scratch array and it keeps the last call's contents: calls that overlap
  *     on the GPU (different streams, no ordering between them) race and give wrong results. */
 kap_status kap_attn_propose_noalloc(const kap_kv_pool *pool, const kap_page_map *map, const kap_view *view,

@@ -88,6 +88,7 @@ def _declare(lib):
         "kap_device_error": ([P], I),
         "kap_attn_propose_noalloc": ([P, P, P, P, P, P, P], I),
         "kap_noalloc_scratch_bytes": ([], Z),
+        "kap_rope_inv_freq": ([I, ctypes.c_double, P], I),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -478,7 +479,8 @@ def workspace(nbytes: int, device) -> torch.Tensor:
 
 
 def rope_inv_freq(d: int, theta: float = 1.0e4, device="cpu") -> torch.Tensor:
-    """RoPE inverse frequencies theta^(-2i/d), i < d/2: computed in fp64 on the host, rounded once to fp32."""
-    import numpy as np
-    f = np.power(np.float64(theta), -2.0 * np.arange(d // 2, dtype=np.float64) / d).astype(np.float32)
-    return torch.from_numpy(f).to(device)
+    """RoPE inverse frequencies theta^(-2i/d), i < d/2, from the library (kap_rope_inv_freq: fp64, rounded once to
+    fp32), as a tensor on `device`."""
+    out = torch.empty(d // 2, dtype=torch.float32)
+    _check("kap_rope_inv_freq", load().kap_rope_inv_freq(int(d), float(theta), ctypes.c_void_p(out.data_ptr())))
+    return out.to(device)

@@ -4,6 +4,7 @@
 
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <mutex>
 #include <string>
 
@@ -13,8 +14,16 @@ namespace kap {
 __device__ int g_error_word;
 
 namespace {
-
 thread_local std::string g_last_cuda_error;
+}  // namespace
+
+bool record_cuda_error(cudaError_t e) {
+  if (e == cudaSuccess) return false;
+  g_last_cuda_error = cudaGetErrorString(e);
+  return true;
+}
+
+namespace {
 
 constexpr int kMaxDevices = 64;
 
@@ -32,11 +41,7 @@ int *error_word() {
   return ptrs[dev];
 }
 
-kap_status cuda_status(cudaError_t e) {
-  if (e == cudaSuccess) return KAP_OK;
-  g_last_cuda_error = cudaGetErrorString(e);
-  return KAP_ECUDA;
-}
+kap_status cuda_status(cudaError_t e) { return record_cuda_error(e) ? KAP_ECUDA : KAP_OK; }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -395,6 +400,13 @@ const char *kap_status_str(kap_status s) {
     case KAP_EUNSUPPORTED: return "shape or dtype without a kernel in this build";
   }
   return "unknown status";
+}
+
+kap_status kap_rope_inv_freq(int32_t head_dim, double theta, float *inv_freq_host) {
+  if (!inv_freq_host || head_dim <= 0 || (head_dim & 1) || !std::isfinite(theta) || !(theta > 0.0)) return KAP_EINVAL;
+  for (int32_t i = 0; i < head_dim / 2; ++i)
+    inv_freq_host[i] = static_cast<float>(std::pow(theta, -2.0 * i / head_dim));
+  return KAP_OK;
 }
 
 const char *kap_last_cuda_error(void) { return g_last_cuda_error.c_str(); }

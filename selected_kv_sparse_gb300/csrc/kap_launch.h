@@ -90,4 +90,7 @@ cudaError_t launch_verify(const PoolArgs &p, const MapArgs &m, int max_q, int to
 // number of SMs of the current device (cached per device)
 int device_sm_count();
 
+// Records the text of a failed CUDA call for kap_last_cuda_error (this thread) and returns true when e is an error.
+bool record_cuda_error(cudaError_t e);
+
 }  // namespace kap

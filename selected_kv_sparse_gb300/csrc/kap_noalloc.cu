@@ -23,7 +23,8 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
-// Device address of the scratch array on the current device (looked up on the first call per device).
+// Device address of the scratch array on the current device (looked up on the first call per device and kept for
+// the life of the process: a cudaDeviceReset of that device invalidates it, see kap.h).
 cudaError_t scratch_address(void **out) {
   static void *addr[kMaxDevices] = {nullptr};
   static std::mutex mu;
@@ -54,11 +55,11 @@ extern "C" kap_status kap_attn_propose_noalloc(const kap_kv_pool *pool, const ka
       kap_propose_workspace_size(map->num_seqs, pool->num_kv_heads, pool->num_q_heads, pool->head_dim);
   if (need == 0 || need > kScratchBytes) return KAP_ECAPACITY;  // the shape needs more than the fixed scratch
   void *scratch = nullptr;
-  if (scratch_address(&scratch) != cudaSuccess) return KAP_ECUDA;
+  if (kap::record_cuda_error(scratch_address(&scratch))) return KAP_ECUDA;
   // The per-row arrival counters at the start of the scratch must be zero when the kernel starts; the array keeps
   // whatever the previous call left, so clear them on the caller's stream.
   const size_t counter_bytes = static_cast<size_t>(map->num_seqs) * pool->num_kv_heads * sizeof(int);
-  if (cudaMemsetAsync(scratch, 0, counter_bytes, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+  if (kap::record_cuda_error(cudaMemsetAsync(scratch, 0, counter_bytes, reinterpret_cast<cudaStream_t>(stream))))
     return KAP_ECUDA;
   return kap_attn_propose(pool, map, view, q_dev, out, lse, scratch, kScratchBytes, stream);
 }

@@ -112,6 +112,11 @@ def run_cycle_and_oracle(w, check_rows=None, nthreads=8, fused=True, ws_pages=0,
     res["S_orc"] = S
     sel, nsel = oracle_selection(w, S, f32(w.q_route))
     res["sel_orc"], res["nsel_orc"] = sel, nsel
+    if w.spans is None:   # page scores: the score workspace holds them [R][rows][max_pages] after the plan
+        rows = w.Hkv if w.per_kv_head else 1
+        res["scores_orc"], _ = oracle.scores(f32(w.q_route), S, bt, ctx, per_head=w.per_kv_head)
+        mp = int(w.block_table.shape[1])
+        res["scores_gpu"] = cyc.ws_score[: w.R * rows * mp * 4].view(torch.float32).view(w.R, rows, mp).cpu().numpy()
     res["sel_gpu"], res["nsel_gpu"] = i32(cyc.sel_ids), i32(cyc.n_sel)
     inv = oracle.inv_freq(w.d, w.theta)
     # proposal steps: oracle appends token i (RoPE'd) at position seq0 + i and attends from there
@@ -152,6 +157,27 @@ def run_cycle_and_oracle(w, check_rows=None, nthreads=8, fused=True, ws_pages=0,
     res["V_after_orc"], res["V_after_gpu"] = V, f32(Vp[:w.num_pages])
     res["K_pool"], res["V_pool"] = Kp, Vp
     return res
+
+
+def oracle_first_proposal(w, nthreads=8):
+    """The oracle's first proposal step on workload w, from the generator's tensors alone: summaries, selection,
+    the step token's K (RoPE at seq_len0) and V written into a copy of the pool, the query rotated at the same
+    position, then attention over the selection. Returns (o, lse); the inputs must not yet be modified by a cycle."""
+    K, V = f32(w.K), f32(w.V)
+    bt, ctx, seq0 = i32(w.block_table), i32(w.ctx_len), i32(w.seq_len0)
+    S = oracle.build_summaries(K, bt, ctx)
+    sel, nsel = oracle_selection(w, S, f32(w.q_route))
+    inv = oracle.inv_freq(w.d, w.theta)
+    krot = oracle.rope(f32(w.k_new_prop[0]), seq0, inv)
+    qrot = oracle.rope(f32(w.q_prop[0]), seq0, inv)
+    vp = f32(w.v_new_prop[0])
+    rnd = (lambda x: x.astype(np.float32)) if w.dtype == torch.float32 else \
+        (lambda x: torch.from_numpy(x).to(torch.bfloat16).float().numpy())
+    for r in range(w.R):
+        s = oracle.slot(bt[r], int(seq0[r]))
+        K[s // PAGE, :, s % PAGE] = rnd(krot[r])
+        V[s // PAGE, :, s % PAGE] = vp[r]
+    return oracle.attn_propose(rnd(qrot), K, V, bt, ctx, seq0 + 1, sel, nsel, nthreads=nthreads)
 
 
 def assert_close_attn(o_gpu, o_orc, lse_gpu, lse_orc, dtype, what=""):

@@ -71,6 +71,24 @@ def test_rope_inv_freq_matches_oracle(orc):
         assert np.array_equal(rope_inv_freq(d).numpy(), orc.inv_freq(d, 1.0e4))
 
 
+def test_rope_inv_freq_raw_abi(lib, orc):
+    """kap_rope_inv_freq through the raw C ABI: bit-identical to the oracle's table for several widths and bases;
+    documented argument errors (KAP_EINVAL = -1) for a NULL buffer, odd or non-positive d and a bad theta."""
+    f = lib.kap_rope_inv_freq
+    f.argtypes = [ctypes.c_int32, ctypes.c_double, ctypes.c_void_p]
+    f.restype = ctypes.c_int32
+    for d in (2, 64, 96, 128, 256):
+        for theta in (1.0e4, 5.0e5, 2.0):
+            out = np.full(d // 2, np.nan, dtype=np.float32)
+            assert f(d, theta, out.ctypes.data) == 0
+            assert np.array_equal(out, orc.inv_freq(d, theta)), (d, theta)
+    buf = np.zeros(64, dtype=np.float32)
+    assert f(128, 1.0e4, None) == -1
+    for d, theta in ((0, 1.0e4), (-2, 1.0e4), (63, 1.0e4), (64, 0.0), (64, -1.0), (64, float("nan")),
+                     (64, float("inf"))):
+        assert f(d, theta, buf.ctypes.data) == -1, (d, theta)
+
+
 def test_long_spans_recipe():
     import torch
     from workloads.gen import _spans_long

@@ -100,6 +100,20 @@ def test_view_and_slots_bit_exact(results, case):
 
 
 @pytest.mark.parametrize("case", CASES, ids=_id)
+def test_scores_bit_exact(results, case):
+    """The Q.K page scores themselves (not only the selection they lead to): bit-identical to the oracle's fixed-order
+    fp32 scores for every prompt page of every row."""
+    w, res = results[_id(case)]
+    if "scores_gpu" not in res:
+        pytest.skip("span selection has no scores")
+    ctx = w.ctx_len.cpu().numpy()
+    g, o = res["scores_gpu"], res["scores_orc"]
+    for r in range(w.R):
+        N = (int(ctx[r]) + 15) // 16
+        assert np.array_equal(g[r, :, :N].view(np.uint32), o[r, :, :N].view(np.uint32)), r
+
+
+@pytest.mark.parametrize("case", CASES, ids=_id)
 def test_append_rope(results, case):
     w, res = results[_id(case)]
     Kg, Ko = res["K_after_gpu"], res["K_after_orc"]

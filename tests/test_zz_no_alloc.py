@@ -1,4 +1,4 @@
-"""The allocation-free proposal entry point (kap_attn_propose_noalloc) against the workspace one.
+"""The allocation-free proposal entry point (kap_attn_propose_noalloc) against the workspace one and the oracle.
 
 Callers such as a serving host that fixes its device memory budget at start-up, or a plug-in with no access to the
 host's allocator, cannot hand the library a freshly allocated workspace; the no-alloc entry point runs the same
@@ -14,9 +14,10 @@ pytestmark = pytest.mark.gpu
 
 @pytest.mark.parametrize("name,kw", [("llama", dict(scale=1 / 16)), ("mixed", dict(scale=1 / 32, ragged=True))])
 def test_noalloc_matches_workspace_entry_point(kap, name, kw):
-    from tests.gpu_helpers import TOL, make_cycle
+    from tests.gpu_helpers import TOL, assert_close_attn, make_cycle, oracle_first_proposal
     from workloads import make_workload
     w = make_workload(name, device="cuda", **kw)
+    o_orc, lse_orc = oracle_first_proposal(w)   # before the cycle writes the step token into the pool
     pool, cyc = make_cycle(w)
     kap.kap_build_summaries(pool, kap.PageMap(w.block_table, w.ctx_len, w.seq_len0))
     q = w.q_prop[0].clone()
@@ -36,6 +37,8 @@ def test_noalloc_matches_workspace_entry_point(kap, name, kw):
         lerr = (l - ref_l).abs().max().item()
         assert np.isfinite(err) and err <= TOL[w.dtype], (call, err)
         assert np.isfinite(lerr) and lerr <= 1e-3, (call, lerr)
+        # and against the oracle's own first proposal step on the generator's inputs
+        assert_close_attn(o.float().cpu().numpy(), o_orc, l.cpu().numpy(), lse_orc, w.dtype, f"noalloc call {call}")
     assert kap.kap_device_error() == 0
 
 
