@@ -118,7 +118,7 @@ struct Cfg {
   static_assert(NI % RC == 0, "chunk rows");
   static_assert(kBarSeg0 + NSEG <= 16, "named barriers");
   static_assert(QPB % 16 == 0, "query area alignment");
-  static_assert(NCW < SLOTS, "a warp's next entry lies in a later slot");
+  static_assert(NCW <= SLOTS, "a round of issues fits in the ring");
 };
 
 struct Params {
@@ -173,13 +173,16 @@ __device__ __forceinline__ int ld_acquire_shared(const int *p) {
   return v;
 }
 
-// Waits until ring entry kk (this CTA's entry index) has landed in its slot. Warp groups consume the ring out of
-// order, so the slot's barrier may still be a phase (or more) behind: a parity wait can then return for an earlier
-// phase. The producer stamps the slot with kk before the phase of kk can complete, so after each completed wait the
-// stamp tells whether the phase was ours; if not, wait for the other parity (the pending earlier phase) and retry.
-// All waits suspend in hardware and are bounded.
+// Waits until ring entry kk (this CTA's entry sequence number) has landed in its slot. The slot's barrier completes
+// one phase per entry issued to it, in order, and a warp may reach its entry before the slot's earlier entries have
+// landed: a parity wait can then return for an earlier phase. The producer stamps the slot with kk before the phase
+// of kk can complete, so after each completed wait the stamp tells whether the phase was ours; if not, wait for the
+// other parity (the pending earlier phase) and retry. Every attempt that fails moves the slot on by a phase, and
+// at most kk / SLOTS phases precede kk's, which bounds the attempts. All waits suspend in hardware and are bounded.
+template <int SLOTS>
 __device__ __forceinline__ bool wait_entry(const int *stamp, uint64_t *full, int kk, uint32_t parity, int *err) {
-  for (int attempt = 0; attempt < 8; ++attempt) {
+  const int attempts = kk / SLOTS + 2;
+  for (int attempt = 0; attempt < attempts; ++attempt) {
     if (!mbar_wait(full, parity, err)) return false;
     if (ld_acquire_shared(stamp) == kk) return true;
     if (!mbar_wait(full, parity ^ 1u, err)) return false;
@@ -388,81 +391,102 @@ __global__ void __launch_bounds__((Shape<T, D, G>::THREADS)) __maxnreg__((Shape<
     if (warp == C::NCW) {
       // ============================================================================================== producer
       const uint64_t pol = l2_evict_first_policy();  // the selected pages are streamed once per launch
-      // The window's entries past the ring's first fill are prefetched into L2 at once (up to kPrefetchAhead), so
-      // that the ring refills from L2 when the consumers free their slots; before the dependency wait, only pages
-      // whose visible tokens are all prompt tokens.
-      if (nseg > 0) {
-        const int64_t pf_lo = segs[0].b + C::SLOTS, pf_hi = min(win_end, pf_lo + kPrefetchAhead);
-        for (int si = 0; si < nseg && pf_lo < pf_hi; ++si) {
-          const Seg sg = segs[si];
-          const int64_t lo = sg.b > pf_lo ? sg.b : pf_lo, hi = sg.e < pf_hi ? sg.e : pf_hi;
-          if (lo >= hi) continue;
-          const int r = sg.row / p.hkv, h = sg.row - r * p.hkv;
-          const int L = p.ctx_len[r], S = p.seq_len[r], nsel = p.vnsel[sg.vr];
-          for (int64_t e = lo + lane; e < hi; e += 32) {
-            const int i = static_cast<int>(e - sg.rb);
-            const size_t o = static_cast<size_t>(sg.vr) * p.vcap + i;
-            const int page = p.vbt[o], base = p.vlp[o] * kPage;
-            const int thi = min(kPage, S - base), tlo = (i < nsel) ? 0 : max(0, L - base);
-            if (thi > tlo && page >= 0 && page < p.num_pages && (waited || base + thi <= L)) {
-              const size_t off = (static_cast<size_t>(page) * p.hkv + h) * kPage * D;
-              bulk_prefetch_l2(Kp + off, C::CHUNK);
-              bulk_prefetch_l2(Vp + off, C::CHUNK);
-            }
+      // Issue order: the window's segments take turns, each issuing in round j the entries j*nw .. j*nw + nw - 1
+      // of its own range (nw = its warps), so that all groups stream at once and every warp's next entry is about
+      // one ring length ahead at most. Entry u of a round, counted over the segments in order, gets the sequence
+      // number (kacc + u) of this CTA: its ring slot and the stamp the consumer checks.
+      // The entries past the ring's first fill (up to kPrefetchAhead, in each segment's share) are prefetched into
+      // L2 at once, so that the ring refills from L2 when the consumers free their slots; before the dependency
+      // wait, only pages whose visible tokens are all prompt tokens.
+      for (int si = 0; si < nseg; ++si) {
+        const Seg sg = segs[si];
+        const int64_t n = sg.e - sg.b;
+        const int64_t lo = sg.b + (static_cast<int64_t>(C::SLOTS) * sg.nw) / C::NCW;
+        const int64_t hi = min(sg.e, sg.b + (static_cast<int64_t>(C::SLOTS + kPrefetchAhead) * sg.nw) / C::NCW);
+        if (n <= 0 || lo >= hi) continue;
+        const int r = sg.row / p.hkv, h = sg.row - r * p.hkv;
+        const int L = p.ctx_len[r], S = p.seq_len[r], nsel = p.vnsel[sg.vr];
+        for (int64_t e = lo + lane; e < hi; e += 32) {
+          const int i = static_cast<int>(e - sg.rb);
+          const size_t o = static_cast<size_t>(sg.vr) * p.vcap + i;
+          const int page = p.vbt[o], base = p.vlp[o] * kPage;
+          const int thi = min(kPage, S - base), tlo = (i < nsel) ? 0 : max(0, L - base);
+          if (thi > tlo && page >= 0 && page < p.num_pages && (waited || base + thi <= L)) {
+            const size_t off = (static_cast<size_t>(page) * p.hkv + h) * kPage * D;
+            bulk_prefetch_l2(Kp + off, C::CHUNK);
+            bulk_prefetch_l2(Vp + off, C::CHUNK);
           }
         }
       }
-      for (int si = 0; si < nseg; ++si) {
-        const Seg sg = segs[si];
-        const int r = sg.row / p.hkv, h = sg.row - r * p.hkv;
-        const int L = p.ctx_len[r], S = p.seq_len[r], nsel = p.vnsel[sg.vr];
-        const int rn = static_cast<int>(sg.re - sg.rb);
-        for (int64_t e0 = sg.b; e0 < sg.e; e0 += C::BATCH) {
-          const int64_t e = e0 + lane;
-          const bool act = lane < C::BATCH && e < sg.e;
-          int i = 0, page = 0, base = 0, tlo = 0, thi = 0;
-          if (act) {
-            i = static_cast<int>(e - sg.rb);  // entry index within the row's view
-            const size_t o = static_cast<size_t>(sg.vr) * p.vcap + i;
-            const int lp = p.vlp[o];
-            page = p.vbt[o];
-            base = lp * kPage;
-            thi = min(kPage, S - base);
-            tlo = (i < nsel) ? 0 : max(0, L - base);
-            if (thi > tlo && (page < 0 || page >= p.num_pages)) {
-              set_error(p.err, kErrPage);
-              tlo = thi = 0;
+      int64_t kacc = (nseg > 0) ? segs[0].b - cta_begin : 0;
+      for (int j = 0;; ++j) {
+        // this round's share of every segment; lane u < total takes entry u of the round
+        int total = 0, my_si = -1, my_u = 0;
+#pragma unroll
+        for (int s2 = 0; s2 < C::NSEG; ++s2) {
+          if (s2 < nseg) {
+            const int64_t left = (segs[s2].e - segs[s2].b) - static_cast<int64_t>(j) * segs[s2].nw;
+            const int c = left <= 0 ? 0 : (left < segs[s2].nw ? static_cast<int>(left) : segs[s2].nw);
+            if (lane >= total && lane < total + c) {
+              my_si = s2;
+              my_u = lane - total;
             }
-            if (thi <= tlo) tlo = thi = 0;
+            total += c;
           }
-          // Before the dependency wait only pages whose visible tokens are all prompt tokens are copied: a later
-          // position of a page (a generated token) may have been written by the previous kernel.
-          if (!waited && __any_sync(0xffffffffu, act && thi > tlo && base + thi > L)) {
-            grid_dependency_wait();
-            waited = true;
-          }
-          if (act) {
-            int step_tok = -1;
-            if (fused) {
-              const int tk = S - 1 - base;
-              if (tk >= tlo && tk < thi) step_tok = tk;
-              if (i == rn - 1 && base + kPage <= S - 1) set_error(p.err, kErrLength);  // the view misses P
-            }
-            const int64_t k = e - cta_begin;
-            const int slot = static_cast<int>(k % C::SLOTS);
-            if (k >= C::SLOTS) mbar_wait(&empty[slot], static_cast<uint32_t>((k / C::SLOTS) - 1) & 1u, p.err);
-            smeta[slot] = make_int4(tlo | (thi << 16), step_tok, page, static_cast<int>(k));
-            if (thi > tlo) {
-              const size_t off = (static_cast<size_t>(page) * p.hkv + h) * kPage * D;
-              mbar_arrive_expect_tx(&full[slot], 2 * C::CHUNK);
-              bulk_g2s_stream(kv + slot * C::SLOT, Kp + off, C::CHUNK, &full[slot], pol);
-              bulk_g2s_stream(kv + slot * C::SLOT + C::CHUNK, Vp + off, C::CHUNK, &full[slot], pol);
-            } else {
-              mbar_arrive(&full[slot]);
-            }
-          }
-          __syncwarp();
         }
+        if (total == 0) break;
+        const bool act = my_si >= 0;
+        int i = 0, page = 0, base = 0, tlo = 0, thi = 0, L = 0, S = 0, h = 0, rn = 0;
+        if (act) {
+          const Seg sg = segs[my_si];
+          const int r = sg.row / p.hkv;
+          h = sg.row - r * p.hkv;
+          L = p.ctx_len[r];
+          S = p.seq_len[r];
+          const int nsel = p.vnsel[sg.vr];
+          rn = static_cast<int>(sg.re - sg.rb);
+          const int64_t e = sg.b + static_cast<int64_t>(j) * sg.nw + my_u;
+          i = static_cast<int>(e - sg.rb);  // entry index within the row's view
+          const size_t o = static_cast<size_t>(sg.vr) * p.vcap + i;
+          const int lp = p.vlp[o];
+          page = p.vbt[o];
+          base = lp * kPage;
+          thi = min(kPage, S - base);
+          tlo = (i < nsel) ? 0 : max(0, L - base);
+          if (thi > tlo && (page < 0 || page >= p.num_pages)) {
+            set_error(p.err, kErrPage);
+            tlo = thi = 0;
+          }
+          if (thi <= tlo) tlo = thi = 0;
+        }
+        // Before the dependency wait only pages whose visible tokens are all prompt tokens are copied: a later
+        // position of a page (a generated token) may have been written by the previous kernel.
+        if (!waited && __any_sync(0xffffffffu, act && thi > tlo && base + thi > L)) {
+          grid_dependency_wait();
+          waited = true;
+        }
+        if (act) {
+          int step_tok = -1;
+          if (fused) {
+            const int tk = S - 1 - base;
+            if (tk >= tlo && tk < thi) step_tok = tk;
+            if (i == rn - 1 && base + kPage <= S - 1) set_error(p.err, kErrLength);  // the view misses P
+          }
+          const int64_t k = kacc + lane;
+          const int slot = static_cast<int>(k % C::SLOTS);
+          if (k >= C::SLOTS) mbar_wait(&empty[slot], static_cast<uint32_t>((k / C::SLOTS) - 1) & 1u, p.err);
+          smeta[slot] = make_int4(tlo | (thi << 16), step_tok, page, static_cast<int>(k));
+          if (thi > tlo) {
+            const size_t off = (static_cast<size_t>(page) * p.hkv + h) * kPage * D;
+            mbar_arrive_expect_tx(&full[slot], 2 * C::CHUNK);
+            bulk_g2s_stream(kv + slot * C::SLOT, Kp + off, C::CHUNK, &full[slot], pol);
+            bulk_g2s_stream(kv + slot * C::SLOT + C::CHUNK, Vp + off, C::CHUNK, &full[slot], pol);
+          } else {
+            mbar_arrive(&full[slot]);
+          }
+        }
+        __syncwarp();
+        kacc += total;
       }
     } else if (nseg > 0) {
       // ============================================================================================= consumers
@@ -554,13 +578,31 @@ __global__ void __launch_bounds__((Shape<T, D, G>::THREADS)) __maxnreg__((Shape<
           ok_own[c * C::VPC + k] = v < C::RC * G;
           wp_off[c * C::VPC + k] = tok_own[c * C::VPC + k] * G + g_own[c * C::VPC + k];
         }
-      // this warp's entries: kk = kk0, kk0 + nw, ... (CTA-local indices, fewer than 2^31) in slot kk % SLOTS,
-      // phase parity (kk / SLOTS) & 1, both advanced as kk moves on (nw < SLOTS)
-      const int kk0 = static_cast<int>(sg.b - cta_begin) + gw, kk_end = static_cast<int>(sg.e - cta_begin);
-      int slot = kk0 % C::SLOTS;
-      uint32_t ph = static_cast<uint32_t>(kk0 / C::SLOTS) & 1u;
-      for (int kk = kk0; kk < kk_end; kk += nw) {
-        wait_entry(&smeta[slot].w, &full[slot], kk, ph, p.err);
+      // This warp's entries are gw, gw + nw, ... of its segment: the one of round j has the sequence number
+      // k0 + (entries of all segments in earlier rounds) + (entries of earlier segments in round j) + gw, the order
+      // in which the producer issues them (fewer than 2^31 per CTA); slot kk % SLOTS, phase parity (kk / SLOTS) & 1.
+      int sn[C::NSEG], sw[C::NSEG];
+#pragma unroll
+      for (int s2 = 0; s2 < C::NSEG; ++s2) {
+        sn[s2] = s2 < nseg ? static_cast<int>(segs[s2].e - segs[s2].b) : 0;
+        sw[s2] = s2 < nseg ? segs[s2].nw : 1;
+      }
+      const int n_mine = static_cast<int>(sg.e - sg.b);
+      int issued = static_cast<int>(segs[0].b - cta_begin);  // sequence number of round j's first entry
+      for (int j = 0; j * nw + gw < n_mine; ++j) {
+        int before = 0, round = 0;
+#pragma unroll
+        for (int s2 = 0; s2 < C::NSEG; ++s2) {
+          const int left = sn[s2] - j * sw[s2];
+          const int c = left <= 0 ? 0 : (left < sw[s2] ? left : sw[s2]);
+          before += (s2 < si) ? c : 0;
+          round += c;
+        }
+        const int kk = issued + before + gw;
+        issued += round;
+        const int slot = kk % C::SLOTS;
+        if (!wait_entry<C::SLOTS>(&smeta[slot].w, &full[slot], kk, static_cast<uint32_t>(kk / C::SLOTS) & 1u, p.err))
+          break;  // timed out (error recorded): stop reading the ring
         const int4 mt = smeta[slot];
         const int tlo = mt.x & 0xffff, thi = mt.x >> 16;
         unsigned char *kb = kv + slot * C::SLOT;
@@ -700,11 +742,6 @@ __global__ void __launch_bounds__((Shape<T, D, G>::THREADS)) __maxnreg__((Shape<
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
-        slot += nw;
-        if (slot >= C::SLOTS) {
-          slot -= C::SLOTS;
-          ph ^= 1u;
-        }
       }
 
       // ---- end of this warp's share of the segment: its state into comb[warp]
