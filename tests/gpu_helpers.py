@@ -159,6 +159,106 @@ def run_cycle_and_oracle(w, check_rows=None, nthreads=8, fused=True, ws_pages=0,
     return res
 
 
+def run_cycle_per_request(w, nthreads=16, fused=True):
+    """One full cycle on the GPU, then the oracle request by request on that request's own pages only, for pools
+    too large to copy to the host (the mixed batch's 2^20-page pool holds 64 GiB).
+
+    Each request's pages (its block-table row, prompt and tail) are copied to the host before the cycle, in the pool
+    dtype; the oracle then runs on them with a local table 0..n-1, appending the cycle's tokens itself. Yields, per
+    request r, a dict of GPU and oracle results: summaries, scores, selection, view row, slots, appended K/V, every
+    proposal step and the verify rows.
+    """
+    pool, cyc = make_cycle(w, fused=fused)
+    kap.kap_build_summaries(pool, kap.PageMap(w.block_table, w.ctx_len, w.seq_len0))
+    bt, ctx, seq0 = i32(w.block_table), i32(w.ctx_len), i32(w.seq_len0)
+    qo = i32(w.q_offsets)
+    horizon = max(w.k_prop, int(w.n_q.max()))
+    npg = [(int(ctx[r]) + horizon + PAGE - 1) // PAGE for r in range(w.R)]
+    snap = []
+    for r in range(w.R):   # the generator's pages of request r, before the cycle writes into them
+        idx = w.block_table[r, :npg[r]].to(torch.int64)
+        snap.append((w.K.index_select(0, idx).cpu(), w.V.index_select(0, idx).cpu()))
+    q_route_np = f32(w.q_route)
+    q_prop_raw, q_ver_raw = f32(w.q_prop), f32(w.q_ver)
+    kp, vp = f32(w.k_new_prop), f32(w.v_new_prop)
+    kv_, vv_ = f32(w.k_new_ver), f32(w.v_new_ver)
+    cyc.run(w.q_route.clone(), w.q_prop.clone(), w.k_new_prop, w.v_new_prop, w.q_ver.clone(), w.k_new_ver,
+            w.v_new_ver)
+    torch.cuda.synchronize()
+    mp = int(w.block_table.shape[1])
+    rows = cyc.rows
+    scores_gpu = cyc.ws_score[: w.R * rows * mp * 4].view(torch.float32).view(w.R, rows, mp).cpu().numpy()
+    sel_gpu, nsel_gpu = i32(cyc.sel_ids), i32(cyc.n_sel)
+    vbt, vlp = i32(cyc.view.block_table), i32(cyc.view.logical_page)
+    vn, vns = i32(cyc.view.n_entries), i32(cyc.view.n_selected)
+    slots = cyc.slots_prop.cpu().numpy().reshape(w.R, cyc.horizon)
+    o_prop, lse_prop = f32(cyc.o_prop), f32(cyc.lse_prop)
+    o_ver, lse_ver = f32(cyc.o_ver), f32(cyc.lse_ver)
+    inv = oracle.inv_freq(w.d, w.theta)
+    rnd = (lambda x: x.astype(np.float32)) if w.dtype == torch.float32 else \
+        (lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16).float().numpy())
+    for r in range(w.R):
+        N = (int(ctx[r]) + PAGE - 1) // PAGE
+        idx = w.block_table[r, :npg[r]].to(torch.int64)
+        K = snap[r][0].float().numpy()
+        V = snap[r][1].float().numpy()
+        lbt = np.arange(npg[r], dtype=np.int32)[None]
+        lctx, lseq = ctx[r:r + 1], seq0[r:r + 1]
+        out = dict(r=r, N=N)
+        out["S_gpu"] = pool.k_summary.index_select(0, idx[:N]).cpu().numpy()
+        S = oracle.build_summaries(K, lbt, lctx)
+        out["S_orc"] = S[:N]
+        if w.spans is None:
+            sc, _ = oracle.scores(q_route_np[r:r + 1], S, lbt, lctx, per_head=w.per_kv_head)
+            out["scores_orc"], out["scores_gpu"] = sc[0, :, :N], scores_gpu[r, :, :N]
+            a, rr, k = (int(x) for x in w.ark[r].tolist())
+            sels = [oracle.topk_ark(sc[0, v], N, a, rr, k) for v in range(rows)]
+        else:
+            so = i32(w.span_offsets)
+            a, rr, _ = (int(x) for x in w.ark[r].tolist())
+            sels = [oracle.select_spans(N, i32(w.spans)[so[r]:so[r + 1]], a, rr)]
+        cap = max(1, max(len(x) for x in sels))
+        sel = np.zeros((1, rows, cap), np.int32)
+        nsel = np.zeros((1, rows), np.int32)
+        for v, x in enumerate(sels):
+            sel[0, v, :len(x)] = x
+            nsel[0, v] = len(x)
+        out["sel_orc"], out["nsel_orc"] = sel[0], nsel[0]
+        out["sel_gpu"], out["nsel_gpu"] = sel_gpu[r], nsel_gpu[r]
+        out["view"] = []
+        for v in range(rows):
+            cbt, clog, ns = oracle.compile_view_row(bt[r], int(ctx[r]), int(seq0[r]), cyc.horizon,
+                                                    sels[v])
+            out["view"].append(((cbt, clog, ns), (vbt[r, v, :vn[r, v]], vlp[r, v, :vn[r, v]], vns[r, v])))
+        out["slots"] = [(slots[r, i], oracle.slot(bt[r], int(seq0[r]) + i)) for i in range(cyc.horizon)]
+        # proposal steps: the oracle appends step token i at seq0 + i (local slot) and attends from there
+        out["prop"] = []
+        for i in range(w.k_prop):
+            pos = np.array([seq0[r] + i], np.int32)
+            krot = oracle.rope(kp[i, r:r + 1], pos, inv)
+            qrot = oracle.rope(q_prop_raw[i, r:r + 1], pos, inv)
+            s = oracle.slot(lbt[0], int(pos[0]))
+            K[s // PAGE, :, s % PAGE] = rnd(krot[0])
+            V[s // PAGE, :, s % PAGE] = vp[i, r]
+            o, l = oracle.attn_propose(rnd(qrot), K, V, lbt, lctx, lseq + i + 1, sel, nsel, nthreads=nthreads)
+            out["prop"].append((o_prop[i, r], o[0], lse_prop[i, r], l[0]))
+        # verify window at seq0 .. seq0 + n_q - 1
+        nq = int(qo[r + 1] - qo[r])
+        posv = (seq0[r] + np.arange(nq)).astype(np.int32)
+        krot = oracle.rope(kv_[qo[r]:qo[r + 1]], posv, inv)
+        qrot = oracle.rope(q_ver_raw[qo[r]:qo[r + 1]], posv, inv)
+        for j in range(nq):
+            s = oracle.slot(lbt[0], int(posv[j]))
+            K[s // PAGE, :, s % PAGE] = rnd(krot[j])
+            V[s // PAGE, :, s % PAGE] = vv_[qo[r] + j]
+        o, l = oracle.attn_verify(rnd(qrot), K, V, lbt, np.array([0, nq], np.int32), lseq, nthreads=nthreads)
+        out["ver"] = (o_ver[qo[r]:qo[r + 1]], o, lse_ver[qo[r]:qo[r + 1]], l)
+        out["K_after"] = (w.K.index_select(0, idx).float().cpu().numpy(), K)
+        out["V_after"] = (w.V.index_select(0, idx).float().cpu().numpy(), V)
+        out["k_in_max"] = max(float(np.abs(kp[:, r]).max()), float(np.abs(kv_[qo[r]:qo[r + 1]]).max()))
+        yield out
+
+
 def oracle_first_proposal(w, nthreads=8):
     """The oracle's first proposal step on workload w, from the generator's tensors alone: summaries, selection,
     the step token's K (RoPE at seq_len0) and V written into a copy of the pool, the query rotated at the same

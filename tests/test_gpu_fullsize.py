@@ -41,3 +41,47 @@ def test_full_size_cycle(kap, case):
     assert kap.kap_device_error() == 0
     del one, res, w
     torch.cuda.empty_cache()
+
+
+def test_mixed_serving_batch_at_full_size(kap):
+    """The mixed serving batch at its stated size: 32 requests with prompts log-uniform in 4K-128K tokens, per-request
+    retention s in {2, 5.5, 10, 25}% and splits A1R2 / A4R4 / A0R0, one proposal launch for every request and one
+    verify launch with windows of 2, 4 or 8, all pages scattered over a shared 2^20-page pool (64 GiB of K and V).
+    The oracle runs request by request on that request's own pages; every element is compared."""
+    import numpy as np
+    import torch
+    from tests.gpu_helpers import LSE_TOL, TOL, assert_close_attn, run_cycle_per_request
+    from workloads import make_workload
+    w = make_workload("mixed", device="cuda")
+    assert w.num_pages == 1 << 20 and w.R == 32
+    ctx = w.ctx_len.cpu().numpy()
+    assert ctx.min() >= 4096 and ctx.max() < 131072
+    seen = 0
+    for res in run_cycle_per_request(w, nthreads=16):
+        r = res["r"]
+        assert np.array_equal(res["S_gpu"].view(np.uint32), res["S_orc"].view(np.uint32)), r
+        assert np.array_equal(res["scores_gpu"].view(np.uint32), res["scores_orc"].view(np.uint32)), r
+        assert np.array_equal(res["nsel_gpu"], res["nsel_orc"]), r
+        for v in range(len(res["nsel_orc"])):
+            n = res["nsel_orc"][v]
+            assert np.array_equal(res["sel_gpu"][v, :n], res["sel_orc"][v, :n]), (r, v)
+        for (cbt, clog, ns), (gbt, glp, gns) in res["view"]:
+            assert gns == ns and np.array_equal(gbt, cbt) and np.array_equal(glp, clog), r
+        for g_slot, o_slot in res["slots"]:
+            assert g_slot == o_slot, r
+        Kg, Ko = res["K_after"]
+        Vg, Vo = res["V_after"]
+        assert np.array_equal(np.isnan(Kg), np.isnan(Ko)) and np.array_equal(np.isnan(Vg), np.isnan(Vo)), r
+        m = ~np.isnan(Ko)
+        ulp = np.maximum(np.abs(Ko[m]), 1e-30) * 2.0 ** -7
+        assert (np.abs(Kg[m] - Ko[m]) <= 2 * ulp + 2.0 ** -19 * res["k_in_max"]).all(), r
+        assert np.array_equal(Vg[~np.isnan(Vo)], Vo[~np.isnan(Vo)]), r
+        for i, (og, oo, lg, lo) in enumerate(res["prop"]):
+            assert_close_attn(og, oo, lg, lo, w.dtype, f"request {r} proposal {i}")
+        og, oo, lg, lo = res["ver"]
+        assert_close_attn(og, oo, lg, lo, w.dtype, f"request {r} verify")
+        seen += 1
+    assert seen == 32
+    assert kap.kap_device_error() == 0
+    del w
+    torch.cuda.empty_cache()
