@@ -228,7 +228,81 @@ class SideFlowDecode:
                     self.cycles[l + 1].plan(q_route[l + 1], self.side)
                     self.routed[l + 1].record(self.side)
             main.wait_event(self.routed[l])
-            # the view was written on the other stream and is complete: the kernel just ahead of this one on the
-            # main stream is the previous layer's proposal, so the view may be treated as settled
-            c.propose_step(0, q[l], k_new[l], v_new[l], main, settled=True)
+            # Not settled: the view comes from a kernel on the other stream. In a captured graph every incoming
+            # edge of a dependent launch is programmatic, the one from the routing kernel included, so the proposal
+            # may start before the routing has finished; it must read the view only after its dependency wait.
+            c.propose_step(0, q[l], k_new[l], v_new[l], main, settled=False)
         main.wait_stream(self.side)
+
+
+class DecodeLoop:
+    """EarlySelectKV decode over `steps` generated tokens on one attention layer, on the library calls.
+
+    EarlySelectKV page: every decode step routes (scores the K-summary cache on a proxy query, keeps the top pages)
+    and then attends with the real query over the chosen pages only. Before step t the routing compiles the view at
+    the committed length seq_len0 + t with a one-token horizon; step t then appends its token at position
+    seq_len0 + t and attends over the selected prompt pages and every generated token (the view's tail grows by a
+    page every 16 steps). Summaries cover prompt tokens only, so the generated tokens need no refresh.
+
+    The lengths of every step are known ahead (one token per step), so each step has its own page map in device
+    memory and nothing runs on the host between steps: a run of steps can be captured in one CUDA graph. plan() and
+    propose_step() act on the current step; advance() moves to the next (the same interface as DecodeCycle's
+    single-step use, so SideFlowDecode can run a stack of loops).
+    """
+
+    def __init__(self, pool: kb.KVPool, block_table: torch.Tensor, ctx_len: torch.Tensor, seq_len0: torch.Tensor,
+                 steps: int, inv_freq: torch.Tensor, policy: kb.AccessPolicy, s_max: float = 1.0):
+        dev = block_table.device
+        self.pool, self.policy, self.inv_freq, self.s_max = pool, policy, inv_freq, s_max
+        self.steps = int(steps)
+        self.R = int(block_table.shape[0])
+        self.Hq = pool.num_q_heads
+        self.Hkv = int(pool.k_pages.shape[1])
+        self.d = int(pool.k_pages.shape[3])
+        self.rows = self.Hkv if policy.per_kv_head else 1
+        self.sel_cap = int(policy.cap)
+        self.view_cap = self.sel_cap + (self.steps + PAGE - 1) // PAGE + 2   # selected pages + every tail page
+        ar = torch.arange(self.steps + 1, dtype=torch.int32, device=dev)
+        self.lens = (seq_len0.to(torch.int32)[None, :] + ar[:, None]).contiguous()   # [steps + 1][R]
+        self.maps = [kb.PageMap(block_table, ctx_len, self.lens[t]) for t in range(self.steps + 1)]
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.sel_ids = torch.zeros(self.R, self.rows, self.sel_cap, **i32)
+        self.n_sel = torch.zeros(self.R, self.rows, **i32)
+        self.view = kb.View.empty(self.R, self.rows, self.view_cap, dev)
+        self.fallback = torch.zeros(self.R, **i32)
+        self.slots = torch.zeros(self.R, dtype=torch.int64, device=dev)
+        self.pos = torch.zeros(self.R, **i32)
+        mp = int(block_table.shape[1])
+        self.ws_score = kb.workspace(kb.kap_score_workspace_size(self.R, self.rows, mp), dev)
+        self.ws_prop = kb.workspace(kb.kap_propose_workspace_size(self.R, self.Hkv, self.Hq, self.d), dev)
+        self.o = torch.empty(self.steps, self.R, self.Hq, self.d, dtype=pool.dtype, device=dev)
+        self.lse = torch.empty(self.steps, self.R, self.Hq, dtype=torch.float32, device=dev)
+        self.t = 0
+        self._routed = False
+
+    def plan(self, q_route: torch.Tensor, stream=None):
+        """Routing of step t: scores on q_route [R][Hq][d], A/R/K top-K and the view at length seq_len0 + t."""
+        kb.kap_score_topk_view(self.pool, self.maps[self.t], q_route, self.policy, self.sel_ids, self.n_sel,
+                               self.ws_score, 1, self.view, self.fallback, self.s_max, self.slots, self.pos, stream)
+        self._routed = True
+
+    def propose_step(self, i: int, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, stream=None,
+                     settled: Optional[bool] = None):
+        """Step t: the token's K (RoPE at seq_len0 + t) and V into the pool, attention of q (before RoPE) over the
+        view; outputs o[t], lse[t]. i is the step's index within a cycle and must be 0 (one token per step)."""
+        if i != 0:
+            raise ValueError("a decode step proposes one token")
+        st = (not self._routed) if settled is None else bool(settled)
+        kb.kap_append_propose(self.pool, self.maps[self.t + 1], self.view, q, k_new, v_new, self.inv_freq,
+                              self.o[self.t], self.lse[self.t], self.ws_prop, stream, settled=st)
+        self._routed = False
+
+    def advance(self):
+        if self.t + 1 > self.steps:
+            raise ValueError("the loop has run all its steps")
+        self.t += 1
+
+    def reset(self):
+        """Back to step 0 (a replayed loop writes the same tokens into the same slots)."""
+        self.t = 0
+        self._routed = False

@@ -60,6 +60,9 @@ class Workload:
     needles: List[List[int]] = field(default_factory=list)
     theta: float = 1.0e4
     sigma: float = 1.0
+    # [k_prop][R][Hq][d] the routing query of every proposal step (early workload: each step's own noisy proxy of
+    # its query, for a decode loop that re-routes at every step); step 0 equals q_route
+    q_route_steps: Optional[torch.Tensor] = None
 
     @property
     def max_pages(self) -> int:
@@ -287,6 +290,16 @@ def make_workload(name: str, device="cpu", scale: float = 1.0, ragged: bool = Fa
     k_new_ver = _randn((tq, Hkv, d), g, device, sigma).to(dtype)
     v_new_ver = _randn((tq, Hkv, d), g, device, sigma).to(dtype)
 
+    # Decode-loop proxies of the early workload: the proxy of step t > 0 is its query plus fresh N(0, 0.3^2) noise,
+    # drawn after everything above so that the other tensors do not depend on the number of steps.
+    q_route_steps = None
+    if name == "early":
+        q_route_steps = torch.empty((k_prop, R, Hq, d), dtype=torch.float32, device=device)
+        q_route_steps[0] = q_route
+        if k_prop > 1:
+            q_route_steps[1:] = q_prop[1:] + _randn((k_prop - 1, R, Hq, d), g, device, 0.3)
+        q_route_steps = q_route_steps.to(dtype)
+
     dev = lambda t: t.to(device) if t is not None else None  # noqa: E731
     return Workload(
         name=name, dtype=dtype, R=R, Hq=Hq, Hkv=Hkv, d=d, num_pages=P, K=K, V=V,
@@ -296,7 +309,7 @@ def make_workload(name: str, device="cpu", scale: float = 1.0, ragged: bool = Fa
         n_q=dev(torch.tensor(n_q, dtype=torch.int32)), q_offsets=dev(q_offsets), q_ver=q_ver,
         k_new_ver=k_new_ver, v_new_ver=v_new_ver, ark=dev(torch.tensor(ark, dtype=torch.int32)),
         per_kv_head=per_kv_head, spans=dev(spans), span_offsets=dev(span_offsets), needles=needles,
-        sigma=sigma)
+        sigma=sigma, q_route_steps=q_route_steps)
 
 
 def make_prior(w: Workload, num_layers: int = 32, device="cpu", seed_offset: int = 0,
