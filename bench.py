@@ -48,6 +48,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-accept", action="store_true", help="skip the acceptance and commit timing")
     ap.add_argument("--no-materialize", action="store_true", help="skip the materialised-workspace timing")
     ap.add_argument("--no-side-flow", action="store_true", help="skip the EarlySelectKV side-flow timing")
+    ap.add_argument("--no-decode-loop", action="store_true", help="skip the 1024-step EarlySelectKV decode loop")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the long-context and mixed-batch workload lines")
     ap.add_argument("--unfused", action="store_true", help="separate KV-append and proposal launches per step")
     ap.add_argument("--no-overlap", action="store_true",
                     help="proposal kernels wait for the previous kernel before reading their view")
@@ -227,7 +230,7 @@ def time_prior(layers, steps: int, hbm_peak: float, dev):
 
 
 # ------------------------------------------------------------------------------ EarlySelectKV side flow
-def time_side_flow(steps: int, dev, layers_n: int = 8):
+def time_side_flow(steps: int, dev, hbm_peak: float, layers_n: int = 8):
     """EarlySelectKV-shaped decode steps (40960-token prompts, Hq 32, Hkv 8, d 128, A0R0K8 per KV head on a proxy
     query = q + N(0, 0.3^2)) over a stack of layers, batch 1 and 8: routing (scores, top-K, view) and the step's
     append + proposal attention per layer, run in turn on one stream or with the next layer's routing on a second
@@ -267,14 +270,94 @@ def time_side_flow(steps: int, dev, layers_n: int = 8):
             e1.record()
             torch.cuda.synchronize()
             res[name] = e0.elapsed_time(e1) * 1e3 / n
+        # algorithmic bytes of one decode step over all layers: the summaries the routing scores (one fp32 summary
+        # per prompt page and KV head), the K and V of every token the proposal attends to, the step token written
+        by = [step_bytes(w, c, c.sel_ids, c.n_sel) for w, c in layers]
+        b_step = sum(b["score"] + b["propose"][0] + w.R * w.Hkv * w.d * 2 * 2 for b, (w, _) in zip(by, layers))
+        b_att = sum(b["propose"][0] for b in by)
+        t = res["side_flow"] * 1e-6
         out[f"batch{batch}"] = {"us_per_step_sequential": res["sequential"], "us_per_step_side_flow": res["side_flow"],
                                 "decode_steps_per_s": 1e6 / res["side_flow"],
-                                "speedup": res["sequential"] / res["side_flow"]}
+                                "speedup": res["sequential"] / res["side_flow"],
+                                "bytes_per_step": b_step, "attention_bytes_per_step": b_att,
+                                "gbs": b_step / t / 1e9, "pct_of_roofline": 100 * b_step / t / 1e9 / hbm_peak}
         del layers, flow
         torch.cuda.empty_cache()
     out["layers"] = layers_n
     out["workload"] = ("EarlySelectKV-shaped: 40960-token prompts, Hq 32, Hkv 8, d 128, A0R0K8 per KV head on a "
                        "proxy query; a step = routing + append + proposal attention per layer")
+    return out
+
+
+# ------------------------------------------------------------------------ EarlySelectKV 1024-step decode loop
+def time_decode_loop(dev, hbm_peak: float, steps: int = 1024, layers_n: int = 8, chunk: int = 128, reps: int = 2):
+    """EarlySelectKV decode over `steps` generated tokens (40960-token prompts, Hq 32, Hkv 8, d 128, A0R0K8 per KV
+    head on each step's own noisy proxy query), batch 1 and 8, over a stack of `layers_n` layers: every step routes
+    and then appends its token and attends, layer after layer, with the next layer's routing on a second stream
+    (SideFlowDecode over DecodeLoop). The loop is captured as CUDA graphs of `chunk` steps and timed whole.
+    Algorithmic bytes of step t per layer and request: the summaries the routing scores (N * Hkv * d * 4), the K
+    and V of the 8 selected pages and of the t + 1 generated tokens, and the step token written."""
+    import torch
+    import selected_kv_sparse_gb300 as kap
+    from workloads import make_workload
+    out = {}
+    for batch in (1, 8):
+        loops, ins = [], []
+        for l in range(layers_n):
+            w = make_workload("early", device=dev, batch=batch, seed_offset=400 + l, poison=False,
+                              k_prop_override=steps)
+            pool = kap.KVPool(w.K, w.V, w.Hq, torch.zeros(w.num_pages, w.Hkv, w.d, dtype=torch.float32, device=dev))
+            kap.kap_build_summaries(pool, kap.PageMap(w.block_table, w.ctx_len, w.seq_len0))
+            loops.append(kap.DecodeLoop(pool, w.block_table, w.ctx_len, w.seq_len0, steps,
+                                        kap.rope_inv_freq(w.d, w.theta, dev), policy_of(w)))
+            ins.append(w)
+        flow = kap.SideFlowDecode(loops)
+
+        def run(t0, t1):
+            for t in range(t0, t1):
+                flow.step([w.q_route_steps[t] for w in ins], [w.q_prop[t] for w in ins],
+                          [w.k_new_prop[t] for w in ins], [w.v_new_prop[t] for w in ins])
+                for lp in loops:
+                    lp.advance()
+        for lp in loops:
+            lp.reset()
+        run(0, steps)   # eager pass
+        torch.cuda.synchronize()
+        graphs = []
+        for lp in loops:
+            lp.reset()
+        for c0 in range(0, steps, chunk):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                run(c0, min(steps, c0 + chunk))
+            graphs.append(g)
+        for g in graphs:   # warm-up: one whole loop
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            for g in graphs:
+                g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / (reps * steps)
+        w = ins[0]
+        N = (int(w.ctx_len[0]) + PAGE - 1) // PAGE
+        kv_tok = w.d * 2 * 2
+        sel_tok = 8 * PAGE
+        per_req = sum(N * w.Hkv * w.d * 4 + (sel_tok + t + 1) * w.Hkv * kv_tok + w.Hkv * kv_tok for t in range(steps))
+        b = per_req * w.R * layers_n / steps     # average bytes of one decode step (all layers)
+        out[f"batch{batch}"] = {"us_per_step": us, "decode_steps_per_s": 1e6 / us, "tokens_per_s": 1e6 / us * w.R,
+                                "bytes_per_step": b, "gbs": b / (us * 1e-6) / 1e9,
+                                "pct_of_roofline": 100 * b / (us * 1e-6) / 1e9 / hbm_peak}
+        del loops, ins, flow, graphs
+        torch.cuda.empty_cache()
+    out.update(layers=layers_n, steps=steps, graph_chunk=chunk, reps=reps,
+               workload="EarlySelectKV-shaped decode: 40960-token prompts, Hq 32, Hkv 8, d 128, A0R0K8 per KV head "
+                        "re-routed every step on that step's proxy query (q + N(0, 0.3^2)), 1024 generated tokens "
+                        "appended one per step; a step = routing + append + attention on every layer, the next "
+                        "layer's routing on a second stream")
     return out
 
 
@@ -387,6 +470,92 @@ def time_accept(layers, steps: int, hbm_peak: float, dev):
             "window": f"carry + {w0.k_prop} proposals x {w0.R} requests, fp32 logits",
             "acceptance_rate": acc_rate, "l2": f"{len(calls)} distinct logit sets, "
                                               f"{len(calls) * b / 1e6:.0f} MB per replay"}
+
+
+# ------------------------------------------------------------------------------------ the other workloads
+def policy_of(w):
+    """Access policy of workload w: its A/R/K split (one for all requests, or one per request), per-KV-head or
+    shared selection, and the selection capacity."""
+    import selected_kv_sparse_gb300 as kap
+    a, r, k = (int(x) for x in w.ark[0].tolist())
+    same = bool((w.ark == w.ark[0]).all())
+    return kap.AccessPolicy(a, r, k, w.per_kv_head, w.sel_cap(), None if same else w.ark.contiguous())
+
+
+def time_workload(name: str, layers_n: int, steps: int, warmup: int, hbm_peak: float, dev, **kw):
+    """One decode cycle of workload `name` per layer (plan, every proposal step fused with its append, window
+    append, verification) over `layers_n` layer replicas, each phase one CUDA graph over the layers, timed with
+    CUDA events between replays. Returns per-launch times, algorithmic bytes, GB/s and the fraction of the HBM
+    roofline of the proposal and verification launches, the cycle time and the steps per second."""
+    import torch
+    import selected_kv_sparse_gb300 as kap
+    from workloads import make_workload
+    layers = []
+    for l in range(layers_n):
+        w = make_workload(name, device=dev, seed_offset=300 + l, poison=False, **kw)
+        pool = kap.KVPool(w.K, w.V, w.Hq, torch.zeros(w.num_pages, w.Hkv, w.d, dtype=torch.float32, device=dev))
+        kap.kap_build_summaries(pool, kap.PageMap(w.block_table, w.ctx_len, w.seq_len0))
+        pol = policy_of(w)
+        cyc = kap.DecodeCycle(pool, w.block_table, w.ctx_len, w.seq_len0, w.k_prop, w.n_q,
+                              kap.rope_inv_freq(w.d, w.theta, dev), policy=pol, spans=w.spans,
+                              span_offsets=w.span_offsets, sel_cap=pol.cap)
+        layers.append((w, cyc))
+    k_prop = layers[0][0].k_prop
+    phases = [("plan", lambda: [c.plan(w.q_route) for w, c in layers])]
+    for i in range(k_prop):
+        phases.append((f"prop{i}", lambda i=i: [c.propose_step(i, w.q_prop[i], w.k_new_prop[i], w.v_new_prop[i],
+                                                               settled=True) for w, c in layers]))
+    phases.append(("vapp", lambda: [c.append_window(w.q_ver, w.k_new_ver, w.v_new_ver) for w, c in layers]))
+    phases.append(("ver", lambda: [c.verify(w.q_ver) for w, c in layers]))
+    for _, fn in phases:
+        fn()
+    torch.cuda.synchronize()
+    graphs = []
+    for nm, fn in phases:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        graphs.append((nm, g))
+    for _ in range(warmup):
+        for _, g in graphs:
+            g.replay()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(graphs) + 1)] for _ in range(steps)]
+    for s_ in range(steps):
+        evs[s_][0].record()
+        for j, (_, g) in enumerate(graphs):
+            g.replay()
+            evs[s_][j + 1].record()
+    torch.cuda.synchronize()
+    ph = {nm: sum(evs[s_][j].elapsed_time(evs[s_][j + 1]) for s_ in range(steps)) / steps
+          for j, (nm, _) in enumerate(graphs)}
+    by = [step_bytes(w, c, c.sel_ids, c.n_sel) for w, c in layers]
+    L = layers_n
+    b_prop = sum(sum(b["propose"]) for b in by) / (k_prop * L)
+    b_ver = sum(b["verify"] for b in by) / L
+    b_score = sum(b["score"] for b in by) / L
+    t_prop = sum(ph[f"prop{i}"] for i in range(k_prop)) / (k_prop * L) * 1e-3   # s per launch
+    t_ver = ph["ver"] / L * 1e-3
+    t_cycle = sum(ph.values()) / L * 1e-3
+    b_cycle = sum(b["score"] + sum(b["propose"]) + b["verify"] + b["append"] for b in by) / L
+    w0 = layers[0][0]
+    s_frac = [float(b["propose"][0]) for b in by]
+    out = {
+        "layers": L, "requests": w0.R, "proposal_steps_per_cycle": k_prop,
+        "propose": {"us_per_launch": t_prop * 1e6, "bytes_per_launch": b_prop, "gbs": b_prop / t_prop / 1e9,
+                    "pct_of_roofline": 100 * b_prop / t_prop / 1e9 / hbm_peak, "steps_per_s": 1.0 / t_prop},
+        "verify": {"us_per_launch": t_ver * 1e6, "bytes_per_launch": b_ver, "gbs": b_ver / t_ver / 1e9,
+                   "pct_of_roofline": 100 * b_ver / t_ver / 1e9 / hbm_peak, "steps_per_s": 1.0 / t_ver},
+        "plan_us_per_layer": ph["plan"] / L * 1e3, "score_bytes_per_layer": b_score,
+        "window_append_us_per_layer": ph["vapp"] / L * 1e3,
+        "cycle": {"us_per_layer": t_cycle * 1e6, "bytes_per_layer": b_cycle, "gbs": b_cycle / t_cycle / 1e9,
+                  "pct_of_roofline": 100 * b_cycle / t_cycle / 1e9 / hbm_peak, "cycles_per_s": 1.0 / t_cycle},
+        "selected_fraction": b_prop / max(1.0, b_ver),
+        "steps": steps, "warmup": warmup,
+    }
+    del layers, graphs, phases, by, s_frac
+    torch.cuda.empty_cache()
+    return out
 
 
 # ------------------------------------------------------------------------------------------------ arenas
@@ -691,7 +860,21 @@ def run_kap(args, world, rank, local):
     prior = None if args.no_prior else time_prior(layers, K, hbm_peak, dev)
     accept = None if args.no_accept else time_accept(layers, K, hbm_peak, dev)
     mat = None if args.no_materialize else time_materialize(layers, K, hbm_peak, dev)
-    side = None if args.no_side_flow else time_side_flow(K, dev)
+    side = None if args.no_side_flow else time_side_flow(K, dev, hbm_peak)
+    loop = None if args.no_decode_loop else time_decode_loop(dev, hbm_peak)
+    other = None
+    if not args.no_configs:
+        nst = max(3, min(K, 20))
+        other = {
+            "long": dict(time_workload("long", 8, nst, 3, hbm_peak, dev),
+                         workload="GraphSpec-like long context: 1 request x 131072 tokens (8192 pages), Hq 40, Hkv 8, "
+                                  "d 128, 451-page evidence-span view (s = 5.5%) shared by the KV heads, 8 proposal "
+                                  "steps + verify window 8 per cycle, 8 layer replicas"),
+            "mixed": dict(time_workload("mixed", 1, nst, 3, hbm_peak, dev),
+                          workload="mixed serving batch: 32 requests, prompts log-uniform in 4K-128K tokens, s in "
+                                   "{2, 5.5, 10, 25}%, splits A1R2/A4R4/A0R0, 1 proposal launch for all requests + 1 "
+                                   "verify launch with windows {2, 4, 8}, shared 2^20-page pool (64 GiB)"),
+        }
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -738,6 +921,8 @@ def run_kap(args, world, rank, local):
             "accept_commit": accept,
             "materialize": mat,
             "early_side_flow": side,
+            "early_decode_loop": loop,
+            "workloads": other,
             "phase_ms_per_step": {k2: v / K for k2, v in phase_ms.items()},
             "roofline": {"bound": "hbm", "kernel": "verify_tc_kernel", "achieved": ver_gbs, "peak": hbm_peak,
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": ver_gbs / hbm_peak, "traffic": traffic},
