@@ -470,29 +470,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int b = u & 1;
       if (!mbar_wait(&ofull[b], (u >> 1) & 1, p.err)) return false;
       tc_fence_after();
-      float ot[NPMAX];
+      // 16 columns at a time, so that only one chunk of the tile is held in registers beside the running output
 #pragma unroll
-      for (int c = 0; c < NPMAX / 16; ++c)
-        if (c * 16 < npad_u) tmem_ld16(tmem + 2 * NPMAX + b * NPMAX + lane_base + c * 16, ot + c * 16);
-      tmem_wait_ld();
+      for (int c = 0; c < NPMAX / 16; ++c) {
+        if (c * 16 < npad_u) {
+          float ot[16];
+          tmem_ld16(tmem + 2 * NPMAX + b * NPMAX + lane_base + c * 16, ot);
+          tmem_wait_ld();
+          if (resc_u) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) oreg[c * 16 + e] = fmaf(oreg[c * 16 + e], alpha_s[b * NPMAX + c * 16 + e], ot[e]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) oreg[c * 16 + e] += ot[e];
+          }
+        }
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ofree[b]);
-      if (resc_u) {
-#pragma unroll
-        for (int n = 0; n < NPMAX; ++n)
-          if (n < npad_u) oreg[n] = fmaf(oreg[n], alpha_s[b * NPMAX + n], ot[n]);
-      } else {
-#pragma unroll
-        for (int n = 0; n < NPMAX; ++n)
-          if (n < npad_u) oreg[n] += ot[n];
-      }
       return true;
     };
     // Last arriver of a row: merges the partial records of CTAs b_first..b_last and writes the row's output.
     // Thread t owns 16 consecutive head dims of one query column (8 threads per column, 16 columns at a time); for
-    // every chunk of 8 contributors it issues all its loads (the (m, l) pair and four 16-byte pieces of the
-    // partial output per contributor) before using any, so a chunk costs one round trip and no barrier.
+    // every chunk of kMergeChunkV contributors it issues all its loads (the (m, l) pair and four 16-byte pieces of
+    // the partial output per contributor) before using any, so a chunk costs one round trip and no barrier. Wide
+    // tiles take fewer contributors per chunk: their running state already holds most of the registers.
+    constexpr int kMergeChunkV = NPMAX <= 16 ? 8 : 4;
     auto merge_row = [&](int row, int b_first, int b_last, int qoff, int nreal) {
       const int h = row - (row / p.hkv) * p.hkv;
       __nv_bfloat16 *outp = static_cast<__nv_bfloat16 *>(p.out);
@@ -505,11 +509,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e) acc[e] = 0.0f;
         float M = -INFINITY, Ls = 0.0f;
-        for (int b0 = 0; b0 < nc; b0 += 8) {
-          float2 ml[8];
-          float4 pv[8][4];
+        for (int b0 = 0; b0 < nc; b0 += kMergeChunkV) {
+          float2 ml[kMergeChunkV];
+          float4 pv[kMergeChunkV][4];
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
+          for (int c = 0; c < kMergeChunkV; ++c) {
             const size_t sl = static_cast<size_t>(b_first + min(b0 + c, nc - 1) + row);
             ml[c] = __ldcg(reinterpret_cast<const float2 *>(p.ml) + sl * p.npad_ws + nn);
             const float4 *pp = reinterpret_cast<const float4 *>(p.part + (sl * p.npad_ws + nn) * 128 + d0);
@@ -518,7 +522,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           float Mc = M;
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
+          for (int c = 0; c < kMergeChunkV; ++c)
             if (b0 + c < nc) Mc = fmaxf(Mc, ml[c].x);
           if (Mc == -INFINITY) continue;
           const float rs = (M == -INFINITY) ? 0.0f : exp2f(M - Mc);
@@ -526,7 +530,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int e = 0; e < 16; ++e) acc[e] *= rs;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
+          for (int c = 0; c < kMergeChunkV; ++c) {
             if (b0 + c >= nc || ml[c].x == -INFINITY) continue;
             const float w = exp2f(ml[c].x - Mc);
             Ls = fmaf(ml[c].y, w, Ls);
@@ -626,7 +630,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&sfree[b]);
       const int pos = m.tile * kTileTok + tid;
-      float mr[NPMAX];
+      // the running maxima are read from shared memory at each use (not held in registers beside x, lt and oreg)
+      const volatile float *mrv = m_run;
       bool over = false;
       // column n is window row n / G: visible when this token's position is at most qpos0 + n / G
       const int rel = pos - qpos0;  // the token is visible to window rows i >= rel
@@ -635,8 +640,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int n = 0; n < NPMAX; ++n) {
         const bool vis = n < nreal && n >= n_first;
         x[n] = vis ? x[n] * scale2 : -INFINITY;
-        mr[n] = m_run[n];
-        over |= x[n] > mr[n] + kRescaleThreshold;
+        over |= x[n] > mrv[n] + kRescaleThreshold;
       }
       // ---- running max: only when some logit of this tile exceeds it by more than 2^8
       const bool rescale = named_or_128(over);
@@ -656,8 +660,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           m_run[tid] = mn;
         }
         named_sync_128();
-#pragma unroll
-        for (int n = 0; n < NPMAX; ++n) mr[n] = m_run[n];
       }
       // ---- P = exp2(x - m_run) as bf16, K-major with 128-byte swizzle (row n, column = token)
       {
@@ -665,7 +667,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int katom = tid >> 6, c = (tid & 63) >> 3, e = tid & 7;
 #pragma unroll
         for (int n = 0; n < NPMAX; ++n) {
-          const float pv = (x[n] == -INFINITY) ? 0.0f : fast_exp2(x[n] - mr[n]);
+          const float pv = (x[n] == -INFINITY) ? 0.0f : fast_exp2(x[n] - mrv[n]);
           lt[n] = rescale ? fmaf(lt[n], alpha_s[b * NPMAX + n], pv) : lt[n] + pv;
           *reinterpret_cast<__nv_bfloat16 *>(pd + katom * L::KATOM + (n >> 3) * 1024 + (n & 7) * 128 +
                                             ((c ^ (n & 7)) << 4) + e * 2) = __float2bfloat16_rn(pv);
