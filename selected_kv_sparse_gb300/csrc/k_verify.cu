@@ -93,8 +93,8 @@ struct TcSmem {
   static constexpr int OFF_Q = OFF_V + kStages * kStageBytes;     // Q[2] (segment parity)
   static constexpr int OFF_P = OFF_Q + 2 * 2 * KATOM;              // P[2] (tile parity)
   static constexpr int OFF_CM = OFF_P + 2 * 2 * KATOM;             // column maxima [4][NPMAX]
-  static constexpr int OFF_ST = OFF_CM + 4 * NPMAX * 4;            // m_run, lsum, alpha[2] : [4][NPMAX]
-  static constexpr int OFF_FLAG = OFF_ST + 4 * NPMAX * 4;          // rescale flag per tile parity [2]
+  static constexpr int OFF_ST = OFF_CM + 4 * NPMAX * 4;            // m_run, lsum, alpha[2], m_sub : [5][NPMAX]
+  static constexpr int OFF_FLAG = OFF_ST + 5 * NPMAX * 4;          // rescale flag per tile parity [2]
   static constexpr int OFF_BAR = OFF_FLAG + 16;
   static constexpr int kMetaRing = 2 * kStages;  // tile metadata outlives its K stage (read until MMA2 and softmax)
   // kfull, vfull, kempty, vempty [kStages]; sfull, sfree, pfull, ofull, ofree, qfull, qempty [2];
@@ -105,6 +105,7 @@ struct TcSmem {
   static constexpr int BYTES = OFF_TMEM + 16;
   static constexpr int ALLOC = BYTES + 1024;  // room to align the base to 1024 bytes
   static constexpr int TMEM_COLS = (4 * NPMAX <= 32) ? 32 : (4 * NPMAX <= 64 ? 64 : (4 * NPMAX <= 128 ? 128 : 256));
+  static_assert(ALLOC <= 227 * 1024, "shared memory per CTA");
 };
 
 // 2^x with the hardware approximation (relative error about 2^-22; the result is rounded to bf16 for P anyway).
@@ -115,6 +116,19 @@ __device__ __forceinline__ float fast_exp2(float x) {
 }
 
 __device__ __forceinline__ void named_sync_128() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// 16 consecutive floats from shared memory (16-byte aligned) in four 16-byte loads, ordered after earlier barriers
+__device__ __forceinline__ void load16_shared(const float *src, float *v) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    float4 f;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(f.x), "=f"(f.y), "=f"(f.z), "=f"(f.w)
+                 : "r"(smem_u32(src + 4 * q)) : "memory");
+    v[4 * q] = f.x;
+    v[4 * q + 1] = f.y;
+    v[4 * q + 2] = f.z;
+    v[4 * q + 3] = f.w;
+  }
+}
 __device__ __forceinline__ bool named_or_128(bool v) {
   uint32_t r;
   asm volatile(
@@ -145,6 +159,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   float *m_run = reinterpret_cast<float *>(sm + L::OFF_ST);
   float *lsum = m_run + NPMAX;
   float *alpha_s = lsum + NPMAX;  // [2][NPMAX]
+  // the running maxima as subtracted from the logits: m_run, or 0 while a column has seen no visible token (its
+  // logits are then all -inf, and -inf - 0 gives the weight 0 where -inf - m_run would give NaN)
+  float *m_sub = alpha_s + 2 * NPMAX;
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
   constexpr int kMR = L::kMetaRing;
   uint64_t *kfull = bars, *vfull = bars + kStages, *kempty = bars + 2 * kStages, *vempty = bars + 3 * kStages;
@@ -606,6 +623,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (m.first) {
         if (tid < NPMAX) {
           m_run[tid] = -INFINITY;
+          m_sub[tid] = 0.0f;
           lsum[tid] = 0.0f;
         }
 #pragma unroll
@@ -624,23 +642,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       float x[NPMAX];
 #pragma unroll
       for (int c = 0; c < NPMAX / 16; ++c)
-        if (c * 16 < npad) tmem_ld16(tmem + b * NPMAX + lane_base + c * 16, x + c * 16);
+        if (c * 16 < npad) {
+          tmem_ld16(tmem + b * NPMAX + lane_base + c * 16, x + c * 16);
+        } else {  // columns past this row's padded width: no logits, weight 0
+#pragma unroll
+          for (int e = 0; e < 16; ++e) x[c * 16 + e] = -INFINITY;
+        }
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sfree[b]);
       const int pos = m.tile * kTileTok + tid;
-      // the running maxima are read from shared memory at each use (not held in registers beside x, lt and oreg)
-      const volatile float *mrv = m_run;
+      // the running maxima are read from shared memory 16 columns at a time (not all held in registers beside x,
+      // lt and oreg)
       bool over = false;
       // column n is window row n / G: visible when this token's position is at most qpos0 + n / G
       const int rel = pos - qpos0;  // the token is visible to window rows i >= rel
       const int n_first = rel <= 0 ? 0 : rel * G;
+      // Columns past nreal (padding) need no mask: their query rows are zero and their outputs are never written.
+      // Only a tile that reaches the window has masked entries; a warp without any scales its logits only.
+      if (__all_sync(0xffffffffu, n_first == 0)) {
 #pragma unroll
-      for (int n = 0; n < NPMAX; ++n) {
-        const bool vis = n < nreal && n >= n_first;
-        x[n] = vis ? x[n] * scale2 : -INFINITY;
-        over |= x[n] > mrv[n] + kRescaleThreshold;
+        for (int n = 0; n < NPMAX; ++n) x[n] *= scale2;
+      } else {
+#pragma unroll
+        for (int n = 0; n < NPMAX; ++n) x[n] = (n >= n_first) ? x[n] * scale2 : -INFINITY;
+      }
+#pragma unroll
+      for (int c = 0; c < NPMAX / 16; ++c) {
+        float mr[16];
+        load16_shared(m_run + c * 16, mr);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) over |= x[c * 16 + e] > mr[e] + kRescaleThreshold;
       }
       // ---- running max: only when some logit of this tile exceeds it by more than 2^8
       const bool rescale = named_or_128(over);
@@ -658,19 +691,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const float mn = fmaxf(mo, cm);
           alpha_s[b * NPMAX + tid] = (mn == -INFINITY) ? 1.0f : exp2f(mo - mn);
           m_run[tid] = mn;
+          m_sub[tid] = (mn == -INFINITY) ? 0.0f : mn;
         }
         named_sync_128();
+        // this thread's running sums follow the raised maxima (the tile's weights are added below)
+#pragma unroll
+        for (int cc = 0; cc < NPMAX / 16; ++cc) {
+          float al[16];
+          load16_shared(alpha_s + b * NPMAX + cc * 16, al);
+#pragma unroll
+          for (int ee = 0; ee < 16; ++ee) lt[cc * 16 + ee] *= al[ee];
+        }
       }
-      // ---- P = exp2(x - m_run) as bf16, K-major with 128-byte swizzle (row n, column = token)
+      // ---- P = exp2(x - m_run) as bf16, K-major with 128-byte swizzle (row n, column = token); a masked logit
+      // (-inf) gives 0 since m_sub is finite
       {
         unsigned char *pd = Ps + b * 2 * L::KATOM;
         const int katom = tid >> 6, c = (tid & 63) >> 3, e = tid & 7;
 #pragma unroll
-        for (int n = 0; n < NPMAX; ++n) {
-          const float pv = (x[n] == -INFINITY) ? 0.0f : fast_exp2(x[n] - mrv[n]);
-          lt[n] = rescale ? fmaf(lt[n], alpha_s[b * NPMAX + n], pv) : lt[n] + pv;
-          *reinterpret_cast<__nv_bfloat16 *>(pd + katom * L::KATOM + (n >> 3) * 1024 + (n & 7) * 128 +
-                                            ((c ^ (n & 7)) << 4) + e * 2) = __float2bfloat16_rn(pv);
+        for (int cc = 0; cc < NPMAX / 16; ++cc) {
+          float mr[16];
+          load16_shared(m_sub + cc * 16, mr);
+#pragma unroll
+          for (int ee = 0; ee < 16; ++ee) {
+            const int n = cc * 16 + ee;
+            const float pv = fast_exp2(x[n] - mr[ee]);
+            lt[n] += pv;
+            *reinterpret_cast<__nv_bfloat16 *>(pd + katom * L::KATOM + (n >> 3) * 1024 + (n & 7) * 128 +
+                                              ((c ^ (n & 7)) << 4) + e * 2) = __float2bfloat16_rn(pv);
+          }
         }
       }
       // tokens past the last query position carry no weight; their V rows may hold anything (even NaN) and must
