@@ -330,6 +330,14 @@ kap_status kap_attn_propose_noalloc(const kap_kv_pool *pool, const kap_page_map 
                                     const void *q_dev, void *out, float *lse, kap_stream stream);
 size_t kap_noalloc_scratch_bytes(void);
 
+/* Check of the bounded waits. Every wait of a kernel on an mbarrier (a copy landing, a slot freed, an MMA done)
+ * gives up after at most about a second, sets bit 8 of the device error word and lets the kernel return, so that a
+ * lost arrival cannot hang the GPU. This call runs the same bounded wait, on a barrier that nothing completes and
+ * with nothing in flight, for `polls` polls of at most `suspend_ns` each (1 <= polls <= 1024,
+ * 1 <= suspend_ns <= 2^20), and writes 1 to *timed_out_dev (device int32) when the wait gave up, 0 otherwise. The
+ * pages have no counterpart: this is a diagnostic of the library. KAP_EINVAL for out-of-range arguments. */
+kap_status kap_selftest_wait_timeout(uint32_t polls, uint32_t suspend_ns, int32_t *timed_out_dev, kap_stream stream);
+
 /* Diagnostics. */
 const char *kap_status_str(kap_status s);
 const char *kap_last_cuda_error(void);   /* text of the last CUDA error seen by this thread, "" if none */

@@ -13,5 +13,5 @@ from ._binding import (  # noqa: F401
 )
 from ._binding import kap_append_propose, kap_attn_propose_noalloc, kap_noalloc_scratch_bytes  # noqa: F401
 from ._binding import kap_accept_commit, kap_accept_workspace_size, kap_materialize_view, kap_prior_topk  # noqa: F401
-from ._binding import kap_refresh_summaries, kap_score_topk_view  # noqa: F401
+from ._binding import kap_refresh_summaries, kap_score_topk_view, kap_selftest_wait_timeout  # noqa: F401
 from .pipeline import DecodeCycle, DecodeLoop, SideFlowDecode  # noqa: F401

@@ -89,6 +89,7 @@ def _declare(lib):
         "kap_attn_propose_noalloc": ([P, P, P, P, P, P, P], I),
         "kap_noalloc_scratch_bytes": ([], Z),
         "kap_rope_inv_freq": ([I, ctypes.c_double, P], I),
+        "kap_selftest_wait_timeout": ([ctypes.c_uint32, ctypes.c_uint32, P, P], I),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -464,6 +465,15 @@ def kap_attn_verify(pool: KVPool, pmap: PageMap, vp: VerifyPolicy, q: torch.Tens
     _check("kap_attn_verify", lib.kap_attn_verify(ctypes.byref(p), ctypes.byref(m), ctypes.byref(v), _ptr(q),
                                                   _ptr(out), _ptr(lse), _ptr(workspace),
                                                   workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def kap_selftest_wait_timeout(polls: int, suspend_ns: int, timed_out: torch.Tensor, stream=None):
+    """Runs the library's bounded mbarrier wait on a barrier that nothing completes (see kap.h); timed_out is a
+    one-element int32 CUDA tensor that receives 1 when the wait gave up."""
+    if timed_out.dtype != torch.int32 or not timed_out.is_cuda or timed_out.numel() < 1:
+        raise ValueError("timed_out must be an int32 CUDA tensor")
+    _check("kap_selftest_wait_timeout",
+           load().kap_selftest_wait_timeout(int(polls), int(suspend_ns), _ptr(timed_out), _stream(stream)))
 
 
 def kap_device_error() -> int:

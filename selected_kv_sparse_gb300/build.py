@@ -17,7 +17,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 OUT = os.path.join(HERE, "libkap.so")
 BUILD_DIR = os.path.join(HERE, "_build")
 SOURCES = ["kap_api.cu", "k_select.cu", "k_append.cu", "k_propose.cu", "k_verify.cu", "k_accept.cu",
-           "k_materialize.cu", "kap_noalloc.cu"]
+           "k_materialize.cu", "kap_noalloc.cu", "k_selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -411,6 +411,13 @@ kap_status kap_rope_inv_freq(int32_t head_dim, double theta, float *inv_freq_hos
 
 const char *kap_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
 
+kap_status kap_selftest_wait_timeout(uint32_t polls, uint32_t suspend_ns, int32_t *timed_out_dev, kap_stream stream) {
+  if (!timed_out_dev || polls == 0 || polls > 1024u || suspend_ns == 0 || suspend_ns > (1u << 20)) return KAP_EINVAL;
+  int *err = error_word();
+  if (!err) return KAP_ECUDA;
+  return cuda_status(launch_wait_probe(polls, suspend_ns, err, timed_out_dev, cs(stream)));
+}
+
 kap_status kap_device_error(int32_t *code_out) {
   if (!code_out) return KAP_EINVAL;
   int v = 0;

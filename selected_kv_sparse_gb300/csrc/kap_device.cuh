@@ -157,18 +157,18 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-// A waiting thread is suspended in hardware until the phase completes (it is woken at once) or kSuspendNs pass,
-// so a wait costs a few instructions per kSuspendNs instead of a busy loop that takes issue slots from the warps
+// A waiting thread is suspended in hardware until the phase completes (it is woken at once) or suspend_ns pass,
+// so a wait costs a few instructions per suspension instead of a busy loop that takes issue slots from the warps
 // doing the work.
 constexpr uint32_t kSuspendNs = 1u << 20;  // about 1 ms
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity, uint32_t suspend_ns = kSuspendNs) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(suspend_ns)
       : "memory");
   return ok != 0;
 }
@@ -191,11 +191,15 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
 constexpr uint32_t kWaitPolls = 1u << 10;
 // Bound on the polls of a loop that tests barriers without suspending (the verification MMA issuer).
 constexpr uint32_t kSpinPolls = 1u << 26;
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err) {
-  for (uint32_t i = 0; i < kWaitPolls; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, int *err, uint32_t polls,
+                                                  uint32_t suspend_ns) {
+  for (uint32_t i = 0; i < polls; ++i)
+    if (mbar_try_wait(bar, parity, suspend_ns)) return true;
   set_error(err, kErrTimeout);
   return false;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err) {
+  return mbar_wait_bounded(bar, parity, err, kWaitPolls, kSuspendNs);
 }
 
 // ------------------------------------------------------------------------------------------ bulk copies

@@ -90,6 +90,9 @@ cudaError_t launch_verify(const PoolArgs &p, const MapArgs &m, int max_q, int to
 // number of SMs of the current device (cached per device)
 int device_sm_count();
 
+// bounded-wait check (k_selftest.cu): one bounded mbarrier wait that nothing completes
+cudaError_t launch_wait_probe(uint32_t polls, uint32_t suspend_ns, int *err, int32_t *timed_out, cudaStream_t s);
+
 // Records the text of a failed CUDA call for kap_last_cuda_error (this thread) and returns true when e is an error.
 bool record_cuda_error(cudaError_t e);
 

@@ -107,3 +107,13 @@ def test_refresh_checks_its_arguments(abi):
     bad.k_summary = None
     assert lib.kap_refresh_summaries(_ref(bad), P, P, 3, None) == KAP_EINVAL            # pool without summaries
     assert lib.kap_refresh_summaries(_ref(_pool(b, d=96)), P, P, 3, None) == KAP_EUNSUPPORTED
+
+
+def test_wait_check_rejects_out_of_range_limits(abi):
+    b, lib = abi
+    P = ctypes.c_void_p(ADDR)
+    assert lib.kap_selftest_wait_timeout(0, 1000, P, None) == KAP_EINVAL          # no poll
+    assert lib.kap_selftest_wait_timeout(1025, 1000, P, None) == KAP_EINVAL       # more polls than a kernel's wait
+    assert lib.kap_selftest_wait_timeout(8, 0, P, None) == KAP_EINVAL             # no suspension
+    assert lib.kap_selftest_wait_timeout(8, (1 << 20) + 1, P, None) == KAP_EINVAL  # longer than a kernel's poll
+    assert lib.kap_selftest_wait_timeout(8, 1000, None, None) == KAP_EINVAL       # nowhere to report
