@@ -889,9 +889,20 @@ def run_kap(args, world, rank, local):
             dt += t_
             b += b_
             n_cyc += 1
+        # the same cycles on one thread (the oracle's attention is parallel over (row, head) units)
+        dt1 = b1 = 0.0
+        n1 = 0
+        while dt1 < 6.0:
+            t_, b_ = oracle_sample(w_cpu, 1, r=n1 % w_cpu.R)
+            dt1 += t_
+            b1 += b_
+            n1 += 1
         cpu = {"value": b / dt / 1e9, "unit": "GB/s", "cores": nth, "kind": "oracle",
                "sample": f"{n_cyc} full cycles, each one request of one layer (summaries, fixed-order scores, "
-                         f"A1R2K125 top-K, 4 proposals, verify window 4) in fp64: {dt:.1f} s"}
+                         f"A1R2K125 top-K, 4 proposals, verify window 4) in fp64: {dt:.1f} s",
+               "single_thread": {"value": b1 / dt1 / 1e9, "unit": "GB/s", "cores": 1,
+                                 "sample": f"{n1} of the same cycles on one thread: {dt1:.1f} s"},
+               "ms_per_request_layer_cycle": {"all_cores": dt / n_cyc * 1e3, "one_thread": dt1 / n1 * 1e3}}
 
     dev_err = kap.kap_device_error()   # nonzero: a kernel met a bad page, length or timed-out wait
     if rank == 0:
