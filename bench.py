@@ -622,7 +622,9 @@ def recorded_traffic(kernel: str):
 
 # ------------------------------------------------------------------------------------------------ oracle arm
 def oracle_sample(w_cpu, nthreads: int, r: int = 0):
-    """Runs the oracle on one request of one layer for one full cycle; returns (seconds, algorithmic bytes)."""
+    """Runs the oracle on one request of one layer for one full cycle of workload w_cpu (summaries, scores and A/R/K
+    top-K per KV head or shared, or span selection; every proposal step; the verify window); returns (seconds,
+    algorithmic bytes)."""
     import numpy as np
     import oracle
     bt = w_cpu.block_table.numpy()
@@ -636,18 +638,22 @@ def oracle_sample(w_cpu, nthreads: int, r: int = 0):
     lctx, lseq = ctx[r:r + 1], seq0[r:r + 1]
     qr = w_cpu.q_route[r:r + 1].float().numpy()
     a, rr, k = (int(x) for x in w_cpu.ark[r].tolist())
+    N = (int(lctx[0]) + PAGE - 1) // PAGE
+    rows = w_cpu.Hkv if w_cpu.per_kv_head else 1
     t0 = time.perf_counter()
     S = oracle.build_summaries(K, lbt, lctx)
-    sc, _ = oracle.scores(qr, S, lbt, lctx, per_head=True)
-    N = (int(lctx[0]) + PAGE - 1) // PAGE
-    sels = [oracle.topk_ark(sc[0, h], N, a, rr, k) for h in range(w_cpu.Hkv)]
-    cap = max(len(s) for s in sels)
-    sel = np.zeros((1, w_cpu.Hkv, cap), np.int32)
-    nsel = np.zeros((1, w_cpu.Hkv), np.int32)
-    for h, s in enumerate(sels):
-        sel[0, h, :len(s)] = s
-        nsel[0, h] = len(s)
-    prop_bytes = 0
+    if w_cpu.spans is not None:
+        so = w_cpu.span_offsets.numpy()
+        sels = [oracle.select_spans(N, w_cpu.spans.numpy()[so[r]:so[r + 1]], a, rr)]
+    else:
+        sc, _ = oracle.scores(qr, S, lbt, lctx, per_head=w_cpu.per_kv_head)
+        sels = [oracle.topk_ark(sc[0, v], N, a, rr, k) for v in range(rows)]
+    cap = max(len(x) for x in sels)
+    sel = np.zeros((1, rows, cap), np.int32)
+    nsel = np.zeros((1, rows), np.int32)
+    for v, x in enumerate(sels):
+        sel[0, v, :len(x)] = x
+        nsel[0, v] = len(x)
     for i in range(w_cpu.k_prop):
         q = w_cpu.q_prop[i, r:r + 1].float().numpy()
         oracle.attn_propose(q, K, V, lbt, lctx, lseq + i + 1, sel, nsel, nthreads=nthreads)
@@ -656,13 +662,35 @@ def oracle_sample(w_cpu, nthreads: int, r: int = 0):
     oracle.attn_verify(qv, K, V, lbt, np.array([0, nq], np.int32), lseq, nthreads=nthreads)
     dt = time.perf_counter() - t0
     kv_tok = w_cpu.d * 2 * 2
+    prop_bytes = 0
     for i in range(w_cpu.k_prop):
         for h in range(w_cpu.Hkv):
-            p = sel[0, h, :nsel[0, h]].astype(np.int64)
+            v = 0 if rows == 1 else h
+            p = sel[0, v, :nsel[0, v]].astype(np.int64)
             prop_bytes += int((np.minimum(PAGE, int(lctx[0]) - PAGE * p).clip(min=0).sum() + i + 1) * kv_tok)
     ver_bytes = (int(lseq[0]) + nq) * w_cpu.Hkv * kv_tok
-    score_bytes = N * w_cpu.Hkv * w_cpu.d * 4
+    score_bytes = N * w_cpu.Hkv * w_cpu.d * 4 if w_cpu.spans is None else 0
     return dt, prop_bytes + ver_bytes + score_bytes
+
+
+def oracle_workloads(nthreads: int, budget_s: float = 3.0):
+    """The oracle's time for one request-cycle of the long-context, EarlySelectKV (batch 1, one step) and mixed
+    workloads at their stated sizes, each repeated over requests until `budget_s` seconds are spent."""
+    from workloads import make_workload
+    out = {}
+    # the mixed batch's requests are timed on a batch of 4 drawn the same way, in a pool of just their pages
+    for name, kw in (("long", {}), ("early", dict(batch=1)), ("mixed", dict(batch=4, pool_min_override=0))):
+        w = make_workload(name, device="cpu", poison=False, **kw)
+        dt = b = 0.0
+        n = 0
+        while dt < budget_s:
+            t_, b_ = oracle_sample(w, nthreads, r=n % w.R)
+            dt += t_
+            b += b_
+            n += 1
+        out[name] = {"ms_per_request_cycle": dt / n * 1e3, "gbs": b / dt / 1e9, "cycles": n, "cores": nthreads}
+        del w
+    return out
 
 
 def run_reference(args, world, rank):
@@ -897,7 +925,9 @@ def run_kap(args, world, rank, local):
             dt1 += t_
             b1 += b_
             n1 += 1
+        per_workload = oracle_workloads(nth)
         cpu = {"value": b / dt / 1e9, "unit": "GB/s", "cores": nth, "kind": "oracle",
+               "other_workloads": per_workload,
                "sample": f"{n_cyc} full cycles, each one request of one layer (summaries, fixed-order scores, "
                          f"A1R2K125 top-K, 4 proposals, verify window 4) in fp64: {dt:.1f} s",
                "single_thread": {"value": b1 / dt1 / 1e9, "unit": "GB/s", "cores": 1,

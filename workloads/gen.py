@@ -130,10 +130,11 @@ def _spans_long(g_cpu, n_pages: int, n_spans: int = 30, total: int = 446, lo: in
 
 def make_workload(name: str, device="cpu", scale: float = 1.0, ragged: bool = False, seed_offset: int = 0,
                   batch: Optional[int] = None, poison: bool = True, n_q_override: Optional[int] = None,
-                  k_prop_override: Optional[int] = None) -> Workload:
+                  k_prop_override: Optional[int] = None, pool_min_override: Optional[int] = None) -> Workload:
     """Builds one seeded workload on `device`.
 
     scale < 1 shortens every prompt (never below 64 tokens) and, for `mixed`, the batch, keeping the structure.
+    pool_min_override replaces the workload's minimum pool size (0: only the pages the requests use).
     ragged=True makes prompt lengths not page-aligned. poison=True fills every slot that holds no token with NaN,
     so that reading an invisible slot shows up in the output. seed_offset selects an independent replica (a
     different layer of the same model).
@@ -210,6 +211,8 @@ def make_workload(name: str, device="cpu", scale: float = 1.0, ragged: bool = Fa
         raise ValueError(f"unknown workload {name!r}")
     if n_q_override is not None:
         n_q = [n_q_override] * R
+    if pool_min_override is not None:
+        pool_min = pool_min_override
     if k_prop_override is not None:
         k_prop = k_prop_override
 
