@@ -38,6 +38,8 @@ constexpr int kMaxRowsScan = 256;            // rows whose entry offsets are sca
 constexpr int kBarSeg0 = 1;                  // named barriers kBarSeg0 .. kBarSeg0 + NSEG - 1, one per segment
 constexpr int kMergeChunk = 8;               // partial records loaded at once by a merging CTA
 constexpr int kPrefetchAhead = 32;           // entries beyond the ring prefetched into L2 per window
+constexpr int kShortEntries = 64;            // entries per CTA up to which a launch leaves spare SMs
+constexpr int kSpareDiv = 19;                // ... 1/kSpareDiv of its grid (8 of 152 SMs)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;    // log2 units
@@ -89,11 +91,10 @@ struct Cfg {
   // shared memory carve-up (bytes)
   static constexpr int COMB = NCW * REC * 4;              // per-warp state records
   static constexpr int WLOG = NCW * G * kPage * 8;        // per-warp logits, or probability pairs, of one page
-  static constexpr int SWT = NSEG * G * (NCW + 2) * 4;    // per segment: warp weights, max and sum per head
   static constexpr int SEGB = NSEG * 48;                  // segment table
   static constexpr int QPREP = NSEG * QPB;                // per-segment query and step token
   static constexpr int ROWB = (kMaxRowsScan + 1) * 4;     // per-row entry offsets (row scan)
-  static constexpr int FIXED = COMB + WLOG + SWT + SEGB + QPREP + ROWB + 256;
+  static constexpr int FIXED = COMB + WLOG + SEGB + QPREP + ROWB + 256;
   static constexpr int SLOT = 2 * CHUNK;                  // K and V of one entry
   // per CTA: 227 KB alone on an SM, else its share of the SM's 228 KB less the 1 KB each CTA reserves
   static constexpr int BUDGET = MINB == 1 ? 226 * 1024 : (228 / MINB - 2) * 1024;
@@ -105,8 +106,7 @@ struct Cfg {
   static constexpr int OFF_KV = 0;
   static constexpr int OFF_COMB = OFF_KV + SLOTS * SLOT;
   static constexpr int OFF_WLOG = OFF_COMB + COMB;
-  static constexpr int OFF_SWT = OFF_WLOG + WLOG;
-  static constexpr int OFF_SEG = ((OFF_SWT + SWT + 15) / 16) * 16;
+  static constexpr int OFF_SEG = ((OFF_WLOG + WLOG + 15) / 16) * 16;
   static constexpr int OFF_QP = OFF_SEG + SEGB;          // [NSEG][QPB]
   static constexpr int OFF_SMETA = OFF_QP + QPREP;        // [SLOTS] int4 (tlo | thi << 16, step token, page, entry)
   static constexpr int OFF_BAR = OFF_SMETA + SLOTS * 16;  // full[SLOTS], empty[SLOTS]
@@ -174,17 +174,20 @@ __device__ __forceinline__ int ld_acquire_shared(const int *p) {
 }
 
 // Waits until ring entry kk (this CTA's entry sequence number) has landed in its slot. The slot's barrier completes
-// one phase per entry issued to it, in order, and a warp may reach its entry before the slot's earlier entries have
-// landed: a parity wait can then return for an earlier phase. The producer stamps the slot with kk before the phase
-// of kk can complete, so after each completed wait the stamp tells whether the phase was ours; if not, wait for the
-// other parity (the pending earlier phase) and retry. Every attempt that fails moves the slot on by a phase, and
-// at most kk / SLOTS phases precede kk's, which bounds the attempts. All waits suspend in hardware and are bounded.
+// one phase per entry issued to it, in order (entry kk is phase kk / SLOTS of its slot), and a warp may reach its
+// entry while an earlier phase of the slot is still pending, when a parity wait alone can return for that earlier
+// phase. The producer stamps the slot with kk before it issues kk's copy, and it issues kk only after the slot's
+// previous phase has completed and been consumed. So once the stamp reads kk, the pending phase is kk's own (or it
+// has completed) and the parity wait is exact. Until then the warp waits on the parity of each earlier phase in turn
+// (each attempt that fails moves the slot on by a phase; at most kk / SLOTS phases precede kk's). All waits suspend
+// in hardware and are bounded.
 template <int SLOTS>
 __device__ __forceinline__ bool wait_entry(const int *stamp, uint64_t *full, int kk, uint32_t parity, int *err) {
   const int attempts = kk / SLOTS + 2;
   for (int attempt = 0; attempt < attempts; ++attempt) {
+    if (ld_acquire_shared(stamp) == kk) return mbar_wait(full, parity, err);
     if (!mbar_wait(full, parity, err)) return false;
-    if (ld_acquire_shared(stamp) == kk) return true;
+    if (ld_acquire_shared(stamp) == kk) return mbar_wait(full, parity, err);
     if (!mbar_wait(full, parity ^ 1u, err)) return false;
   }
   set_error(err, kErrTimeout);
@@ -205,6 +208,19 @@ __device__ __forceinline__ void store4<float>(float *dst, float a, float b, floa
   *reinterpret_cast<float4 *>(dst) = make_float4(a, b, c, d);
 }
 
+// Two consecutive elements of T in one load or store.
+template <class T> struct Vec2;
+template <> struct Vec2<__nv_bfloat16> {
+  using type = __nv_bfloat162;
+  __device__ static float get(type v, int t) { return t == 0 ? __low2float(v) : __high2float(v); }
+  __device__ static type make(float a, float b) { return __floats2bfloat162_rn(a, b); }
+};
+template <> struct Vec2<float> {
+  using type = float2;
+  __device__ static float get(type v, int t) { return t == 0 ? v.x : v.y; }
+  __device__ static type make(float a, float b) { return make_float2(a, b); }
+};
+
 template <class T, int D, int G>
 __global__ void __launch_bounds__((Shape<T, D, G>::THREADS)) __maxnreg__((Shape<T, D, G>::MAXREG)) propose_kernel(
     const Params p) {
@@ -213,7 +229,6 @@ __global__ void __launch_bounds__((Shape<T, D, G>::THREADS)) __maxnreg__((Shape<
   unsigned char *kv = smem + C::OFF_KV;
   float *comb = reinterpret_cast<float *>(smem + C::OFF_COMB);      // [C::NCW][REC]
   float *wlog_all = reinterpret_cast<float *>(smem + C::OFF_WLOG);  // [C::NCW][16][G] float2 (or [G][16] float)
-  float *swt_all = reinterpret_cast<float *>(smem + C::OFF_SWT);    // [NSEG][G * NCW + 2G]
   unsigned char *qprep_all = smem + C::OFF_QP;                       // [NSEG][QPB]
   Seg *segs = reinterpret_cast<Seg *>(smem + C::OFF_SEG);
   int4 *smeta = reinterpret_cast<int4 *>(smem + C::OFF_SMETA);
@@ -272,10 +287,17 @@ __global__ void __launch_bounds__((Shape<T, D, G>::THREADS)) __maxnreg__((Shape<
   }
   __syncthreads();
   const int64_t E = s_total;
-  // Split over nb <= E CTAs so that every participating CTA owns at least one entry (the merge counts them).
-  const int nb = static_cast<int>(E < static_cast<int64_t>(gridDim.x) ? E : static_cast<int64_t>(gridDim.x));
+  // Split over nb <= E CTAs so that every participating CTA owns at least one entry (the merge counts them). A short
+  // launch (at most kShortEntries per CTA) leaves the grid's last CTAs idle: they are dispatched last, onto the SMs
+  // that the previous kernel frees last, and waiting for those SMs would hold up the whole launch (as long as the
+  // rest of the launch takes, the SMs freed first then take the next launch's first CTAs).
+  int nb = static_cast<int>(E < static_cast<int64_t>(gridDim.x) ? E : static_cast<int64_t>(gridDim.x));
+  if (E <= static_cast<int64_t>(kShortEntries) * gridDim.x)
+    nb = min(nb, static_cast<int>(gridDim.x - gridDim.x / kSpareDiv));
   if (E == 0 || static_cast<int>(blockIdx.x) >= nb) {
-    if (p.settled) grid_dependency_sync();  // an idle CTA still orders its dependents after the previous kernel
+    // With nothing to do at all, a CTA still orders its dependents after the previous kernel; beside working CTAs,
+    // whose triggers follow their own waits, an idle CTA just leaves.
+    if (p.settled && E == 0) grid_dependency_sync();
     return;
   }
   const int64_t cta_begin = static_cast<int64_t>(blockIdx.x) * E / nb;
@@ -396,29 +418,33 @@ __global__ void __launch_bounds__((Shape<T, D, G>::THREADS)) __maxnreg__((Shape<
       // one ring length ahead at most. Entry u of a round, counted over the segments in order, gets the sequence
       // number (kacc + u) of this CTA: its ring slot and the stamp the consumer checks.
       // The entries past the ring's first fill (up to kPrefetchAhead, in each segment's share) are prefetched into
-      // L2 at once, so that the ring refills from L2 when the consumers free their slots; before the dependency
-      // wait, only pages whose visible tokens are all prompt tokens.
-      for (int si = 0; si < nseg; ++si) {
-        const Seg sg = segs[si];
-        const int64_t n = sg.e - sg.b;
-        const int64_t lo = sg.b + (static_cast<int64_t>(C::SLOTS) * sg.nw) / C::NCW;
-        const int64_t hi = min(sg.e, sg.b + (static_cast<int64_t>(C::SLOTS + kPrefetchAhead) * sg.nw) / C::NCW);
-        if (n <= 0 || lo >= hi) continue;
-        const int r = sg.row / p.hkv, h = sg.row - r * p.hkv;
-        const int L = p.ctx_len[r], S = p.seq_len[r], nsel = p.vnsel[sg.vr];
-        for (int64_t e = lo + lane; e < hi; e += 32) {
-          const int i = static_cast<int>(e - sg.rb);
-          const size_t o = static_cast<size_t>(sg.vr) * p.vcap + i;
-          const int page = p.vbt[o], base = p.vlp[o] * kPage;
-          const int thi = min(kPage, S - base), tlo = (i < nsel) ? 0 : max(0, L - base);
-          if (thi > tlo && page >= 0 && page < p.num_pages && (waited || base + thi <= L)) {
-            const size_t off = (static_cast<size_t>(page) * p.hkv + h) * kPage * D;
-            bulk_prefetch_l2(Kp + off, C::CHUNK);
-            bulk_prefetch_l2(Vp + off, C::CHUNK);
+      // L2 once the ring is full, so that it refills from L2 when the consumers free their slots; before the
+      // dependency wait, only pages whose visible tokens are all prompt tokens. (Issued before the first fill, their
+      // metadata loads would hold back the first copies by a round trip per segment.)
+      auto prefetch_window = [&]() {
+        for (int si = 0; si < nseg; ++si) {
+          const Seg sg = segs[si];
+          const int64_t n = sg.e - sg.b;
+          const int64_t lo = sg.b + (static_cast<int64_t>(C::SLOTS) * sg.nw) / C::NCW;
+          const int64_t hi = min(sg.e, sg.b + (static_cast<int64_t>(C::SLOTS + kPrefetchAhead) * sg.nw) / C::NCW);
+          if (n <= 0 || lo >= hi) continue;
+          const int r = sg.row / p.hkv, h = sg.row - r * p.hkv;
+          const int L = p.ctx_len[r], S = p.seq_len[r], nsel = p.vnsel[sg.vr];
+          for (int64_t e = lo + lane; e < hi; e += 32) {
+            const int i = static_cast<int>(e - sg.rb);
+            const size_t o = static_cast<size_t>(sg.vr) * p.vcap + i;
+            const int page = p.vbt[o], base = p.vlp[o] * kPage;
+            const int thi = min(kPage, S - base), tlo = (i < nsel) ? 0 : max(0, L - base);
+            if (thi > tlo && page >= 0 && page < p.num_pages && (waited || base + thi <= L)) {
+              const size_t off = (static_cast<size_t>(page) * p.hkv + h) * kPage * D;
+              bulk_prefetch_l2(Kp + off, C::CHUNK);
+              bulk_prefetch_l2(Vp + off, C::CHUNK);
+            }
           }
         }
-      }
+      };
       int64_t kacc = (nseg > 0) ? segs[0].b - cta_begin : 0;
+      bool prefetched = false;
       for (int j = 0;; ++j) {
         // this round's share of every segment; lane u < total takes entry u of the round
         int total = 0, my_si = -1, my_u = 0;
@@ -435,6 +461,10 @@ __global__ void __launch_bounds__((Shape<T, D, G>::THREADS)) __maxnreg__((Shape<
           }
         }
         if (total == 0) break;
+        if (!prefetched && kacc + total > C::SLOTS) {  // this round waits for freed slots
+          prefetch_window();
+          prefetched = true;
+        }
         const bool act = my_si >= 0;
         int i = 0, page = 0, base = 0, tlo = 0, thi = 0, L = 0, S = 0, h = 0, rn = 0;
         if (act) {
@@ -501,42 +531,75 @@ __global__ void __launch_bounds__((Shape<T, D, G>::THREADS)) __maxnreg__((Shape<
       unsigned char *qp = qprep_all + si * C::QPB;
       float *qprep = reinterpret_cast<float *>(qp);          // [G][D] query of the group, ready for the dot products
       T *stepkv = reinterpret_cast<T *>(qp + G * D * 4);     // [D] step key (rotated), then [D] step value
+      // The group's first warp prepares what every warp of the group needs once: the G query heads, rotated at the
+      // step position P (fused form), rounded to T as a stored query would be and scaled by log2(e)/sqrt(D); in the
+      // fused form also the step token's key (rotated by the same angles) and value. Lane l takes the rotary pairs
+      // (i, i + D/2) for i = 2l and 2l + 1 (lanes with 2l >= D/2 idle). The angles depend on the lengths only, which
+      // a settled view lets the warp read before the dependency wait; after it, the loads of q and of the step token
+      // (two elements each) are all issued before the first is used (one round trip).
+      const int i2 = 2 * lane;
+      const bool rot_lane = gw == 0 && i2 < D / 2;
+      if (rot_lane && fused) {
+        // cos and sin of the lane's two angles, parked in the lane's own elements of head 0's query row
+        const int P = p.seq_len[r] - 1;
+        rope_factors(P, p.inv_freq[i2], qprep[i2], qprep[i2 + D / 2]);
+        rope_factors(P, p.inv_freq[i2 + 1], qprep[i2 + 1], qprep[i2 + 1 + D / 2]);
+      }
       if (!waited) {
         grid_dependency_sync();  // before q, the step token, outputs and the workspace
         waited = true;
       }
-      if (gw == 0) {
-        // The group's first warp prepares what every warp of the group needs once: the G query heads, rotated at
-        // the step position P (fused form), rounded to T as a stored query would be and scaled by log2(e)/sqrt(D);
-        // in the fused form also the step token's key (rotated by the same angles) and value. Lane l takes the
-        // rotary pairs (i, i + D/2) with i = l, l + 32, ..., so it forms D/64 angles.
-        const T *qrow = static_cast<const T *>(p.q) + (static_cast<size_t>(r) * p.hq + h * G) * D;
-        const int P = fused ? p.seq_len[r] - 1 : 0;
-        const size_t src = (static_cast<size_t>(r) * p.hkv + h) * D;
-        for (int i = lane; i < D / 2; i += 32) {
-          float cs = 1.0f, sn = 0.0f;
-          if (fused) rope_factors(P, p.inv_freq[i], cs, sn);
+      if (rot_lane) {
+        using P2 = typename Vec2<T>::type;
+        const P2 *qrow = reinterpret_cast<const P2 *>(static_cast<const T *>(p.q) +
+                                                      (static_cast<size_t>(r) * p.hq + h * G) * D + i2);
+        const size_t src = (static_cast<size_t>(r) * p.hkv + h) * D + i2;
+        P2 qx[G], qy[G], kx, ky, vx, vy;
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
-            float x = to_f(qrow[g * D + i]), y = to_f(qrow[g * D + i + D / 2]);
+        for (int g = 0; g < G; ++g) {
+          qx[g] = qrow[g * D / 2];
+          qy[g] = qrow[g * D / 2 + D / 4];
+        }
+        if (fused) {
+          const P2 *kn = reinterpret_cast<const P2 *>(static_cast<const T *>(p.k_new) + src);
+          const P2 *vn = reinterpret_cast<const P2 *>(static_cast<const T *>(p.v_new) + src);
+          kx = kn[0];
+          ky = kn[D / 4];
+          vx = vn[0];
+          vy = vn[D / 4];
+        }
+        float c[2] = {1.0f, 1.0f}, sn2[2] = {0.0f, 0.0f};
+        if (fused) {
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            c[t] = qprep[i2 + t];
+            sn2[t] = qprep[i2 + t + D / 2];
+          }
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            float x = Vec2<T>::get(qx[g], t), y = Vec2<T>::get(qy[g], t);
             if (fused) {
               float xr, yr;
-              rope_rotate(x, y, cs, sn, xr, yr);
+              rope_rotate(x, y, c[t], sn2[t], xr, yr);
               x = to_f(from_f<T>(xr));
               y = to_f(from_f<T>(yr));
             }
-            qprep[g * D + i] = x * qscale;
-            qprep[g * D + i + D / 2] = y * qscale;
+            qprep[g * D + i2 + t] = x * qscale;
+            qprep[g * D + i2 + t + D / 2] = y * qscale;
           }
-          if (fused) {
-            const T *kn = static_cast<const T *>(p.k_new) + src, *vn = static_cast<const T *>(p.v_new) + src;
-            float xr, yr;
-            rope_rotate(to_f(kn[i]), to_f(kn[i + D / 2]), cs, sn, xr, yr);
-            stepkv[i] = from_f<T>(xr);
-            stepkv[i + D / 2] = from_f<T>(yr);
-            stepkv[D + i] = vn[i];
-            stepkv[D + i + D / 2] = vn[i + D / 2];
-          }
+        }
+        if (fused) {
+          float xr[2], yr[2];
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+            rope_rotate(Vec2<T>::get(kx, t), Vec2<T>::get(ky, t), c[t], sn2[t], xr[t], yr[t]);
+          *reinterpret_cast<P2 *>(stepkv + i2) = Vec2<T>::make(xr[0], xr[1]);
+          *reinterpret_cast<P2 *>(stepkv + i2 + D / 2) = Vec2<T>::make(yr[0], yr[1]);
+          *reinterpret_cast<P2 *>(stepkv + D + i2) = vx;
+          *reinterpret_cast<P2 *>(stepkv + D + i2 + D / 2) = vy;
         }
       }
       group_sync(bar_id, bar_n);
@@ -775,35 +838,29 @@ __global__ void __launch_bounds__((Shape<T, D, G>::THREADS)) __maxnreg__((Shape<
       }
       group_sync(bar_id, bar_n);
 
-      // ---- the group combines its warps' states. The group's first warp derives, per head, the max M over the
-      // warps, each warp's weight 2^(m_w - M) and the weighted sum L (lane j = warp j of the group); then every
-      // thread forms its elements' weighted sums with all the group's loads in flight.
+      // ---- the group combines its warps' states: for each of its elements (head g), a thread forms the max M over
+      // the group's warps, their weights 2^(m_w - M), the weighted sum L and the weighted output, with no further
+      // barrier.
       const int gt = gw * 32 + lane, GT = nw * 32;
-      float *wts = swt_all + si * (G * C::NCW + 2 * G);  // [G][NCW] weights, then M[G], L[G]
-      if (gw == 0) {
+      auto combined = [&](int i, int g, float &M, float &Ls) {
+        const float *rec = comb + sg.w0 * C::REC;
+        float mw[C::NCW];
+        M = -INFINITY;
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float *rec = comb + (sg.w0 + lane) * C::REC + G * D;
-          const float mw = lane < nw ? rec[g] : -INFINITY;
-          const float lw = lane < nw ? rec[G + g] : 0.0f;
-          const float M = warp_max(mw);
-          const float wgt = (mw == -INFINITY) ? 0.0f : exp2f(mw - M);
-          const float Ls = warp_sum(lw * wgt);
-          if (lane < C::NCW) wts[g * C::NCW + lane] = wgt;
-          if (lane == 0) {
-            wts[G * C::NCW + g] = M;
-            wts[G * C::NCW + G + g] = Ls;
+        for (int j = 0; j < C::NCW; ++j) {
+          mw[j] = j < nw ? rec[j * C::REC + G * D + g] : -INFINITY;
+          M = fmaxf(M, mw[j]);
+        }
+        float acc = 0.0f;
+        Ls = 0.0f;
+#pragma unroll
+        for (int j = 0; j < C::NCW; ++j) {
+          if (j < nw && mw[j] != -INFINITY) {
+            const float w = exp2f(mw[j] - M);
+            Ls = fmaf(rec[j * C::REC + G * D + G + g], w, Ls);
+            acc = fmaf(rec[j * C::REC + i], w, acc);
           }
         }
-      }
-      group_sync(bar_id, bar_n);
-      auto combined = [&](int i, int g) {
-        const float *ci = comb + sg.w0 * C::REC + i;
-        const float *wg = wts + g * C::NCW;
-        float acc = 0.0f;
-#pragma unroll
-        for (int j = 0; j < C::NCW; ++j)
-          if (j < nw) acc = fmaf(ci[j * C::REC], wg[j], acc);
         return acc;
       };
 
@@ -815,8 +872,8 @@ __global__ void __launch_bounds__((Shape<T, D, G>::THREADS)) __maxnreg__((Shape<
       if (b_first == b_last) {
         for (int i = gt; i < G * D; i += GT) {
           const int g = i / D;
-          const float M = wts[G * C::NCW + g], Ls = wts[G * C::NCW + G + g];
-          const float acc = combined(i, g);
+          float M, Ls;
+          const float acc = combined(i, g, M, Ls);
           outp[out_base + i] = from_f<T>(Ls > 0.0f ? acc / Ls : 0.0f);
           if (i - g * D == 0) {
             lse_row[g] = Ls > 0.0f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
@@ -827,8 +884,8 @@ __global__ void __launch_bounds__((Shape<T, D, G>::THREADS)) __maxnreg__((Shape<
         const size_t pslot = static_cast<size_t>(blockIdx.x) + sg.row;
         for (int i = gt; i < G * D; i += GT) {
           const int g = i / D;
-          const float M = wts[G * C::NCW + g], Ls = wts[G * C::NCW + G + g];
-          __stcg(p.part + pslot * G * D + i, combined(i, g));
+          float M, Ls;
+          __stcg(p.part + pslot * G * D + i, combined(i, g, M, Ls));
           if (i - g * D == 0) {
             __stcg(reinterpret_cast<float2 *>(p.ml) + pslot * G + g, make_float2(M, Ls));
           }
