@@ -651,6 +651,8 @@ __global__ void __launch_bounds__((Shape<T, D, G>::THREADS)) __maxnreg__((Shape<
         sw[s2] = s2 < nseg ? segs[s2].nw : 1;
       }
       const int n_mine = static_cast<int>(sg.e - sg.b);
+      // the CTAs sharing this row (formed while the first pages are in flight: two 64-bit divisions)
+      const int b_first = owner_cta(sg.rb, E, nb), b_last = owner_cta(sg.re - 1, E, nb);
       int issued = static_cast<int>(segs[0].b - cta_begin);  // sequence number of round j's first entry
       for (int j = 0; j * nw + gw < n_mine; ++j) {
         int before = 0, round = 0;
@@ -843,29 +845,33 @@ __global__ void __launch_bounds__((Shape<T, D, G>::THREADS)) __maxnreg__((Shape<
       // barrier.
       const int gt = gw * 32 + lane, GT = nw * 32;
       auto combined = [&](int i, int g, float &M, float &Ls) {
+        // every load is issued up front (records past the group's last warp are read at the last warp's index and
+        // weighted out), so that the loads overlap instead of following each other
         const float *rec = comb + sg.w0 * C::REC;
-        float mw[C::NCW];
-        M = -INFINITY;
+        float mw[C::NCW], lw[C::NCW], ow[C::NCW];
 #pragma unroll
         for (int j = 0; j < C::NCW; ++j) {
-          mw[j] = j < nw ? rec[j * C::REC + G * D + g] : -INFINITY;
-          M = fmaxf(M, mw[j]);
+          const float *rj = rec + min(j, nw - 1) * C::REC;
+          mw[j] = rj[G * D + g];
+          lw[j] = rj[G * D + G + g];
+          ow[j] = rj[i];
         }
+        M = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < C::NCW; ++j) M = fmaxf(M, mw[j]);
         float acc = 0.0f;
         Ls = 0.0f;
 #pragma unroll
         for (int j = 0; j < C::NCW; ++j) {
-          if (j < nw && mw[j] != -INFINITY) {
-            const float w = exp2f(mw[j] - M);
-            Ls = fmaf(rec[j * C::REC + G * D + G + g], w, Ls);
-            acc = fmaf(rec[j * C::REC + i], w, acc);
-          }
+          const bool live = j < nw && mw[j] != -INFINITY;
+          const float w = exp2f(live ? mw[j] - M : -INFINITY);
+          Ls = live ? fmaf(lw[j], w, Ls) : Ls;
+          acc = live ? fmaf(ow[j], w, acc) : acc;
         }
         return acc;
       };
 
       // ---- finish the row, or hand over a partial record (the last CTA to finish the row merges)
-      const int b_first = owner_cta(sg.rb, E, nb), b_last = owner_cta(sg.re - 1, E, nb);
       const size_t out_base = (static_cast<size_t>(r) * p.hq + h * G) * D;
       T *outp = static_cast<T *>(p.out);
       float *lse_row = p.lse + static_cast<size_t>(r) * p.hq + h * G;
