@@ -4,6 +4,7 @@
 // Sources: EarlySelectKV news page (pages ranked by their K summaries, proxy query allowed), KRI page (KRI-Q:
 // Q . block-mean K; the A<a>R<r>K<k> tag), KAP paper (compiler: spans resolved to KV pages, compact view in access
 // order with logical positions, block tables and slot mappings).
+#include <algorithm>
 #include "kap_device.cuh"
 #include "kap_launch.h"
 
@@ -65,107 +66,208 @@ __global__ void __launch_bounds__(128) refresh_summaries_kernel(const T *__restr
 }
 
 // ---------------------------------------------------------------------------------------------- scores
-// grid.x: chunks of 64 logical pages; grid.y: (request, selection row). 8 warps; each warp scores 8 pages. The
-// prompt length, the warp's block-table entries and the query rows are loaded together, and the first head's
-// summary loads are in flight (unconditionally, from clamped page ids) while the group-summed query is formed.
+// Work items are (request, selection row, chunk of 32 logical pages), in request, row, chunk order; only chunks that
+// hold prompt pages exist. A grid of a few CTAs per SM walks them: with at most kScoreScanMax requests every CTA scans
+// the requests' item counts into shared memory and takes a contiguous range of items (so ragged prompts balance
+// over the SMs and no CTA is spent on pages past a prompt's end); with more requests, grid row r takes request r's
+// items in a strided loop. Per item, warp w scores 4 pages. The next item's block-table entries and, when its row
+// changes, its query elements are loaded while the current item's summaries are in flight.
 // Dot products follow the fixed order: lane l accumulates fmaf over i = l, l+32, ...; then an xor-butterfly
-// 16, 8, 4, 2, 1.
-constexpr int kScorePagesPerWarp = 4;  // 4 and 8 measured: more, smaller CTAs (fewer registers) win slightly
+// 16, 8, 4, 2, 1. The query of a row is summed over its G heads in ascending order (fp32), once per row.
+constexpr int kScorePagesPerWarp = 4;
 constexpr int kScorePagesPerCta = 8 * kScorePagesPerWarp;
 constexpr int kMaxPooledHeads = 16;
+constexpr int kScoreCtasPerSm = 4;
+constexpr int kScoreScanMax = 2048;
 
-template <class T, int D>
-__global__ void __launch_bounds__(256) score_kernel(const T *__restrict__ q, const float *__restrict__ S, int hkv,
-                                                    int hq, int num_pages, const int32_t *__restrict__ bt,
-                                                    int max_pages, const int32_t *__restrict__ ctx_len,
-                                                    int per_head, float *__restrict__ scores, int *err) {
+struct ScoreItem {
+  int r, v, j0, N;  // request, row within the request, first page, prompt pages of the request
+};
+
+template <class T, int D, bool PER_HEAD>
+__global__ void __launch_bounds__(256, kScoreCtasPerSm) score_kernel(
+    const T *__restrict__ q, const float *__restrict__ S, int hkv, int hq, int num_pages,
+    const int32_t *__restrict__ bt, int max_pages, const int32_t *__restrict__ ctx_len, int R,
+    float *__restrict__ scores, int *err) {
   constexpr int C = D / 32;
+  // query elements a thread sums: one head's row, or the pooled heads' rows
+  constexpr int QPT = ((PER_HEAD ? 1 : kMaxPooledHeads) * D + 255) / 256;
+  constexpr bool per_head = PER_HEAD;
   __shared__ float qbar[kMaxPooledHeads][D];
+  __shared__ int s_cum[kScoreScanMax + 1];  // items before request r
+  __shared__ int s_np[kScoreScanMax];       // prompt pages of request r
+  __shared__ int scan_scratch[32];
   grid_dependency_sync();
   const int rows = per_head ? hkv : 1;
-  const int row = blockIdx.y;
-  const int r = row / rows, v = row - r * rows;
   const int G = hq / hkv;
-  const int h_lo = per_head ? v : 0, h_hi = per_head ? v + 1 : hkv;
+  const int nh = per_head ? 1 : hkv;  // heads pooled into one row
+  const int nq = nh * D;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int j0 = blockIdx.x * kScorePagesPerCta;
-  const int jb = j0 + warp * kScorePagesPerWarp;
-  // independent loads: prompt length, block-table entries of this warp's pages, this thread's query elements
-  const int Lr = ctx_len[r];
-  const int32_t *btr = bt + static_cast<size_t>(r) * max_pages;
-  int pg[kScorePagesPerWarp];
-#pragma unroll
-  for (int u = 0; u < kScorePagesPerWarp; ++u) pg[u] = (jb + u < max_pages) ? btr[jb + u] : -1;
-  const int nq = (h_hi - h_lo) * D;
-  float qsum0 = 0.0f, qsum1 = 0.0f;  // this thread's (at most two) elements of the group-summed query
-  {
-    const int i0 = threadIdx.x, i1 = threadIdx.x + blockDim.x;
-    for (int g = 0; g < G; ++g) {
-      if (i0 < nq)
-        qsum0 = __fadd_rn(qsum0, to_f(q[(static_cast<size_t>(r) * hq + (h_lo + i0 / D) * G + g) * D + i0 % D]));
-      if (i1 < nq)
-        qsum1 = __fadd_rn(qsum1, to_f(q[(static_cast<size_t>(r) * hq + (h_lo + i1 / D) * G + g) * D + i1 % D]));
+  const bool flat = R <= kScoreScanMax;  // uniform over the grid
+  auto pages_of = [&](int r) { return min((ctx_len[r] + kPage - 1) / kPage, max_pages); };
+
+  int64_t t = 0, t_end = 0, t_step = 1;
+  int r_cur = 0;
+  if (flat) {
+    const int per = (R + 255) / 256;
+    const int lo = min(R, static_cast<int>(threadIdx.x) * per), hi = min(R, lo + per);
+    auto items_of = [&](int n) { return rows * ((n + kScorePagesPerCta - 1) / kScorePagesPerCta); };
+    int cnt = 0;
+    for (int r = lo; r < hi; ++r) {
+      const int n = pages_of(r);
+      s_np[r] = n;
+      cnt += items_of(n);
     }
-  }
-  const int N = min((Lr + kPage - 1) / kPage, max_pages);
-  if (j0 >= N) return;  // uniform over the CTA
-  bool ok[kScorePagesPerWarp];
-  int pc[kScorePagesPerWarp];
-#pragma unroll
-  for (int u = 0; u < kScorePagesPerWarp; ++u) {
-    ok[u] = jb + u < N;
-    if (ok[u] && (pg[u] < 0 || pg[u] >= num_pages)) {
-      ok[u] = false;
-      if (lane == 0) set_error(err, kErrPage);
+    const int incl = block_inclusive_scan(cnt, scan_scratch);
+    int run = incl - cnt;
+    for (int r = lo; r < hi; ++r) {
+      s_cum[r] = run;
+      run += items_of(s_np[r]);
     }
-    pc[u] = ok[u] ? pg[u] : 0;  // a valid page: the loads below are unconditional
+    if (threadIdx.x == 255) s_cum[R] = incl;
+    __syncthreads();
+    const int64_t W = s_cum[R];
+    t = static_cast<int64_t>(blockIdx.x) * W / gridDim.x;
+    t_end = static_cast<int64_t>(blockIdx.x + 1) * W / gridDim.x;
+    int lo_r = 0, hi_r = R - 1;  // the request holding item t: the last r with s_cum[r] <= t
+    while (lo_r < hi_r) {
+      const int mid = (lo_r + hi_r + 1) >> 1;
+      if (s_cum[mid] <= t) lo_r = mid; else hi_r = mid - 1;
+    }
+    r_cur = lo_r;
+  } else {
+    r_cur = blockIdx.y;
+    const int n = pages_of(r_cur);
+    t = blockIdx.x;
+    t_step = gridDim.x;
+    t_end = static_cast<int64_t>(rows) * ((n + kScorePagesPerCta - 1) / kScorePagesPerCta);
   }
-  float sv[kScorePagesPerWarp][C];
+  auto decode = [&](int64_t ti) {
+    ScoreItem it;
+    int within;
+    if (flat) {
+      while (ti >= s_cum[r_cur + 1]) ++r_cur;  // items are visited in ascending order
+      it.r = r_cur;
+      it.N = s_np[r_cur];
+      within = static_cast<int>(ti - s_cum[r_cur]);
+    } else {
+      it.r = r_cur;
+      it.N = pages_of(r_cur);
+      within = static_cast<int>(ti);
+    }
+    const int nch = (it.N + kScorePagesPerCta - 1) / kScorePagesPerCta;
+    it.v = within / nch;
+    it.j0 = (within - it.v * nch) * kScorePagesPerCta;
+    return it;
+  };
+  // this warp's block-table entries of an item (-1 past the prompt)
+  auto load_pages = [&](const ScoreItem &it, int (&pg)[kScorePagesPerWarp]) {
+    const int jb = it.j0 + warp * kScorePagesPerWarp;
+    const int32_t *btr = bt + static_cast<size_t>(it.r) * max_pages;
 #pragma unroll
-  for (int u = 0; u < kScorePagesPerWarp; ++u)
+    for (int u = 0; u < kScorePagesPerWarp; ++u) pg[u] = (jb + u < it.N) ? btr[jb + u] : -1;
+  };
+  // this thread's elements of the row's group-summed query (heads ascending, fp32)
+  auto load_query = [&](const ScoreItem &it, float (&qs)[QPT]) {
+    const int h_lo = per_head ? it.v : 0;
 #pragma unroll
-    for (int c = 0; c < C; ++c) sv[u][c] = __ldg(S + (static_cast<size_t>(pc[u]) * hkv + h_lo) * D + lane + 32 * c);
-  // group-summed query rows into shared memory (g ascending, fp32)
-  {
-    const int i0 = threadIdx.x, i1 = threadIdx.x + blockDim.x;
-    if (i0 < nq) qbar[i0 / D][i0 % D] = qsum0;
-    if (i1 < nq) qbar[i1 / D][i1 % D] = qsum1;
-    for (int i = threadIdx.x + 2 * blockDim.x; i < nq; i += blockDim.x) {  // more than 2*blockDim elements
+    for (int e = 0; e < QPT; ++e) {
+      const int i = static_cast<int>(threadIdx.x) + 256 * e;
       float acc = 0.0f;
-      for (int g = 0; g < G; ++g)
-        acc = __fadd_rn(acc, to_f(q[(static_cast<size_t>(r) * hq + (h_lo + i / D) * G + g) * D + i % D]));
-      qbar[i / D][i % D] = acc;
+      if (i < nq) {
+        const T *qr = q + (static_cast<size_t>(it.r) * hq + (h_lo + i / D) * G) * D + i % D;
+        for (int g = 0; g < G; ++g) acc = __fadd_rn(acc, to_f(qr[static_cast<size_t>(g) * D]));
+      }
+      qs[e] = acc;
     }
-  }
-  __syncthreads();
-  if (jb >= N) return;
-  float tot[kScorePagesPerWarp];
-  for (int hh = h_lo; hh < h_hi; ++hh) {
-    if (hh > h_lo) {
-#pragma unroll
-      for (int u = 0; u < kScorePagesPerWarp; ++u)
-#pragma unroll
-        for (int c = 0; c < C; ++c) sv[u][c] = __ldg(S + (static_cast<size_t>(pc[u]) * hkv + hh) * D + lane + 32 * c);
-    }
+  };
+
+  if (t >= t_end) return;
+  ScoreItem cur = decode(t);
+  int pg[kScorePagesPerWarp];
+  float qs[QPT];
+  load_pages(cur, pg);
+  load_query(cur, qs);
+  int qrow = -1;  // the row whose query sits in qbar
+  while (true) {
+    const int row = cur.r * rows + cur.v;
+    const int h_lo = per_head ? cur.v : 0;
+    const int jb = cur.j0 + warp * kScorePagesPerWarp;
+    bool ok[kScorePagesPerWarp];
+    int pc[kScorePagesPerWarp];
 #pragma unroll
     for (int u = 0; u < kScorePagesPerWarp; ++u) {
-      float a = 0.0f;
+      ok[u] = jb + u < cur.N;
+      if (ok[u] && (pg[u] < 0 || pg[u] >= num_pages)) {
+        ok[u] = false;
+        if (lane == 0) set_error(err, kErrPage);
+      }
+      pc[u] = ok[u] ? pg[u] : 0;  // a valid page: the loads below are unconditional
+    }
+    float sv[kScorePagesPerWarp][C];
 #pragma unroll
-      for (int c = 0; c < C; ++c) a = __fmaf_rn(qbar[hh - h_lo][lane + 32 * c], sv[u][c], a);
+    for (int u = 0; u < kScorePagesPerWarp; ++u)
 #pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, o));
-      tot[u] = (hh == h_lo) ? a : __fadd_rn(tot[u], a);
+      for (int c = 0; c < C; ++c) sv[u][c] = __ldg(S + (static_cast<size_t>(pc[u]) * hkv + h_lo) * D + lane + 32 * c);
+    // the next item's block-table entries, and its query when its row differs, while the summaries are in flight
+    const int64_t tn = t + t_step;
+    const bool more = tn < t_end;
+    ScoreItem nxt = cur;
+    int pgn[kScorePagesPerWarp];
+    float qsn[QPT];
+    if (more) {
+      nxt = decode(tn);
+      load_pages(nxt, pgn);
+      if (nxt.r * rows + nxt.v != row) load_query(nxt, qsn);
+    }
+    if (row != qrow) {  // uniform over the CTA
+      __syncthreads();  // every warp is done with the previous row's query
+#pragma unroll
+      for (int e = 0; e < QPT; ++e) {
+        const int i = static_cast<int>(threadIdx.x) + 256 * e;
+        if (i < nq) qbar[i / D][i % D] = qs[e];
+      }
+      __syncthreads();
+      qrow = row;
+    }
+    float tot[kScorePagesPerWarp];
+    for (int hh = 0; hh < nh; ++hh) {
+      if (hh > 0) {
+#pragma unroll
+        for (int u = 0; u < kScorePagesPerWarp; ++u)
+#pragma unroll
+          for (int c = 0; c < C; ++c)
+            sv[u][c] = __ldg(S + (static_cast<size_t>(pc[u]) * hkv + h_lo + hh) * D + lane + 32 * c);
+      }
+#pragma unroll
+      for (int u = 0; u < kScorePagesPerWarp; ++u) {
+        float acc = 0.0f;
+#pragma unroll
+        for (int c = 0; c < C; ++c) acc = __fmaf_rn(qbar[hh][lane + 32 * c], sv[u][c], acc);
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
+        tot[u] = (hh == 0) ? acc : __fadd_rn(tot[u], acc);
+      }
+    }
+    float val = tot[0];
+    bool okl = ok[0];
+#pragma unroll
+    for (int u = 1; u < kScorePagesPerWarp; ++u)
+      if (lane == u) {
+        val = tot[u];
+        okl = ok[u];
+      }
+    if (lane < kScorePagesPerWarp && okl) scores[static_cast<size_t>(row) * max_pages + jb + lane] = val;
+    if (!more) break;
+    t = tn;
+    cur = nxt;
+#pragma unroll
+    for (int u = 0; u < kScorePagesPerWarp; ++u) pg[u] = pgn[u];
+    if (nxt.r * rows + nxt.v != row) {
+#pragma unroll
+      for (int e = 0; e < QPT; ++e) qs[e] = qsn[e];
     }
   }
-  float val = tot[0];
-  bool okl = ok[0];
-#pragma unroll
-  for (int u = 1; u < kScorePagesPerWarp; ++u)
-    if (lane == u) {
-      val = tot[u];
-      okl = ok[u];
-    }
-  if (lane < kScorePagesPerWarp && okl) scores[static_cast<size_t>(row) * max_pages + jb + lane] = val;
 }
 
 // ------------------------------------------------------------------------------------ compaction helper
@@ -630,18 +732,34 @@ cudaError_t launch_refresh_summaries(const PoolArgs &p, const int32_t *pages, co
   return cudaGetLastError();
 }
 
+template <class T, int D>
+void launch_score_td(const PoolArgs &p, const MapArgs &m, const void *q, int per_head, float *scores, int *err,
+                     dim3 grid, cudaStream_t s) {
+  const T *qt = static_cast<const T *>(q);
+  if (per_head)
+    launch_pdl(score_kernel<T, D, true>, grid, dim3(256), 0, s, qt, p.ksum, p.hkv, p.hq, p.num_pages, m.bt,
+               m.max_pages, m.ctx_len, m.R, scores, err);
+  else
+    launch_pdl(score_kernel<T, D, false>, grid, dim3(256), 0, s, qt, p.ksum, p.hkv, p.hq, p.num_pages, m.bt,
+               m.max_pages, m.ctx_len, m.R, scores, err);
+}
+
 cudaError_t launch_score(const PoolArgs &p, const MapArgs &m, const void *q, int per_head, float *scores, int *err,
                          cudaStream_t s) {
   const int rows = per_head ? p.hkv : 1;
-  dim3 grid((m.max_pages + kScorePagesPerCta - 1) / kScorePagesPerCta, m.R * rows);
-#define KAP_SCORE(T, D)                                                                                    \
-  launch_pdl(score_kernel<T, D>, grid, dim3(256), 0, s, static_cast<const T *>(q), p.ksum, p.hkv, p.hq,     \
-             p.num_pages, m.bt, m.max_pages, m.ctx_len, per_head, scores, err)
-  if (p.dtype == 0 && p.d == 128) KAP_SCORE(__nv_bfloat16, 128);
-  else if (p.dtype == 0 && p.d == 64) KAP_SCORE(__nv_bfloat16, 64);
-  else if (p.dtype == 1 && p.d == 128) KAP_SCORE(float, 128);
-  else KAP_SCORE(float, 64);
-#undef KAP_SCORE
+  // Items: at most rows * ceil(max_pages / 32) per request. A few CTAs per SM, never more than there are items.
+  const int64_t per_req = static_cast<int64_t>(rows) * ((m.max_pages + kScorePagesPerCta - 1) / kScorePagesPerCta);
+  const int64_t cap = static_cast<int64_t>(device_sm_count()) * kScoreCtasPerSm;
+  dim3 grid;
+  if (m.R <= kScoreScanMax) {
+    grid = dim3(static_cast<unsigned>(std::min<int64_t>(cap, per_req * m.R)));
+  } else {
+    grid = dim3(static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(per_req, cap / m.R))), m.R);
+  }
+  if (p.dtype == 0 && p.d == 128) launch_score_td<__nv_bfloat16, 128>(p, m, q, per_head, scores, err, grid, s);
+  else if (p.dtype == 0 && p.d == 64) launch_score_td<__nv_bfloat16, 64>(p, m, q, per_head, scores, err, grid, s);
+  else if (p.dtype == 1 && p.d == 128) launch_score_td<float, 128>(p, m, q, per_head, scores, err, grid, s);
+  else launch_score_td<float, 64>(p, m, q, per_head, scores, err, grid, s);
   return cudaGetLastError();
 }
 
