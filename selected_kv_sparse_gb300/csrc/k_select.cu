@@ -66,12 +66,14 @@ __global__ void __launch_bounds__(128) refresh_summaries_kernel(const T *__restr
 }
 
 // ---------------------------------------------------------------------------------------------- scores
-// Work items are (request, selection row, chunk of 32 logical pages), in request, row, chunk order; only chunks that
-// hold prompt pages exist. A grid of a few CTAs per SM walks them: with at most kScoreScanMax requests every CTA scans
-// the requests' item counts into shared memory and takes a contiguous range of items (so ragged prompts balance
-// over the SMs and no CTA is spent on pages past a prompt's end); with more requests, grid row r takes request r's
-// items in a strided loop. Per item, warp w scores 4 pages. The next item's block-table entries and, when its row
-// changes, its query elements are loaded while the current item's summaries are in flight.
+// Work items are (request, selection row, chunk of 32 logical pages); only chunks that hold prompt pages exist. A
+// grid of a few CTAs per SM walks them. With kScoreFlatMin < R <= kScoreScanMax requests, every CTA scans the
+// requests' item counts into shared memory and takes a contiguous range of items in request, row, chunk order (so
+// ragged prompts balance over the SMs and no CTA is spent on pages past a prompt's end). Otherwise grid row r takes
+// request r's items, chunk-major, in a strided loop: a CTA then loads its first item's block-table entries and query
+// together with the prompt length (one round trip fewer for a small batch). Per item, warp w scores 4 pages. The
+// next item's block-table entries and, when its row changes, its query elements are loaded while the current item's
+// summaries are in flight.
 // Dot products follow the fixed order: lane l accumulates fmaf over i = l, l+32, ...; then an xor-butterfly
 // 16, 8, 4, 2, 1. The query of a row is summed over its G heads in ascending order (fp32), once per row.
 constexpr int kScorePagesPerWarp = 4;
@@ -79,6 +81,7 @@ constexpr int kScorePagesPerCta = 8 * kScorePagesPerWarp;
 constexpr int kMaxPooledHeads = 16;
 constexpr int kScoreCtasPerSm = 4;
 constexpr int kScoreScanMax = 2048;
+constexpr int kScoreFlatMin = 8;  // with at most this many requests, each request's items go to its own grid row
 
 struct ScoreItem {
   int r, v, j0, N;  // request, row within the request, first page, prompt pages of the request
@@ -103,7 +106,7 @@ __global__ void __launch_bounds__(256, kScoreCtasPerSm) score_kernel(
   const int nh = per_head ? 1 : hkv;  // heads pooled into one row
   const int nq = nh * D;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const bool flat = R <= kScoreScanMax;  // uniform over the grid
+  const bool flat = R > kScoreFlatMin && R <= kScoreScanMax;  // uniform over the grid
   auto pages_of = [&](int r) { return min((ctx_len[r] + kPage - 1) / kPage, max_pages); };
 
   int64_t t = 0, t_end = 0, t_step = 1;
@@ -135,37 +138,39 @@ __global__ void __launch_bounds__(256, kScoreCtasPerSm) score_kernel(
       if (s_cum[mid] <= t) lo_r = mid; else hi_r = mid - 1;
     }
     r_cur = lo_r;
-  } else {
+  }
+  int n_req = 0;  // per-request mode: the request's prompt pages
+  if (!flat) {
+    // items chunk-major (t = chunk * rows + row), so that an item's pages are known before the prompt length
     r_cur = blockIdx.y;
-    const int n = pages_of(r_cur);
+    n_req = pages_of(r_cur);  // in flight while the first item's loads are issued
     t = blockIdx.x;
     t_step = gridDim.x;
-    t_end = static_cast<int64_t>(rows) * ((n + kScorePagesPerCta - 1) / kScorePagesPerCta);
   }
   auto decode = [&](int64_t ti) {
     ScoreItem it;
-    int within;
     if (flat) {
       while (ti >= s_cum[r_cur + 1]) ++r_cur;  // items are visited in ascending order
       it.r = r_cur;
       it.N = s_np[r_cur];
-      within = static_cast<int>(ti - s_cum[r_cur]);
+      const int within = static_cast<int>(ti - s_cum[r_cur]);
+      const int nch = (it.N + kScorePagesPerCta - 1) / kScorePagesPerCta;
+      it.v = within / nch;
+      it.j0 = (within - it.v * nch) * kScorePagesPerCta;
     } else {
       it.r = r_cur;
-      it.N = pages_of(r_cur);
-      within = static_cast<int>(ti);
+      it.N = n_req;
+      it.v = static_cast<int>(ti % rows);
+      it.j0 = static_cast<int>(ti / rows) * kScorePagesPerCta;
     }
-    const int nch = (it.N + kScorePagesPerCta - 1) / kScorePagesPerCta;
-    it.v = within / nch;
-    it.j0 = (within - it.v * nch) * kScorePagesPerCta;
     return it;
   };
-  // this warp's block-table entries of an item (-1 past the prompt)
+  // this warp's block-table entries of an item (masked to the prompt where the scores are formed)
   auto load_pages = [&](const ScoreItem &it, int (&pg)[kScorePagesPerWarp]) {
     const int jb = it.j0 + warp * kScorePagesPerWarp;
     const int32_t *btr = bt + static_cast<size_t>(it.r) * max_pages;
 #pragma unroll
-    for (int u = 0; u < kScorePagesPerWarp; ++u) pg[u] = (jb + u < it.N) ? btr[jb + u] : -1;
+    for (int u = 0; u < kScorePagesPerWarp; ++u) pg[u] = (jb + u < max_pages) ? btr[jb + u] : -1;
   };
   // this thread's elements of the row's group-summed query (heads ascending, fp32)
   auto load_query = [&](const ScoreItem &it, float (&qs)[QPT]) {
@@ -182,12 +187,20 @@ __global__ void __launch_bounds__(256, kScoreCtasPerSm) score_kernel(
     }
   };
 
-  if (t >= t_end) return;
   ScoreItem cur = decode(t);
   int pg[kScorePagesPerWarp];
   float qs[QPT];
-  load_pages(cur, pg);
-  load_query(cur, qs);
+  if (!flat) {
+    load_pages(cur, pg);
+    load_query(cur, qs);
+    cur.N = n_req;  // the first use of the prompt length
+    t_end = static_cast<int64_t>(rows) * ((n_req + kScorePagesPerCta - 1) / kScorePagesPerCta);
+  }
+  if (t >= t_end) return;
+  if (flat) {
+    load_pages(cur, pg);
+    load_query(cur, qs);
+  }
   int qrow = -1;  // the row whose query sits in qbar
   while (true) {
     const int row = cur.r * rows + cur.v;
@@ -751,7 +764,7 @@ cudaError_t launch_score(const PoolArgs &p, const MapArgs &m, const void *q, int
   const int64_t per_req = static_cast<int64_t>(rows) * ((m.max_pages + kScorePagesPerCta - 1) / kScorePagesPerCta);
   const int64_t cap = static_cast<int64_t>(device_sm_count()) * kScoreCtasPerSm;
   dim3 grid;
-  if (m.R <= kScoreScanMax) {
+  if (m.R > kScoreFlatMin && m.R <= kScoreScanMax) {
     grid = dim3(static_cast<unsigned>(std::min<int64_t>(cap, per_req * m.R)));
   } else {
     grid = dim3(static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(per_req, cap / m.R))), m.R);
