@@ -93,8 +93,8 @@ struct TcSmem {
   static constexpr int OFF_Q = OFF_V + kStages * kStageBytes;     // Q[2] (segment parity)
   static constexpr int OFF_P = OFF_Q + 2 * 2 * KATOM;              // P[2] (tile parity)
   static constexpr int OFF_CM = OFF_P + 2 * 2 * KATOM;             // column maxima [4][NPMAX]
-  static constexpr int OFF_ST = OFF_CM + 4 * NPMAX * 4;            // m_run, lsum, alpha[2], m_sub : [5][NPMAX]
-  static constexpr int OFF_FLAG = OFF_ST + 5 * NPMAX * 4;          // rescale flag per tile parity [2]
+  static constexpr int OFF_ST = OFF_CM + 4 * NPMAX * 4;            // m_run, lsum, alpha[2], m_sub, thr : [6][NPMAX]
+  static constexpr int OFF_FLAG = OFF_ST + 6 * NPMAX * 4;          // rescale flag per tile parity [2]
   static constexpr int OFF_BAR = OFF_FLAG + 16;
   static constexpr int kMetaRing = 2 * kStages;  // tile metadata outlives its K stage (read until MMA2 and softmax)
   // kfull, vfull, kempty, vempty [kStages]; sfull, sfree, pfull, ofull, ofree, qfull, qempty [2];
@@ -162,6 +162,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // the running maxima as subtracted from the logits: m_run, or 0 while a column has seen no visible token (its
   // logits are then all -inf, and -inf - 0 gives the weight 0 where -inf - m_run would give NaN)
   float *m_sub = alpha_s + 2 * NPMAX;
+  // the raw logit above which a column's running max must be raised: (m_run + 8) / scale (-inf before any)
+  float *thr = m_sub + NPMAX;
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
   constexpr int kMR = L::kMetaRing;
   uint64_t *kfull = bars, *vfull = bars + kStages, *kempty = bars + 2 * kStages, *vempty = bars + 3 * kStages;
@@ -475,6 +477,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else if (warp < 4) {
     // ==================================================================================== softmax and merge
     const float scale2 = rsqrtf(128.0f) * kLog2e;
+    const float inv_scale2 = 1.0f / scale2;
+    constexpr bool kRawLogits = NPMAX >= 48;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     float lt[NPMAX];    // softmax role (thread = token): this token's share of each column's sum
     float oreg[NPMAX];  // merge role (thread = head-dim row): running output of each column
@@ -624,6 +628,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (tid < NPMAX) {
           m_run[tid] = -INFINITY;
           m_sub[tid] = 0.0f;
+          thr[tid] = -INFINITY;
           lsum[tid] = 0.0f;
         }
 #pragma unroll
@@ -661,19 +666,37 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int n_first = rel <= 0 ? 0 : rel * G;
       // Columns past nreal (padding) need no mask: their query rows are zero and their outputs are never written.
       // Only a tile that reaches the window has masked entries; a warp without any scales its logits only.
-      if (__all_sync(0xffffffffu, n_first == 0)) {
+      if (kRawLogits) {
+        // Wide tiles keep the logits unscaled: the scale enters the max test through each column's threshold and
+        // the exponent through one fused multiply-add (two instructions fewer per logit on the softmax path that
+        // bounds them). Narrow tiles measured faster with the scaled form below.
+        if (!__all_sync(0xffffffffu, n_first == 0)) {
 #pragma unroll
-        for (int n = 0; n < NPMAX; ++n) x[n] *= scale2;
+          for (int n = 0; n < NPMAX; ++n)
+            if (n < n_first) x[n] = -INFINITY;
+        }
+#pragma unroll
+        for (int c = 0; c < NPMAX / 16; ++c) {
+          float th[16];
+          load16_shared(thr + c * 16, th);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) over |= x[c * 16 + e] > th[e];
+        }
       } else {
+        if (__all_sync(0xffffffffu, n_first == 0)) {
 #pragma unroll
-        for (int n = 0; n < NPMAX; ++n) x[n] = (n >= n_first) ? x[n] * scale2 : -INFINITY;
-      }
+          for (int n = 0; n < NPMAX; ++n) x[n] *= scale2;
+        } else {
 #pragma unroll
-      for (int c = 0; c < NPMAX / 16; ++c) {
-        float mr[16];
-        load16_shared(m_run + c * 16, mr);
+          for (int n = 0; n < NPMAX; ++n) x[n] = (n >= n_first) ? x[n] * scale2 : -INFINITY;
+        }
 #pragma unroll
-        for (int e = 0; e < 16; ++e) over |= x[c * 16 + e] > mr[e] + kRescaleThreshold;
+        for (int c = 0; c < NPMAX / 16; ++c) {
+          float mr[16];
+          load16_shared(m_run + c * 16, mr);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) over |= x[c * 16 + e] > mr[e] + kRescaleThreshold;
+        }
       }
       // ---- running max: only when some logit of this tile exceeds it by more than 2^8
       const bool rescale = named_or_128(over);
@@ -685,13 +708,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         named_sync_128();
         if (tid < NPMAX) {
+          // the column's largest scaled logit (scaling by a positive factor keeps the order and the maximum)
           const float cm = fmaxf(fmaxf(colmax[tid], colmax[NPMAX + tid]),
-                                 fmaxf(colmax[2 * NPMAX + tid], colmax[3 * NPMAX + tid]));
+                                 fmaxf(colmax[2 * NPMAX + tid], colmax[3 * NPMAX + tid])) *
+                           (kRawLogits ? scale2 : 1.0f);
           const float mo = m_run[tid];
           const float mn = fmaxf(mo, cm);
           alpha_s[b * NPMAX + tid] = (mn == -INFINITY) ? 1.0f : exp2f(mo - mn);
           m_run[tid] = mn;
           m_sub[tid] = (mn == -INFINITY) ? 0.0f : mn;
+          thr[tid] = (mn == -INFINITY) ? -INFINITY : (mn + kRescaleThreshold) * inv_scale2;
         }
         named_sync_128();
         // this thread's running sums follow the raised maxima (the tile's weights are added below)
@@ -715,7 +741,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int ee = 0; ee < 16; ++ee) {
             const int n = cc * 16 + ee;
-            const float pv = fast_exp2(x[n] - mr[ee]);
+            const float pv = kRawLogits ? fast_exp2(fmaf(x[n], scale2, -mr[ee])) : fast_exp2(x[n] - mr[ee]);
             lt[n] += pv;
             *reinterpret_cast<__nv_bfloat16 *>(pd + katom * L::KATOM + (n >> 3) * 1024 + (n & 7) * 128 +
                                               ((c ^ (n & 7)) << 4) + e * 2) = __float2bfloat16_rn(pv);
