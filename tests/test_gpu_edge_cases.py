@@ -42,6 +42,37 @@ def test_short_prompts_and_degenerate_splits(kap, ark):
     assert kap.kap_device_error() == 0
 
 
+def test_short_prompts_in_a_large_batch(kap):
+    """More than 8 requests: the score kernel's CTAs scan the requests' chunk counts and take contiguous item ranges
+    that cross requests. Prompts of 1, 16, 17 and 40 tokens among ragged ones of up to 2K; scores, selections,
+    views and attention against the oracle."""
+    from tests.gpu_helpers import assert_close_attn, run_cycle_and_oracle
+    from workloads import make_workload
+    w = make_workload("mixed", device="cuda", scale=1 / 64, batch=12, ragged=True, poison=True)
+    lens = w.ctx_len.clone()
+    for r, n in ((0, 1), (3, 16), (5, 17), (7, 40)):
+        lens[r] = n
+    w.ctx_len = lens.clone()
+    w.seq_len0 = lens.clone()
+    w.needles = [[] for _ in range(w.R)]
+    res = run_cycle_and_oracle(w)
+    ctx = w.ctx_len.cpu().numpy()
+    for r in range(w.R):   # every prompt page's score, bit for bit
+        N = (int(ctx[r]) + 15) // 16
+        g, o = res["scores_gpu"][r, :, :N], res["scores_orc"][r, :, :N]
+        assert np.array_equal(g.view(np.uint32), o.view(np.uint32)), r
+    assert np.array_equal(res["nsel_gpu"], res["nsel_orc"])
+    for r in range(w.R):
+        for v in range(res["nsel_orc"].shape[1]):
+            n = int(res["nsel_orc"][r, v])
+            assert np.array_equal(res["sel_gpu"][r, v, :n], res["sel_orc"][r, v, :n])
+    for st in res["prop"]:
+        assert_close_attn(st["o_gpu"], st["o_orc"], st["lse_gpu"], st["lse_orc"], w.dtype, "propose")
+    v = res["ver"]
+    assert_close_attn(v["o_gpu"], v["o_orc"], v["lse_gpu"], v["lse_orc"], w.dtype, "verify")
+    assert kap.kap_device_error() == 0
+
+
 def test_bad_page_ids_are_skipped_and_reported(kap):
     from tests.gpu_helpers import make_cycle
     from workloads import make_workload
