@@ -10,11 +10,12 @@
 // Design (GB300):
 //  * Work = the concatenated entry lists of all (request, KV head) rows; CTA b owns the contiguous entry range
 //    [b*E/nb, (b+1)*E/nb) (stream-K, one CTA per SM), so long and short rows balance across the SMs. A row split
-//    over several CTAs is merged by the last CTA to finish it (one atomic counter per row, no waiting).
+//    over several CTAs is merged by the last CTA to finish it (one atomic counter per row, no waiting). A short
+//    launch leaves the grid's last CTAs idle, since they start last, on the SMs the previous kernel frees last.
 //  * A producer warp streams the CTA's entries through a ring of page slots: per entry one 1-D bulk copy
 //    (cp.async.bulk) of the 4 KiB (page, head) chunk of K and one of V, completing on the slot's mbarrier. A view
 //    entry and its row's lengths are loaded together, so a copy leaves two dependent loads after the kernel starts.
-//    The window's entries past the ring's first fill are prefetched into L2 at the same time.
+//    Once the ring's first fill is out, the window's next entries are prefetched into L2.
 //  * The range is cut into windows of at most NSEG row segments. Each segment gets its own group of consumer warps
 //    (one at least, the others in proportion to its entries) that takes the segment's entries round-robin, so all
 //    segments of a window stream at once. The group's first warp prepares the segment's query once (rotated,
@@ -25,6 +26,8 @@
 //    page exceeds it by more than 2^8, which is exact.
 //  * A group that has finished its segment combines its warps' states behind its own named barrier and writes the
 //    row's output, or hands a partial record to the row's last CTA, while the other groups keep streaming.
+//  * With a settled view (lengths and prompt pages older than the previous kernel), the row scan, the segment
+//    tables, the copies of pure prompt pages and the query's rotation angles all run before the dependency wait.
 //  * Fused append: the step token of request r sits at position P = seq_len[r] - 1. The warp that consumes the page
 //    holding P writes the prepared K and V into the pool and patches its shared-memory copy of the page first.
 #include "kap_device.cuh"
