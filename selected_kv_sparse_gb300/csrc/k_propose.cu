@@ -843,33 +843,27 @@ __global__ void __launch_bounds__((Shape<T, D, G>::THREADS)) __maxnreg__((Shape<
       }
       group_sync(bar_id, bar_n);
 
-      // ---- the group combines its warps' states: for each of its elements (head g), a thread forms the max M over
-      // the group's warps, their weights 2^(m_w - M), the weighted sum L and the weighted output, with no further
-      // barrier.
+      // ---- the group combines its warps' states: for each of its elements (head g), the max M over the group's
+      // warps, their weights 2^(m_w - M), the weighted sum L and the weighted output, with no further barrier. The
+      // 32 elements a warp takes at once share their head (D is a multiple of 32), so lane j forms warp j's weight
+      // once and every lane reads the weights by shuffle.
       const int gt = gw * 32 + lane, GT = nw * 32;
       auto combined = [&](int i, int g, float &M, float &Ls) {
-        // every load is issued up front (records past the group's last warp are read at the last warp's index and
-        // weighted out), so that the loads overlap instead of following each other
         const float *rec = comb + sg.w0 * C::REC;
-        float mw[C::NCW], lw[C::NCW], ow[C::NCW];
+        const float *rl = rec + min(lane, nw - 1) * C::REC;
+        const float mj = lane < nw ? rl[G * D + g] : -INFINITY;
+        const float lj = lane < nw ? rl[G * D + G + g] : 0.0f;
+        float ow[C::NCW];  // every load issued up front (past the group's last warp: its record, weighted out)
 #pragma unroll
-        for (int j = 0; j < C::NCW; ++j) {
-          const float *rj = rec + min(j, nw - 1) * C::REC;
-          mw[j] = rj[G * D + g];
-          lw[j] = rj[G * D + G + g];
-          ow[j] = rj[i];
-        }
-        M = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < C::NCW; ++j) M = fmaxf(M, mw[j]);
+        for (int j = 0; j < C::NCW; ++j) ow[j] = rec[min(j, nw - 1) * C::REC + i];
+        M = warp_max(mj);
+        const float wj = (mj == -INFINITY) ? 0.0f : exp2f(mj - M);
+        Ls = warp_sum(lj * wj);
         float acc = 0.0f;
-        Ls = 0.0f;
 #pragma unroll
         for (int j = 0; j < C::NCW; ++j) {
-          const bool live = j < nw && mw[j] != -INFINITY;
-          const float w = exp2f(live ? mw[j] - M : -INFINITY);
-          Ls = live ? fmaf(lw[j], w, Ls) : Ls;
-          acc = live ? fmaf(ow[j], w, acc) : acc;
+          const float w = __shfl_sync(0xffffffffu, wj, j);
+          acc = j < nw ? fmaf(ow[j], w, acc) : acc;
         }
         return acc;
       };
