@@ -906,35 +906,48 @@ __global__ void __launch_bounds__((Shape<T, D, G>::THREADS)) __maxnreg__((Shape<
         group_sync(bar_id, bar_n);
         if (s_last[si]) {
           // Last arriver: merge the partial records of CTAs b_first..b_last. A thread owns 4 consecutive elements of
-          // one head; per chunk of kMergeChunk contributors it issues all its loads (an (m, l) pair and a 16-byte piece
-          // of the partial output per contributor) before using any: one round trip per chunk.
-          for (int i4 = gt; i4 < G * D / 4; i4 += GT) {
+          // one head; the kW = D/4 threads (at most a warp) that share a head form each contributor's weight once
+          // (thread c of the group for contributor c) and read the weights by shuffle. Per chunk of kMergeChunk
+          // contributors every load (an (m, l) pair per thread c, a 16-byte piece of the partial output per
+          // contributor) is issued before any is used: one round trip per chunk.
+          constexpr int kW = (D / 4 < 32) ? D / 4 : 32;
+          static_assert(kMergeChunk <= kW, "one contributor per thread of a head's group");
+          const int sub = lane % kW;
+          // a warp-uniform trip count (whole warps take part in the shuffles); past the last element a lane repeats
+          // the last one and stores nothing
+          for (int i4w = gt - lane; i4w < G * D / 4; i4w += GT) {
+            const bool act = i4w + lane < G * D / 4;
+            const int i4 = act ? i4w + lane : G * D / 4 - 1;
             const int i0 = i4 * 4, g = i0 / D;
             float M = -INFINITY, Ls = 0.0f;
             float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
             for (int b0 = b_first; b0 <= b_last; b0 += kMergeChunk) {
-              float2 ml[kMergeChunk];
               float4 pv[kMergeChunk];
 #pragma unroll
               for (int c = 0; c < kMergeChunk; ++c) {
                 const size_t ps = static_cast<size_t>(min(b0 + c, b_last)) + sg.row;  // clamped: always valid
-                ml[c] = __ldcg(reinterpret_cast<const float2 *>(p.ml) + ps * G + g);
                 pv[c] = __ldcg(reinterpret_cast<const float4 *>(p.part + ps * G * D + i0));
               }
-              float Mc = M;
+              const bool mine = sub < kMergeChunk && b0 + sub <= b_last;  // this thread's contributor exists
+              const size_t pc = static_cast<size_t>(min(b0 + min(sub, kMergeChunk - 1), b_last)) + sg.row;
+              float2 mlc = __ldcg(reinterpret_cast<const float2 *>(p.ml) + pc * G + g);
+              if (!mine) mlc = make_float2(-INFINITY, 0.0f);
+              float Mc = mlc.x;
 #pragma unroll
-              for (int c = 0; c < kMergeChunk; ++c)
-                if (b0 + c <= b_last) Mc = fmaxf(Mc, ml[c].x);
-              if (Mc == -INFINITY) continue;
+              for (int o = kW / 2; o >= 1; o >>= 1) Mc = fmaxf(Mc, __shfl_xor_sync(0xffffffffu, Mc, o, kW));
+              Mc = fmaxf(Mc, M);
+              // with no finite maximum yet everything stays zero: the weights below are 0 and rs is 0
               const float rs = (M == -INFINITY) ? 0.0f : exp2f(M - Mc);
-              Ls *= rs;
+              const float wc = (mlc.x == -INFINITY) ? 0.0f : exp2f(mlc.x - Mc);
+              float lw = mlc.y * wc;
+#pragma unroll
+              for (int o = kW / 2; o >= 1; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o, kW);
+              Ls = fmaf(Ls, rs, lw);
 #pragma unroll
               for (int e = 0; e < 4; ++e) acc[e] *= rs;
 #pragma unroll
               for (int c = 0; c < kMergeChunk; ++c) {
-                if (b0 + c > b_last || ml[c].x == -INFINITY) continue;
-                const float w = exp2f(ml[c].x - Mc);
-                Ls = fmaf(ml[c].y, w, Ls);
+                const float w = __shfl_sync(0xffffffffu, wc, c, kW);
                 acc[0] = fmaf(pv[c].x, w, acc[0]);
                 acc[1] = fmaf(pv[c].y, w, acc[1]);
                 acc[2] = fmaf(pv[c].z, w, acc[2]);
@@ -942,6 +955,7 @@ __global__ void __launch_bounds__((Shape<T, D, G>::THREADS)) __maxnreg__((Shape<
               }
               M = Mc;
             }
+            if (!act) continue;
             const float inv = Ls > 0.0f ? 1.0f / Ls : 0.0f;
             store4<T>(outp + out_base + i0, acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
             if (i0 - g * D == 0) {
