@@ -514,9 +514,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     };
     // Last arriver of a row: merges the partial records of CTAs b_first..b_last and writes the row's output.
     // Thread t owns 16 consecutive head dims of one query column (8 threads per column, 16 columns at a time); for
-    // every chunk of kMergeChunkV contributors it issues all its loads (the (m, l) pair and four 16-byte pieces of
-    // the partial output per contributor) before using any, so a chunk costs one round trip and no barrier. Wide
-    // tiles take fewer contributors per chunk: their running state already holds most of the registers.
+    // every chunk of kMergeChunkV contributors it issues all its loads (four 16-byte pieces of the partial output
+    // per contributor, and one contributor's (m, l) pair) before using any, so a chunk costs one round trip and no
+    // barrier. Wide tiles take fewer contributors per chunk: their running state already holds most of the
+    // registers.
     constexpr int kMergeChunkV = NPMAX <= 16 ? 8 : 4;
     auto merge_row = [&](int row, int b_first, int b_last, int qoff, int nreal) {
       const int h = row - (row / p.hkv) * p.hkv;
@@ -530,31 +531,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e) acc[e] = 0.0f;
         float M = -INFINITY, Ls = 0.0f;
+        // the 8 threads of a column form each contributor's weight once (thread c for contributor c) and read the
+        // weights by shuffle within their group of 8
+        const int sub = tid & 7;
         for (int b0 = 0; b0 < nc; b0 += kMergeChunkV) {
-          float2 ml[kMergeChunkV];
           float4 pv[kMergeChunkV][4];
 #pragma unroll
           for (int c = 0; c < kMergeChunkV; ++c) {
             const size_t sl = static_cast<size_t>(b_first + min(b0 + c, nc - 1) + row);
-            ml[c] = __ldcg(reinterpret_cast<const float2 *>(p.ml) + sl * p.npad_ws + nn);
             const float4 *pp = reinterpret_cast<const float4 *>(p.part + (sl * p.npad_ws + nn) * 128 + d0);
 #pragma unroll
             for (int q = 0; q < 4; ++q) pv[c][q] = __ldcg(pp + q);
           }
-          float Mc = M;
+          const bool mine = sub < kMergeChunkV && b0 + sub < nc;
+          const size_t slc = static_cast<size_t>(b_first + min(b0 + min(sub, kMergeChunkV - 1), nc - 1) + row);
+          float2 mlc = __ldcg(reinterpret_cast<const float2 *>(p.ml) + slc * p.npad_ws + nn);
+          if (!mine) mlc = make_float2(-INFINITY, 0.0f);
+          float Mc = mlc.x;
 #pragma unroll
-          for (int c = 0; c < kMergeChunkV; ++c)
-            if (b0 + c < nc) Mc = fmaxf(Mc, ml[c].x);
-          if (Mc == -INFINITY) continue;
+          for (int o = 4; o >= 1; o >>= 1) Mc = fmaxf(Mc, __shfl_xor_sync(0xffffffffu, Mc, o, 8));
+          Mc = fmaxf(Mc, M);
+          // with no finite maximum yet everything stays zero: the weights are 0 and rs is 0
           const float rs = (M == -INFINITY) ? 0.0f : exp2f(M - Mc);
-          Ls *= rs;
+          const float wc = (mlc.x == -INFINITY) ? 0.0f : exp2f(mlc.x - Mc);
+          float lw = mlc.y * wc;
+#pragma unroll
+          for (int o = 4; o >= 1; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o, 8);
+          Ls = fmaf(Ls, rs, lw);
 #pragma unroll
           for (int e = 0; e < 16; ++e) acc[e] *= rs;
 #pragma unroll
           for (int c = 0; c < kMergeChunkV; ++c) {
-            if (b0 + c >= nc || ml[c].x == -INFINITY) continue;
-            const float w = exp2f(ml[c].x - Mc);
-            Ls = fmaf(ml[c].y, w, Ls);
+            const float w = __shfl_sync(0xffffffffu, wc, c, 8);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               acc[4 * q] = fmaf(pv[c][q].x, w, acc[4 * q]);
